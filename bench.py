@@ -1,0 +1,456 @@
+#!/usr/bin/env python
+"""Benchmark of the fp8 e4m3 KV cache hot path on one GB300 (or N replicas).
+
+One step = one decode step of the 64-sequence full-attention workload
+(64 seqs, 32 q / 4 KV heads, head_dim 128, contexts U[1K, 32K], block 16,
+bf16 relative bias of extent 1,024):
+  kv_amax_calibrate on the step's new K/V tokens   (calibration pass)
+  kv_store_e4m3 of the new tokens                   (quant-on-store)
+  paged_attn_fp8_decode over the whole cache        (fp8 attention)
+`value` is the step's algorithmic HBM bytes / step time (GB/s).  The other
+workloads (varlen prefill, 128K calibrated decode, 1M decode) are measured the
+same way and reported under "extra".
+
+--impl reference times the CPU oracle (float64, plain C) on a bounded sample
+of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "fp8-KV decode attn HBM GB/s (% of ~8 TB/s); prefill fp8 TFLOP/s"
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            m = json.load(f)
+        return {"hbm_gbs": float(m["hbm_gbs"]), "bf16_tflops": float(m["bf16_tflops"]),
+                "bf16_tflops_sustained": float(m.get("bf16_tflops_sustained", m["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas only: no data-path collective)
+# ---------------------------------------------------------------------------
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return rank, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# workloads on the device
+# ---------------------------------------------------------------------------
+class DecodeRun:
+    """A decode workload resident in HBM: cache filled once, then each step
+    calibrates + stores the step's new token per sequence and decodes."""
+
+    def __init__(self, fk, spec, dev, seed=0, scales=(1.0, 1.0, 1.0), calibrate=False):
+        self.fk, self.spec, self.dev = fk, spec, dev
+        inp = workloads.make_decode(spec, device=dev, seed=seed)
+        kv = inp["kv"]
+        self.inp, self.kv = inp, kv
+        sq, sk, sv = scales
+        self.amax = torch.zeros(3, dtype=torch.float32, device=dev)
+        if calibrate:
+            fk.kv_amax_calibrate(kv.k, kv.v, self.amax[0:1], self.amax[1:2], kv.slot_mapping)
+            fk.kv_amax_calibrate(inp["q"], None, self.amax[2:3], None)
+            ak, av, aq = self.amax.cpu().tolist()
+            sk, sv, sq = fk.scale_from_amax(ak), fk.scale_from_amax(av), fk.scale_from_amax(aq)
+        self.scales = (sq, sk, sv)
+        self.cache = fk.KVCache.empty(kv.num_blocks, kv.block_size, spec.Hkv, spec.D, device=dev)
+        fk.kv_store_e4m3(self.cache, kv.k, kv.v, kv.slot_mapping, sk, sv)
+        # the step's new token of each sequence is its last one
+        lens = inp["lens"]
+        last = torch.tensor([s + L - 1 for s, L in zip(kv.tok_start.tolist()[:-1], lens)],
+                            dtype=torch.int64, device=dev)
+        self.k_new = kv.k[last].contiguous()
+        self.v_new = kv.v[last].contiguous()
+        self.slot_new = kv.slot_mapping[last].contiguous()
+        self.q = inp["q"]
+        self.rel = inp["rel"]
+        self.out = torch.empty_like(self.q)
+        B, Hq, D = self.q.shape
+        n = fk.decode_workspace_size(B, Hq, spec.Hkv, D, kv.max_blocks, kv.block_size,
+                                     spec.window, 0)
+        self.ws = torch.empty(n, dtype=torch.uint8, device=dev)
+        self.step_amax = torch.zeros(2, dtype=torch.float32, device=dev)
+        torch.cuda.synchronize()
+        # algorithmic bytes
+        E = 0 if self.rel is None else self.rel.shape[2]
+        kv_bytes = sum(min(L, spec.window) if spec.window else L for L in lens) * spec.Hkv * D * 2
+        self.decode_bytes = kv_bytes + 2 * B * Hq * D * 2 + B * Hq * E * 2
+        nt = B * spec.Hkv * D
+        self.store_bytes = nt * 2 * (2 + 1)     # read bf16 K and V, write e4m3 K and V
+        self.amax_bytes = nt * 2 * 2
+        self.step_bytes = self.decode_bytes + self.store_bytes + self.amax_bytes
+        self.launches_per_step = 4              # amax, store, decode, merge
+
+    def step(self, q=None, k_new=None, v_new=None, slot_new=None, seq_lens=None, out=None):
+        fk, kv = self.fk, self.kv
+        sq, sk, sv = self.scales
+        q = self.q if q is None else q
+        k_new = self.k_new if k_new is None else k_new
+        v_new = self.v_new if v_new is None else v_new
+        slot_new = self.slot_new if slot_new is None else slot_new
+        seq_lens = kv.seq_lens if seq_lens is None else seq_lens
+        out = self.out if out is None else out
+        fk.kv_amax_calibrate(k_new, v_new, self.step_amax[0:1], self.step_amax[1:2], slot_new)
+        fk.kv_store_e4m3(self.cache, k_new, v_new, slot_new, sk, sv)
+        return self.decode(q, seq_lens, out)
+
+    def decode(self, q=None, seq_lens=None, out=None):
+        sq, sk, sv = self.scales
+        return self.fk.paged_attn_fp8_decode(
+            self.cache, self.q if q is None else q, self.kv.block_table,
+            self.kv.seq_lens if seq_lens is None else seq_lens, sq, sk, sv,
+            rel_bias=self.rel, window=self.spec.window, out=self.out if out is None else out,
+            workspace=self.ws)
+
+
+def time_steps(fn, steps, warmup, world):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(steps):
+        fn()
+    e1.record(s)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = e0.elapsed_time(e1) / steps
+    return max_over_ranks(ms, world)
+
+
+def e2e_decode(run, steps, warmup, world):
+    """Same step through the public API from pinned host buffers: per step,
+    copy q / new K / new V / slots / lengths to the device, run, read back out."""
+    host = {
+        "q": run.q.cpu().pin_memory(), "k_new": run.k_new.cpu().pin_memory(),
+        "v_new": run.v_new.cpu().pin_memory(), "slot_new": run.slot_new.cpu().pin_memory(),
+        "seq_lens": run.kv.seq_lens.cpu().pin_memory()}
+    dev = {k: torch.empty_like(v, device=run.dev) for k, v in host.items()}
+    out_h = torch.empty(run.out.shape, dtype=run.out.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+
+    def one():
+        for k in host:
+            dev[k].copy_(host[k], non_blocking=True)
+        o = run.step(**dev)
+        out_h.copy_(o, non_blocking=True)
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+        torch.cuda.current_stream().synchronize()   # the result is on the host each step
+    ms = (time.perf_counter() - t0) * 1e3 / steps
+    ms = max_over_ranks(ms, world)
+    return ms, h2d, d2h
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline (bounded sample)
+# ---------------------------------------------------------------------------
+def oracle_decode_sample(spec, inp, scales, budget_s=15.0):
+    """Time the oracle on whole sequences of the workload (all heads), one
+    after another, until about budget_s of CPU work; returns GB/s over the
+    sample's KV bytes and a description."""
+    import oracle
+    bits = workloads.bf16_bits
+    kv = inp["kv"]
+    sq, sk, sv = scales
+    q = inp["q"]
+    B, Hq, D = q.shape
+    G = Hq // spec.Hkv
+    lens = inp["lens"]
+    starts = kv.tok_start.cpu().tolist()
+    done_bytes, t_total, seqs = 0, 0.0, 0
+    order = list(range(B))
+    for b in order:
+        L = lens[b]
+        L_used = min(L, spec.window) if spec.window else L
+        kb = bits(kv.k[starts[b]:starts[b] + L])
+        vb = bits(kv.v[starts[b]:starts[b] + L])
+        qb = bits(q[b])
+        relb = None if inp["rel"] is None else bits(inp["rel"][b])
+        t0 = time.perf_counter()
+        k8 = oracle.quantize(kb, sk)
+        v8 = oracle.quantize(vb, sv)
+        q8 = oracle.quantize(qb, sq)
+        rows = Hq
+        q_off = np.arange(rows, dtype=np.int64) * D
+        kv_off = (np.arange(rows) // G) * D
+        bias_off = None if relb is None else np.arange(rows, dtype=np.int64) * relb.shape[-1]
+        oracle.attend_rows(D, q8, q_off, k8, v8, kv_off, spec.Hkv * D, [L] * rows,
+                           [L - 1] * rows, 1 / math.sqrt(D), sq, sk, sv, relb, bias_off,
+                           0 if relb is None else relb.shape[-1], spec.window)
+        t_total += time.perf_counter() - t0
+        done_bytes += L_used * spec.Hkv * D * 2
+        seqs += 1
+        if t_total >= budget_s:
+            break
+    return done_bytes / t_total / 1e9, seqs, t_total, oracle.num_threads()
+
+
+# ---------------------------------------------------------------------------
+# secondary workloads
+# ---------------------------------------------------------------------------
+def bench_prefill(fk, dev, steps, warmup, world):
+    spec = workloads.PREFILL_16K
+    inp = workloads.make_prefill(spec, device=dev, seed=0)
+    kv = inp["kv"]
+    cache = fk.KVCache.empty(kv.num_blocks, kv.block_size, spec.Hkv, spec.D, device=dev)
+    q_lens = inp["q_lens"]
+    half = spec.n_seqs // 2
+    groups = []
+    cu = inp["cu_seqlens_q"].tolist()
+    for gi, (lo, hi) in enumerate([(0, half), (half, spec.n_seqs)]):
+        w = spec.windows[gi]
+        cu_g = torch.tensor([c - cu[lo] for c in cu[lo:hi + 1]], dtype=torch.int32, device=dev)
+        groups.append(dict(window=w, q=inp["q"][cu[lo]:cu[hi]], cu=cu_g,
+                           lens=kv.seq_lens[lo:hi].contiguous(),
+                           bt=kv.block_table[lo:hi].contiguous(),
+                           rel=inp["rel"][cu[lo]:cu[hi]],
+                           out=torch.empty_like(inp["q"][cu[lo]:cu[hi]]),
+                           maxq=max(q_lens[lo:hi])))
+    flops = 0
+    for gi, (lo, hi) in enumerate([(0, half), (half, spec.n_seqs)]):
+        w = spec.windows[gi]
+        for L in q_lens[lo:hi]:
+            flops += sum(min(i + 1, w) if w else i + 1 for i in range(L))
+    flops *= 4 * spec.Hq * spec.D
+
+    def step():
+        fk.kv_store_e4m3(cache, kv.k, kv.v, kv.slot_mapping, 1.0, 1.0)
+        for g in groups:
+            fk.attn_fp8_varlen_prefill(cache, g["q"], g["cu"], g["lens"], g["bt"], g["maxq"],
+                                       1.0, 1.0, 1.0, rel_bias=g["rel"], window=g["window"],
+                                       out=g["out"])
+    try:
+        step()
+    except Exception as e:  # noqa: BLE001
+        return {"workload": spec.name, "unavailable": str(e)}
+    ms = time_steps(step, steps, warmup, world)
+    return {"workload": spec.name, "ms_per_step": ms, "tflops": flops / ms / 1e9,
+            "flops_per_step": flops, "tokens": sum(q_lens)}
+
+
+def bench_decode_extra(fk, spec, dev, steps, warmup, world, calibrate=False):
+    run = DecodeRun(fk, spec, dev, calibrate=calibrate)
+    ms = time_steps(run.step, steps, warmup, world)
+    dms = time_steps(run.decode, steps, warmup, world)
+    res = {"workload": spec.name, "ms_per_step": ms, "gbs": run.step_bytes / ms / 1e6,
+           "decode_ms": dms, "decode_gbs": run.decode_bytes / dms / 1e6,
+           "scales": list(run.scales)}
+    del run
+    torch.cuda.empty_cache()
+    return res
+
+
+# ---------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-extra", action="store_true", help="skip the secondary workloads")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    args = ap.parse_args()
+    rank, world = dist_setup(args.gpus)
+    spec = workloads.DECODE_32K
+    cfg = {"workload": spec.name, "seqs": spec.B, "q_heads": spec.Hq, "kv_heads": spec.Hkv,
+           "head_dim": spec.D, "block_size": spec.block_size,
+           "context": "U[%d,%d]" % (spec.ctx_lo, spec.ctx_hi), "rel_extent": spec.rel_extent,
+           "l2": "inputs larger than L2 (~1.1 GB of fp8 KV read per step)",
+           "parallelism": "replicas" if world > 1 else "single"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        # a 4-sequence draw of the same workload recipe (the oracle cannot
+        # hold the whole 64-sequence pool in a few minutes of CPU time)
+        inp = workloads.make_decode(spec, device="cpu", seed=0, B=4)
+        per_step = []
+        desc = None
+        for _ in range(max(1, args.steps)):
+            gbs, seqs, t, cores = oracle_decode_sample(spec, inp, (1.0, 1.0, 1.0),
+                                                       budget_s=max(2.0, 60.0 / max(1, args.steps)))
+            per_step.append(gbs)
+            desc = "%d whole sequences (all 32 q heads) of the workload per step, %.1f s" % (seqs, t)
+        v = statistics.median(per_step)
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
+                "cpu_baseline": {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                 "sample": desc},
+                "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import fp8_e4m3_kv_gb300 as fk
+    dev = torch.device("cuda", torch.cuda.current_device())
+    pk = peaks()
+    run = DecodeRun(fk, spec, dev)
+    # warm-up + timed region (clocks sampled during it)
+    with ClockSampler(dev.index) as clk:
+        ms = time_steps(run.step, args.steps, args.warmup, world)
+        # the dominant kernel's call, timed alone on its stream
+        dms = time_steps(run.decode, args.steps, args.warmup, world)
+    clocks = clk.summary()
+    value = run.step_bytes * world / ms / 1e6          # GB/s over all ranks
+    achieved = run.decode_bytes / dms / 1e6
+    e2e_ms, h2d, d2h = e2e_decode(run, max(3, args.steps // 2), args.warmup, world)
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+            "data": "synthetic", "config": cfg,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
+                         "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": None,
+                         "kernel": "paged_attn_fp8_decode (decode + split merge)",
+                         "peak_source": pk["source"]},
+            "e2e": {"value": run.step_bytes * world / e2e_ms / 1e6, "unit": "GB/s",
+                    "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": run.launches_per_step * args.steps,
+            "clocks": clocks}
+    scales = run.scales
+    inp_cpu = None
+    if rank == 0 and not args.no_cpu:
+        inp_cpu = run.inp
+    del run
+    torch.cuda.empty_cache()
+    if not args.no_extra:
+        extra = []
+        for fn in (lambda: bench_prefill(fk, dev, args.steps, args.warmup, world),
+                   lambda: bench_decode_extra(fk, workloads.DECODE_128K_CAL, dev, args.steps,
+                                              args.warmup, world, calibrate=True),
+                   lambda: bench_decode_extra(fk, workloads.DECODE_1M, dev, args.steps,
+                                              args.warmup, world)):
+            try:
+                extra.append(fn())
+            except Exception as e:  # noqa: BLE001
+                extra.append({"error": repr(e)[:300]})
+            torch.cuda.empty_cache()
+        line["extra"] = extra
+    if rank == 0 and inp_cpu is not None:
+        gbs, seqs, t, cores = oracle_decode_sample(spec, inp_cpu, scales, budget_s=15.0)
+        line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                "sample": "%d whole sequences (all 32 q heads, float64) of the "
+                                          "workload, %.1f s of CPU time" % (seqs, t)}
+    if rank == 0:
+        print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

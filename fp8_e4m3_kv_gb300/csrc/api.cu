@@ -1,0 +1,172 @@
+// api.cu -- host-side parts of libfp8kv shared by every entry point: status
+// text, the scale rules, the device gate, the device error word and the
+// tensor maps over the paged cache.
+#include <math.h>
+#include <string.h>
+
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+
+namespace fp8kv {
+
+// One error word per device (each device that loads the library gets its
+// own copy of this variable).
+__device__ uint32_t g_error_word;
+
+namespace {
+constexpr int kMaxDevices = 64;
+struct DeviceInfo {
+    bool probed = false;
+    fp8kv_status status = FP8KV_ERR_UNSUPPORTED;
+    int num_sms = 0;
+    uint32_t *error_word = nullptr;
+};
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_devices_mu;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
+std::once_flag g_encode_once;
+}  // namespace
+
+static DeviceInfo *current_device_info() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(g_devices_mu);
+    DeviceInfo &d = g_devices[dev];
+    if (!d.probed) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        d.num_sms = sms;
+        // The kernels are built for sm_103a only (GB300).
+        d.status = (major == 10 && minor == 3) ? FP8KV_OK : FP8KV_ERR_UNSUPPORTED;
+        if (d.status == FP8KV_OK) {
+            void *p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) {
+                cudaGetLastError();
+                d.status = FP8KV_ERR_LAUNCH;
+            } else {
+                d.error_word = static_cast<uint32_t *>(p);
+            }
+        }
+        d.probed = true;
+    }
+    return &d;
+}
+
+fp8kv_status check_device(int *num_sms) {
+    DeviceInfo *d = current_device_info();
+    if (!d) return FP8KV_ERR_LAUNCH;
+    if (num_sms) *num_sms = d->num_sms;
+    return d->status;
+}
+
+uint32_t *device_error_word() {
+    DeviceInfo *d = current_device_info();
+    return d ? d->error_word : nullptr;
+}
+
+bool scale_ok(float s) { return isfinite(s) && s > 0.0f; }
+
+bool make_cache_map(CUtensorMap *map, const uint8_t *base, int64_t num_blocks, int block_size,
+                    int num_kv_heads, int head_dim) {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode_tiled = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        else
+            cudaGetLastError();
+    });
+    if (!g_encode_tiled) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)num_kv_heads,
+                                (cuuint64_t)block_size, (cuuint64_t)num_blocks};
+    const cuuint64_t strides[3] = {(cuuint64_t)head_dim, (cuuint64_t)num_kv_heads * head_dim,
+                                   (cuuint64_t)block_size * num_kv_heads * head_dim};
+    const cuuint32_t box[4] = {128u, 1u, (cuuint32_t)block_size, 1u};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    CUresult r = g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<uint8_t *>(base),
+                                dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace fp8kv
+
+extern "C" {
+
+const char *fp8kv_status_string(fp8kv_status s) {
+    switch (s) {
+        case FP8KV_OK: return "ok";
+        case FP8KV_ERR_ARG: return "invalid argument";
+        case FP8KV_ERR_SCALE: return "scale not finite and positive";
+        case FP8KV_ERR_UNSUPPORTED: return "unsupported device or shape";
+        case FP8KV_ERR_WORKSPACE: return "workspace missing or too small";
+        case FP8KV_ERR_LAUNCH: return "CUDA launch or runtime error";
+        case FP8KV_ERR_DEVICE: return "device error word set";
+    }
+    return "unknown status";
+}
+
+fp8kv_status fp8kv_scale_from_amax(float amax, int32_t rule, float *scale) {
+    if (!scale || rule < 0 || rule > 2) return FP8KV_ERR_ARG;
+    if (!(amax >= 0.0f) || !isfinite(amax)) return FP8KV_ERR_SCALE;
+    float s;
+    if (rule == 0) {
+        s = amax / fp8kv::kE4M3Max;
+    } else if (rule == 1) {
+        float t = amax / fp8kv::kE4M3Max;
+        uint32_t u;
+        memcpy(&u, &t, sizeof u);
+        if (u & 0xFFFFu) u = (u & 0xFFFF0000u) + 0x10000u;   // round up to a bf16 value
+        memcpy(&s, &u, sizeof s);
+    } else {
+        double r = static_cast<double>(amax) * 1.3 / 448.0;
+        s = static_cast<float>(r > 1.0 ? r : 1.0);
+    }
+    if (!fp8kv::scale_ok(s)) return FP8KV_ERR_SCALE;
+    *scale = s;
+    return FP8KV_OK;
+}
+
+size_t fp8kv_cache_bytes(int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                         int32_t head_dim) {
+    if (num_blocks < 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0) return 0;
+    return static_cast<size_t>(num_blocks) * block_size * num_kv_heads * head_dim;
+}
+
+fp8kv_status fp8kv_device_error(uint32_t *flags, int32_t clear) {
+    if (!flags) return FP8KV_ERR_ARG;
+    fp8kv_status st = fp8kv::check_device(nullptr);
+    if (st != FP8KV_OK) return st;
+    uint32_t *w = fp8kv::device_error_word();
+    if (!w) return FP8KV_ERR_LAUNCH;
+    if (cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        return FP8KV_ERR_LAUNCH;
+    }
+    if (cudaMemcpy(flags, w, sizeof(uint32_t), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8KV_ERR_LAUNCH;
+    }
+    if (clear && cudaMemset(w, 0, sizeof(uint32_t)) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8KV_ERR_LAUNCH;
+    }
+    return FP8KV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,644 @@
+// attn_decode.cu -- split-KV paged decode attention over the e4m3 cache
+// (vLLM PR 54705 "Purpose": query quantization, descale fold into the
+// softmax scale before the exact bf16 relative bias, v_scale post-multiply;
+// full-causal or sliding-window layers).
+//
+// One CTA handles one (split of the key range, KV head, sequence) and all
+// query heads of that KV head (the GQA group, padded to 16).  The work is
+// streamed in tiles of 128 keys:
+//   warp 4  (producer)  TMA-loads the K and V tiles of the split's blocks
+//                       (one box of block_size rows x 128 bytes per block and
+//                       128-byte column) into a 3-stage ring;
+//   warp 5  (MMA)       one thread issues the tcgen05 FP8 MMAs:
+//                       S^T[key][head] = K_tile . Q8^T             (M=128, N=16)
+//                       O^T[d][head]  = V_tile^T . (P_hi + P_lo)^T  (M=128, N=16)
+//                       into TMEM (S and O double-buffered);
+//   warps 0-3 (softmax) thread t owns key row t of S^T and value row d = t of
+//                       O^T: it applies the folded descale and the bias,
+//                       masks, keeps the running max per head (block-wide
+//                       max through warp shuffles), forms P, and
+//                       accumulates O in registers with the online rescale.
+// P is exp2(z - m + 8) (at most 256) split into two e4m3 terms,
+// P_hi = e4m3(P) and P_lo = e4m3(P - P_hi), so the PV product runs on the FP8
+// tensor cores while the weights keep ~8 significant bits.  The partial
+// (o, m, l) of each split go to the workspace; a second kernel merges the
+// splits with the log-sum-exp rule and writes v_scale * o / l in bf16.
+#include <math.h>
+
+#include "common.cuh"
+
+namespace fp8kv {
+namespace {
+
+constexpr int kDecThreads = 192;   // warps 0-3 softmax, warp 4 producer, warp 5 MMA
+constexpr int kNPad = 16;          // query heads per KV head, padded to the MMA N
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct DecCfg {
+    static constexpr int kCB = D / 128;               // 128-byte column blocks per row
+    static constexpr int kStages = 3;
+    static constexpr int kTileBytes = kTile * D;      // one K (or V) tile
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kQBytes = kNPad * D;         // Q8: 16 rows x D bytes
+    static constexpr int kPBytes = kNPad * kTile;     // one P term: 16 rows x 128 keys
+    static constexpr int kOffQ = kStages * kStageBytes;
+    static constexpr int kOffP = kOffQ + kQBytes;     // [2 buffers][hi, lo]
+    static constexpr int kOffMisc = kOffP + 4 * kPBytes;
+    static constexpr int kMiscBytes = 1024;
+    static constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;   // + alignment slack
+    static constexpr uint32_t kTmemCols = 128;
+    static constexpr uint32_t kColS = 0;              // S^T buffers: cols 0, 16
+    static constexpr uint32_t kColO = 32;             // O^T buffers: 32 + buf*16*kCB + half*16
+};
+
+struct DecodeParams {
+    const uint16_t *q;
+    const int32_t *block_table;
+    const int32_t *seq_lens;
+    const uint16_t *rel;
+    float *part_o;          // [B][Hq][S][D]
+    float *part_ml;         // [B][Hq][S][2]  (running max in log2 units, sum)
+    uint32_t *err;
+    int64_t bias_tok_stride;
+    int64_t num_blocks;
+    int32_t max_blocks;
+    int32_t Hq;
+    int32_t G;
+    int32_t block_size;
+    int32_t rel_extent;
+    int32_t window;
+    int32_t split_tiles;
+    int32_t num_splits;
+    float q_scale;
+    float score_log2;       // softmax_scale * q_scale * k_scale * log2(e)
+};
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Bounded wait that ignores the CTA's abort flag: used only in the teardown
+// to let copies and MMAs that are already in flight finish.
+__device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity, uint32_t *err) {
+    CtaFail never{0};
+    mbar_wait(bar, parity, &never, err);
+}
+
+// Every lane of the warp waits on the barrier (each thread then observes the
+// phase), and the warp agrees on the outcome, so that the .sync.aligned
+// tcgen05 loads that follow never run diverged.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, CtaFail *fail,
+                                          uint32_t *err) {
+    const bool ok = mbar_wait(bar, parity, fail, err);
+    return __all_sync(0xffffffffu, ok);
+}
+
+template <int D, int GMAX>
+__global__ void __launch_bounds__(kDecThreads, D == 128 ? 2 : 1)
+decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+              const DecodeParams p) {
+    using C = DecCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const int h0 = kvh * p.G;
+    const int64_t len = p.seq_lens[b];
+    const int64_t lo = (p.window > 0 && len > p.window) ? len - p.window : 0;
+    const int64_t t0 = lo / kTile + static_cast<int64_t>(split) * p.split_tiles;
+    const int64_t t_end = (len + kTile - 1) / kTile;
+    const int ntiles = static_cast<int>(t_end - t0 < p.split_tiles ? t_end - t0 : p.split_tiles);
+
+    if (ntiles <= 0) {   // nothing to attend in this split: mark it empty
+        if (threadIdx.x < p.G) {
+            float *ml = p.part_ml + ((static_cast<int64_t>(b) * p.Hq + h0 + threadIdx.x) *
+                                         p.num_splits + split) * 2;
+            ml[0] = -INFINITY;
+            ml[1] = 0.0f;
+        }
+        return;
+    }
+
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffMisc);
+    uint64_t *full = bars;          // [3] TMA landed
+    uint64_t *empty = bars + 3;     // [3] stage consumed (MMA commit)
+    uint64_t *s_full = bars + 6;    // [2] S^T in TMEM
+    uint64_t *s_free = bars + 8;    // [2] S^T read by the softmax warps
+    uint64_t *p_full = bars + 10;   // [2] P written to shared memory
+    uint64_t *o_full = bars + 12;   // [2] O^T in TMEM
+    uint64_t *o_free = bars + 14;   // [2] O^T read by the softmax warps
+    uint64_t *mma_done = bars + 16; // teardown: all MMAs complete
+    uint64_t *red_bar = bars + 17;  // [2] the 4 softmax warps' tile maxima are in `red`
+    uint64_t *l_bar = bars + 19;    // the 4 softmax warps' row sums are in `lred`
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc + 160);
+    CtaFail *fail = reinterpret_cast<CtaFail *>(smem + C::kOffMisc + 164);
+    float *red = reinterpret_cast<float *>(smem + C::kOffMisc + 256);   // [2][4][16]
+    float *lred = red + 128;                                             // [4][16]
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_free[i], 4);
+            mbar_init(&p_full[i], 4);
+            mbar_init(&o_full[i], 1);
+            mbar_init(&o_free[i], 4);
+            mbar_init(&red_bar[i], 4);
+        }
+        mbar_init(mma_done, 1);
+        mbar_init(l_bar, 4);
+        fail->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 5) tmem_alloc(tmem_slot, C::kTmemCols);
+    if (warp < 4) {
+        // Q8 = e4m3(q / q_scale) for the group's heads, rows >= G zero;
+        // 128-byte swizzled, K-major (row = head, D bytes per row).
+        uint8_t *q8 = smem + C::kOffQ;
+        for (int e = threadIdx.x * 8; e < kNPad * D; e += 128 * 8) {
+            const int g = e / D, d = e % D;
+            uint2 packed = make_uint2(0u, 0u);
+            if (g < p.G) {
+                const uint4 w = *reinterpret_cast<const uint4 *>(
+                    p.q + (static_cast<int64_t>(b) * p.Hq + h0 + g) * D + d);
+                packed.x = quantize_bf16x2(w.x, p.q_scale) | (quantize_bf16x2(w.y, p.q_scale) << 16);
+                packed.y = quantize_bf16x2(w.z, p.q_scale) | (quantize_bf16x2(w.w, p.q_scale) << 16);
+            }
+            *reinterpret_cast<uint2 *>(q8 + (d / 128) * (kNPad * 128) + sw128_offset(g, d % 128)) =
+                packed;
+        }
+        uint4 *pz = reinterpret_cast<uint4 *>(smem + C::kOffP);
+        for (int i = threadIdx.x; i < 4 * C::kPBytes / 16; i += 128) pz[i] = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+    }
+    if (warp == 4 && lane == 0) {
+        tma_prefetch_map(&kmap);
+        tma_prefetch_map(&vmap);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ producer
+        const uint64_t pol = l2_policy_evict_first();
+        const int nb = kTile / p.block_size;   // blocks per tile (1..8)
+        int last_issued[C::kStages];
+#pragma unroll
+        for (int s = 0; s < C::kStages; ++s) last_issued[s] = -1;
+        for (int i = 0; i < ntiles; ++i) {
+            const int s = i % C::kStages;
+            int32_t phys = static_cast<int32_t>(p.num_blocks);   // out of range: zero fill
+            if (lane < nb) {
+                const int64_t lb = (t0 + i) * nb + lane;
+                if (lb * p.block_size < len && lb < p.max_blocks) {
+                    const int32_t id = __ldg(p.block_table + static_cast<int64_t>(b) * p.max_blocks + lb);
+                    if (id >= 0 && id < p.num_blocks)
+                        phys = id;
+                    else
+                        atomicOr(p.err, FP8KV_DEVERR_BAD_BLOCK);
+                }
+            }
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait(&empty[s], ((i / C::kStages) & 1) ^ 1, fail, p.err);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            if (lane == 0) mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+            __syncwarp();
+            if (lane < nb) {
+                uint8_t *kdst = smem + s * C::kStageBytes + lane * p.block_size * 128;
+                uint8_t *vdst = kdst + C::kTileBytes;
+#pragma unroll
+                for (int cb = 0; cb < C::kCB; ++cb) {
+                    tma_load_4d(kdst + cb * (kTile * 128), &kmap, &full[s], cb * 128, kvh, 0, phys, pol);
+                    tma_load_4d(vdst + cb * (kTile * 128), &vmap, &full[s], cb * 128, kvh, 0, phys, pol);
+                }
+            }
+            last_issued[s] = i;
+        }
+        if (lane == 0 && fail->abort) {   // let copies already issued land
+            for (int s = 0; s < C::kStages; ++s)
+                if (last_issued[s] >= 0) mbar_drain(&full[s], (last_issued[s] / C::kStages) & 1, p.err);
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc_qk = idesc_e4m3_f32(128, kNPad, false, false);
+            const uint32_t idesc_pv = idesc_e4m3_f32(128, kNPad, true, false);
+            const uint32_t q_addr = smem_u32(smem + C::kOffQ);
+            for (int i = 0; i <= ntiles; ++i) {
+                if (i < ntiles) {
+                    const int s = i % C::kStages, sb = i & 1;
+                    if (!mbar_wait(&full[s], (i / C::kStages) & 1, fail, p.err)) break;
+                    if (!mbar_wait(&s_free[sb], ((i >> 1) & 1) ^ 1, fail, p.err)) break;
+                    tc_fence_after_sync();
+                    const uint32_t k_addr = smem_u32(smem + s * C::kStageBytes);
+#pragma unroll
+                    for (int kk = 0; kk < D / 32; ++kk) {
+                        const uint32_t cb = kk / 4, ko = (kk % 4) * 32;
+                        const uint64_t a = sdesc_sw128(k_addr + cb * (kTile * 128) + ko, 16, 1024);
+                        const uint64_t bd = sdesc_sw128(q_addr + cb * (kNPad * 128) + ko, 16, 1024);
+                        mma_e4m3(tmem + C::kColS + sb * kNPad, a, bd, idesc_qk, kk > 0);
+                    }
+                    tc_commit(&s_full[sb]);
+                }
+                if (i >= 1) {
+                    const int j = i - 1, s = j % C::kStages, pb = j & 1;
+                    if (!mbar_wait(&p_full[pb], (j >> 1) & 1, fail, p.err)) break;
+                    if (!mbar_wait(&o_free[pb], ((j >> 1) & 1) ^ 1, fail, p.err)) break;
+                    tc_fence_after_sync();
+                    const uint32_t v_addr = smem_u32(smem + s * C::kStageBytes + C::kTileBytes);
+                    const uint32_t p_addr = smem_u32(smem + C::kOffP + pb * 2 * C::kPBytes);
+#pragma unroll
+                    for (int mh = 0; mh < C::kCB; ++mh) {
+                        const uint32_t dcol = tmem + C::kColO + pb * kNPad * C::kCB + mh * kNPad;
+#pragma unroll
+                        for (int part = 0; part < 2; ++part) {
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk) {
+                                // V tile, MN-major: rows are keys (128 bytes of d each),
+                                // 8-row groups 1024 bytes apart; 32 keys per MMA.
+                                const uint64_t a = sdesc_sw128(
+                                    v_addr + mh * (kTile * 128) + kk * 32 * 128, kTile * 128, 1024);
+                                const uint64_t bd =
+                                    sdesc_sw128(p_addr + part * C::kPBytes + kk * 32, 16, 1024);
+                                mma_e4m3(dcol, a, bd, idesc_pv, (part | kk) != 0);
+                            }
+                        }
+                    }
+                    tc_commit(&o_full[pb]);
+                    tc_commit(&empty[s]);
+                }
+            }
+            tc_commit(mma_done);
+            mbar_drain(mma_done, 0, p.err);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax
+        const int t = threadIdx.x;                       // key row / value row
+        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+        const uint16_t *bias = p.rel ? p.rel + static_cast<int64_t>(b) * p.bias_tok_stride +
+                                           static_cast<int64_t>(h0) * p.rel_extent
+                                     : nullptr;
+        float m_run[GMAX], l_part[GMAX], alpha_prev[GMAX], o_acc[C::kCB][GMAX];
+#pragma unroll
+        for (int g = 0; g < GMAX; ++g) {
+            m_run[g] = -INFINITY;
+            l_part[g] = 0.0f;
+            alpha_prev[g] = 1.0f;
+#pragma unroll
+            for (int mh = 0; mh < C::kCB; ++mh) o_acc[mh][g] = 0.0f;
+        }
+        bool ok = true;
+        // Accumulate O^T of tile j (rescaled by alpha) into the registers.
+        auto take_o = [&](int j, const float *alpha) -> bool {
+            const int pb = j & 1;
+            if (!warp_wait(&o_full[pb], (j >> 1) & 1, fail, p.err)) return false;
+            tc_fence_after_sync();
+#pragma unroll
+            for (int mh = 0; mh < C::kCB; ++mh) {
+                float o[16];
+                tmem_ld_x16(tmem + lane_base + C::kColO + pb * kNPad * C::kCB + mh * kNPad, o);
+#pragma unroll
+                for (int g = 0; g < GMAX; ++g) o_acc[mh][g] = fmaf(o_acc[mh][g], alpha[g], o[g]);
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&o_free[pb]);
+            return true;
+        };
+        for (int i = 0; i < ntiles; ++i) {
+            const int sb = i & 1;
+            if (!warp_wait(&s_full[sb], (i >> 1) & 1, fail, p.err)) { ok = false; break; }
+            tc_fence_after_sync();
+            float sc[16];
+            tmem_ld_x16(tmem + lane_base + C::kColS + sb * kNPad, sc);
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_free[sb]);
+
+            const int64_t j = (t0 + i) * kTile + t;       // key position
+            const bool valid = j < len && j >= lo;
+            const int64_t dist = len - 1 - j;
+            const bool has_bias = bias && valid && dist < p.rel_extent;
+            float z[GMAX];
+#pragma unroll
+            for (int g = 0; g < GMAX; ++g) {
+                float zz = -INFINITY;
+                if (valid && g < p.G) {
+                    zz = sc[g] * p.score_log2;
+                    if (has_bias) zz = fmaf(bf16_bits_to_float(__ldg(bias + g * p.rel_extent + dist)),
+                                            kLog2e, zz);
+                }
+                z[g] = zz;
+            }
+            // block-wide max per head: warp shuffles, then the 4 warps via
+            // shared memory and a (bounded) mbarrier exchange
+            float *rb = red + (i & 1) * 64;
+#pragma unroll
+            for (int g = 0; g < GMAX; ++g) {
+                const float mx = warp_max(z[g]);
+                if (lane == 0) rb[warp * 16 + g] = mx;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&red_bar[i & 1]);
+            if (!warp_wait(&red_bar[i & 1], (i >> 1) & 1, fail, p.err)) { ok = false; break; }
+            float alpha[GMAX];
+            uint8_t *phi = smem + C::kOffP + sb * 2 * C::kPBytes;
+            uint8_t *plo = phi + C::kPBytes;
+#pragma unroll
+            for (int g = 0; g < GMAX; ++g) {
+                const float tile_max =
+                    fmaxf(fmaxf(rb[g], rb[16 + g]), fmaxf(rb[32 + g], rb[48 + g]));
+                const float m_new = fmaxf(m_run[g], tile_max);
+                alpha[g] = (m_new == -INFINITY) ? 1.0f : exp2f(m_run[g] - m_new);
+                const float pv = (z[g] == -INFINITY) ? 0.0f : exp2f(z[g] - m_new + 8.0f);
+                // two-term e4m3 split of P: hi = e4m3(P), lo = e4m3(P - hi)
+                const uint16_t hi2 = f32x2_to_e4m3x2(pv, 0.0f);
+                const float hi_val = __low2float(e4m3x2_to_half2(hi2));
+                const uint16_t lo2 = f32x2_to_e4m3x2(pv - hi_val, 0.0f);
+                l_part[g] = fmaf(l_part[g], alpha[g], pv);
+                m_run[g] = m_new;
+                const uint32_t off = sw128_offset(g, t);
+                phi[off] = static_cast<uint8_t>(hi2 & 0xFF);
+                plo[off] = static_cast<uint8_t>(lo2 & 0xFF);
+            }
+            // Keys past the sequence end may hold stale bytes (NaN codes
+            // included); zero their V rows so that 0 * V stays 0 in the MMA.
+            if (j >= len) {
+                uint8_t *vrow = smem + (i % C::kStages) * C::kStageBytes + C::kTileBytes;
+#pragma unroll
+                for (int cb = 0; cb < C::kCB; ++cb) {
+                    uint4 *r = reinterpret_cast<uint4 *>(vrow + cb * (kTile * 128) + t * 128);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) r[c] = make_uint4(0, 0, 0, 0);
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_full[sb]);
+            if (i >= 1 && !take_o(i - 1, alpha_prev)) { ok = false; break; }
+#pragma unroll
+            for (int g = 0; g < GMAX; ++g) alpha_prev[g] = alpha[g];
+        }
+        if (ok) ok = take_o(ntiles - 1, alpha_prev);
+
+        // l per head: sum of the thread partials
+#pragma unroll
+        for (int g = 0; g < GMAX; ++g) {
+            const float s = warp_sum(l_part[g]);
+            if (lane == 0) lred[warp * 16 + g] = s;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(l_bar);
+        if (!warp_wait(l_bar, 0, fail, p.err)) ok = false;
+        const int64_t row0 = (static_cast<int64_t>(b) * p.Hq + h0) * p.num_splits + split;
+        if (t == 0) {
+#pragma unroll
+            for (int g = 0; g < GMAX; ++g) {
+                if (g < p.G) {
+                    float *ml = p.part_ml + (row0 + static_cast<int64_t>(g) * p.num_splits) * 2;
+                    ml[0] = ok ? m_run[g] : -INFINITY;
+                    ml[1] = lred[g] + lred[16 + g] + lred[32 + g] + lred[48 + g];
+                }
+            }
+        }
+#pragma unroll
+        for (int g = 0; g < GMAX; ++g) {
+            if (g < p.G) {
+                float *po = p.part_o + (row0 + static_cast<int64_t>(g) * p.num_splits) * D;
+#pragma unroll
+                for (int mh = 0; mh < C::kCB; ++mh) po[mh * 128 + t] = o_acc[mh][g];
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+// Merge the splits of one (sequence, query head): m = max m_s,
+// l = sum l_s 2^(m_s - m), o = sum o_s 2^(m_s - m); out = v_scale * o / l.
+template <int D>
+__global__ void __launch_bounds__(128)
+decode_merge_kernel(const float *__restrict__ part_o, const float *__restrict__ part_ml,
+                    uint16_t *__restrict__ out, int32_t Hq, int32_t S, float v_scale) {
+    __shared__ float red[4];
+    const int h = blockIdx.x, b = blockIdx.y;
+    const int64_t row = static_cast<int64_t>(b) * Hq + h;
+    const float *ml = part_ml + row * S * 2;
+    float m = -INFINITY;
+    for (int s = threadIdx.x; s < S; s += 128) m = fmaxf(m, ml[2 * s]);
+    m = warp_max(m);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    m = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    constexpr int kPer = D / 128;
+    float acc[kPer];
+#pragma unroll
+    for (int c = 0; c < kPer; ++c) acc[c] = 0.0f;
+    float l = 0.0f;
+    if (m != -INFINITY) {
+        for (int s = 0; s < S; ++s) {
+            const float ms = ml[2 * s];
+            if (ms == -INFINITY) continue;
+            const float w = exp2f(ms - m);
+            l = fmaf(ml[2 * s + 1], w, l);
+            const float *po = part_o + (row * S + s) * D;
+#pragma unroll
+            for (int c = 0; c < kPer; ++c) acc[c] = fmaf(po[c * 128 + threadIdx.x], w, acc[c]);
+        }
+    }
+    const float f = l > 0.0f ? v_scale / l : 0.0f;
+    uint16_t *o = out + row * D;
+#pragma unroll
+    for (int c = 0; c < kPer; ++c)
+        o[c * 128 + threadIdx.x] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[c] * f));
+}
+
+struct SplitPlan {
+    int num_splits;
+    int split_tiles;
+};
+
+// Split plan: enough CTAs for ~8 waves of the resident CTAs, at least 4 tiles
+// (512 keys) per split, all splits of equal length in tiles.
+bool plan_splits(int32_t num_seqs, int32_t num_kv_heads, int32_t head_dim,
+                 int32_t max_blocks_per_seq, int32_t block_size, int32_t window,
+                 int32_t split_tokens, int num_sms, SplitPlan *plan) {
+    const int64_t max_len = static_cast<int64_t>(max_blocks_per_seq) * block_size;
+    int64_t tiles = (max_len + kTile - 1) / kTile;
+    if (window > 0) {
+        const int64_t wt = (static_cast<int64_t>(window) - 1) / kTile + 2;
+        if (wt < tiles) tiles = wt;
+    }
+    if (tiles < 1) tiles = 1;
+    int64_t st;
+    if (split_tokens > 0) {
+        if (split_tokens % kTile) return false;
+        st = split_tokens / kTile;
+    } else {
+        const int64_t ctas_per_sm = head_dim == 128 ? 2 : 1;
+        const int64_t target = static_cast<int64_t>(num_sms) * ctas_per_sm * 8;
+        int64_t pairs = static_cast<int64_t>(num_seqs) * num_kv_heads;
+        if (pairs < 1) pairs = 1;
+        const int64_t want = (target + pairs - 1) / pairs;
+        st = (tiles + want - 1) / want;
+        if (st < 4) st = 4;
+    }
+    const int64_t S = (tiles + st - 1) / st;
+    if (S > (1 << 20) || st > (1 << 24)) return false;
+    plan->num_splits = static_cast<int>(S);
+    plan->split_tiles = static_cast<int>(st);
+    return true;
+}
+
+size_t workspace_bytes_for(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim, int S) {
+    return static_cast<size_t>(num_seqs) * num_q_heads * S * (head_dim + 2) * sizeof(float);
+}
+
+template <int D, int GMAX>
+fp8kv_status launch_decode(const CUtensorMap &km, const CUtensorMap &vm, const DecodeParams &p,
+                           int num_kv_heads, int num_seqs, cudaStream_t stream) {
+    using C = DecCfg<D>;
+    auto kern = decode_kernel<D, GMAX>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return FP8KV_ERR_LAUNCH;
+    }
+    dim3 grid(p.num_splits, num_kv_heads, num_seqs);
+    kern<<<grid, kDecThreads, C::kSmemBytes, stream>>>(km, vm, p);
+    if (cudaGetLastError() != cudaSuccess) return FP8KV_ERR_LAUNCH;
+    return FP8KV_OK;
+}
+
+}  // namespace
+}  // namespace fp8kv
+
+using namespace fp8kv;
+
+extern "C" size_t fp8kv_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads,
+                                              int32_t num_kv_heads, int32_t head_dim,
+                                              int32_t max_blocks_per_seq, int32_t block_size,
+                                              int32_t window, int32_t split_tokens) {
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_blocks_per_seq <= 0 ||
+        block_size <= 0 || window < 0 || split_tokens < 0 || (head_dim != 128 && head_dim != 256))
+        return 0;
+    int sms = 0;
+    if (split_tokens == 0 && check_device(&sms) != FP8KV_OK) return 0;
+    SplitPlan plan;
+    if (!plan_splits(num_seqs, num_kv_heads, head_dim, max_blocks_per_seq, block_size, window,
+                     split_tokens, sms, &plan))
+        return 0;
+    return workspace_bytes_for(num_seqs, num_q_heads, head_dim, plan.num_splits);
+}
+
+extern "C" fp8kv_status paged_attn_fp8_decode_ex(
+    const fp8kv_cache *cache, const fp8kv_bf16 *q, int32_t num_q_heads, const int32_t *block_table,
+    int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t num_seqs, float q_scale,
+    float k_scale, float v_scale, float softmax_scale, const fp8kv_bf16 *rel_bias,
+    int64_t bias_tok_stride, int32_t rel_extent, int32_t window, fp8kv_bf16 *out, void *workspace,
+    size_t workspace_bytes, int32_t split_tokens, void *stream) {
+    if (!cache || num_seqs < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || window < 0 ||
+        split_tokens < 0)
+        return FP8KV_ERR_ARG;
+    if (!scale_ok(q_scale) || !scale_ok(k_scale) || !scale_ok(v_scale) || !scale_ok(softmax_scale))
+        return FP8KV_ERR_SCALE;
+    const int D = cache->head_dim, bs = cache->block_size, Hkv = cache->num_kv_heads;
+    if (Hkv <= 0 || cache->num_blocks < 0 || num_q_heads % Hkv != 0) return FP8KV_ERR_ARG;
+    const int G = num_q_heads / Hkv;
+    if ((D != 128 && D != 256) || G > kNPad || (bs != 16 && bs != 32 && bs != 64 && bs != 128) ||
+        num_seqs > 65535 || Hkv > 65535 || num_q_heads > 65535 || cache->num_blocks >= (1ll << 31))
+        return FP8KV_ERR_UNSUPPORTED;
+    if (rel_bias && (rel_extent <= 0 || bias_tok_stride < 0)) return FP8KV_ERR_ARG;
+    if (split_tokens % kTile) return FP8KV_ERR_ARG;
+    if (num_seqs == 0) return FP8KV_OK;
+    if (!q || !block_table || !seq_lens || !out || !cache->k || !cache->v) return FP8KV_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(cache->k) & 15) ||
+        (reinterpret_cast<uintptr_t>(cache->v) & 15) || (reinterpret_cast<uintptr_t>(out) & 1))
+        return FP8KV_ERR_ARG;
+    int sms = 0;
+    fp8kv_status st = check_device(&sms);
+    if (st != FP8KV_OK) return st;
+    SplitPlan plan;
+    if (!plan_splits(num_seqs, Hkv, D, max_blocks_per_seq, bs, window, split_tokens, sms, &plan))
+        return FP8KV_ERR_ARG;
+    const size_t need = workspace_bytes_for(num_seqs, num_q_heads, D, plan.num_splits);
+    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 15))
+        return FP8KV_ERR_WORKSPACE;
+    CUtensorMap km, vm;
+    if (!make_cache_map(&km, cache->k, cache->num_blocks, bs, Hkv, D) ||
+        !make_cache_map(&vm, cache->v, cache->num_blocks, bs, Hkv, D))
+        return FP8KV_ERR_LAUNCH;
+
+    DecodeParams p;
+    p.q = q;
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.rel = rel_bias;
+    p.part_o = static_cast<float *>(workspace);
+    p.part_ml = p.part_o + static_cast<size_t>(num_seqs) * num_q_heads * plan.num_splits * D;
+    p.err = device_error_word();
+    p.bias_tok_stride = bias_tok_stride;
+    p.num_blocks = cache->num_blocks;
+    p.max_blocks = max_blocks_per_seq;
+    p.Hq = num_q_heads;
+    p.G = G;
+    p.block_size = bs;
+    p.rel_extent = rel_bias ? rel_extent : 0;
+    p.window = window;
+    p.split_tiles = plan.split_tiles;
+    p.num_splits = plan.num_splits;
+    p.q_scale = q_scale;
+    p.score_log2 = static_cast<float>(static_cast<double>(softmax_scale) * q_scale * k_scale *
+                                      1.4426950408889634);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (D == 128)
+        st = G <= 8 ? launch_decode<128, 8>(km, vm, p, Hkv, num_seqs, s)
+                    : launch_decode<128, 16>(km, vm, p, Hkv, num_seqs, s);
+    else
+        st = G <= 8 ? launch_decode<256, 8>(km, vm, p, Hkv, num_seqs, s)
+                    : launch_decode<256, 16>(km, vm, p, Hkv, num_seqs, s);
+    if (st != FP8KV_OK) return st;
+    if (D == 128)
+        decode_merge_kernel<128><<<dim3(num_q_heads, num_seqs), 128, 0, s>>>(
+            p.part_o, p.part_ml, out, num_q_heads, plan.num_splits, v_scale);
+    else
+        decode_merge_kernel<256><<<dim3(num_q_heads, num_seqs), 128, 0, s>>>(
+            p.part_o, p.part_ml, out, num_q_heads, plan.num_splits, v_scale);
+    if (cudaGetLastError() != cudaSuccess) return FP8KV_ERR_LAUNCH;
+    return FP8KV_OK;
+}
+
+extern "C" fp8kv_status paged_attn_fp8_decode(
+    const fp8kv_cache *cache, const fp8kv_bf16 *q, int32_t num_q_heads, const int32_t *block_table,
+    int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t num_seqs, float q_scale,
+    float k_scale, float v_scale, float softmax_scale, const fp8kv_bf16 *rel_bias,
+    int64_t bias_tok_stride, int32_t rel_extent, int32_t window, fp8kv_bf16 *out, void *workspace,
+    size_t workspace_bytes, void *stream) {
+    return paged_attn_fp8_decode_ex(cache, q, num_q_heads, block_table, max_blocks_per_seq,
+                                    seq_lens, num_seqs, q_scale, k_scale, v_scale, softmax_scale,
+                                    rel_bias, bias_tok_stride, rel_extent, window, out, workspace,
+                                    workspace_bytes, 0, stream);
+}

@@ -1,0 +1,178 @@
+// kv_store.cu -- quant-on-store of bf16 K/V into the e4m3 paged cache and the
+// amax calibration pass (vLLM PR 54705 "Purpose", quant-on-store;
+// Qwen3.8-27B-FP8-KVcal "What it fixes", amax/448 at the cache-write point).
+//
+// Both kernels are HBM-bound streams: each thread owns 16 consecutive
+// elements of one token row (two 16-byte bf16 loads), so a warp reads 1 KiB
+// of one or two rows contiguously; the store writes one 16-byte e4m3 vector
+// per K and per V.  Grids are a multiple of the SM count and grid-stride.
+#include "common.cuh"
+
+namespace fp8kv {
+namespace {
+
+constexpr int kStoreThreads = 256;
+constexpr int kChunk = 16;   // elements per thread-step
+
+// 16 bf16 elements -> 16 e4m3 bytes (quantize_bf16x2: IEEE fp32 x / s,
+// clamp to +-448 keeping NaN, nearest-even saturating conversion, sign kept).
+__device__ __forceinline__ uint4 quantize16(const uint4 lo, const uint4 hi, float s) {
+    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    uint32_t out[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        out[i] = quantize_bf16x2(w[2 * i], s) | (quantize_bf16x2(w[2 * i + 1], s) << 16);
+    return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+__global__ void __launch_bounds__(kStoreThreads)
+kv_store_kernel(const uint16_t *__restrict__ k, const uint16_t *__restrict__ v, int64_t k_stride,
+                int64_t v_stride, const int64_t *__restrict__ slots, int64_t num_tokens,
+                int32_t row_elems, int64_t capacity, uint8_t *__restrict__ ck,
+                uint8_t *__restrict__ cv, float k_scale, float v_scale, uint32_t *err) {
+    const int32_t chunks = row_elems / kChunk;
+    const int64_t total = num_tokens * chunks;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t t = i / chunks;
+        const int32_t c = static_cast<int32_t>(i - t * chunks);
+        const int64_t slot = __ldg(slots + t);
+        if (slot < 0) continue;
+        if (slot >= capacity) {
+            atomicOr(err, FP8KV_DEVERR_BAD_SLOT);
+            continue;
+        }
+        const uint4 *ks = reinterpret_cast<const uint4 *>(k + t * k_stride + c * kChunk);
+        const uint4 *vs = reinterpret_cast<const uint4 *>(v + t * v_stride + c * kChunk);
+        const uint4 k0 = __ldcs(ks), k1 = __ldcs(ks + 1);
+        const uint4 v0 = __ldcs(vs), v1 = __ldcs(vs + 1);
+        const int64_t dst = slot * row_elems + c * kChunk;
+        *reinterpret_cast<uint4 *>(ck + dst) = quantize16(k0, k1, k_scale);
+        *reinterpret_cast<uint4 *>(cv + dst) = quantize16(v0, v1, v_scale);
+    }
+}
+
+__device__ __forceinline__ float absmax16(const uint4 lo, const uint4 hi, float m) {
+    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        // fmaxf ignores NaN operands, so NaN elements never win.
+        m = fmaxf(m, fabsf(__uint_as_float(w[i] << 16)));
+        m = fmaxf(m, fabsf(__uint_as_float(w[i] & 0xFFFF0000u)));
+    }
+    return m;
+}
+
+__device__ __forceinline__ float block_max(float m, float *red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    m = (threadIdx.x < blockDim.x / 32) ? red[threadIdx.x] : 0.0f;
+    if (warp == 0)
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    return m;
+}
+
+__global__ void __launch_bounds__(kStoreThreads)
+kv_amax_kernel(const uint16_t *__restrict__ k, const uint16_t *__restrict__ v, int64_t k_stride,
+               int64_t v_stride, const int64_t *__restrict__ slots, int64_t num_tokens,
+               int32_t row_elems, float *amax_k, float *amax_v) {
+    __shared__ float red[2][kStoreThreads / 32];
+    const int32_t chunks = row_elems / kChunk;
+    const int64_t total = num_tokens * chunks;
+    float mk = 0.0f, mv = 0.0f;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t t = i / chunks;
+        const int32_t c = static_cast<int32_t>(i - t * chunks);
+        if (slots && __ldg(slots + t) < 0) continue;
+        if (k) {
+            const uint4 *p = reinterpret_cast<const uint4 *>(k + t * k_stride + c * kChunk);
+            mk = absmax16(__ldcs(p), __ldcs(p + 1), mk);
+        }
+        if (v) {
+            const uint4 *p = reinterpret_cast<const uint4 *>(v + t * v_stride + c * kChunk);
+            mv = absmax16(__ldcs(p), __ldcs(p + 1), mv);
+        }
+    }
+    mk = block_max(mk, red[0]);
+    mv = block_max(mv, red[1]);
+    // Non-negative floats order like their bit patterns.
+    if (threadIdx.x == 0) {
+        if (k) atomicMax(reinterpret_cast<unsigned int *>(amax_k), __float_as_uint(mk));
+        if (v) atomicMax(reinterpret_cast<unsigned int *>(amax_v), __float_as_uint(mv));
+    }
+}
+
+int grid_for(int64_t work_items, int num_sms) {
+    int64_t blocks = (work_items + kStoreThreads - 1) / kStoreThreads;
+    const int64_t cap = static_cast<int64_t>(num_sms) * 8;   // 8 resident CTAs per SM
+    if (blocks > cap) blocks = cap;
+    return static_cast<int>(blocks < 1 ? 1 : blocks);
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+}  // namespace fp8kv
+
+using namespace fp8kv;
+
+extern "C" fp8kv_status kv_store_e4m3(const fp8kv_cache *cache, const fp8kv_bf16 *k,
+                                      const fp8kv_bf16 *v, int64_t k_tok_stride,
+                                      int64_t v_tok_stride, const int64_t *slot_mapping,
+                                      int64_t num_tokens, float k_scale, float v_scale,
+                                      void *stream) {
+    if (!cache || num_tokens < 0) return FP8KV_ERR_ARG;
+    if (!scale_ok(k_scale) || !scale_ok(v_scale)) return FP8KV_ERR_SCALE;
+    if (cache->num_blocks < 0 || cache->block_size <= 0 || cache->num_kv_heads <= 0 ||
+        cache->head_dim <= 0)
+        return FP8KV_ERR_ARG;
+    const int64_t row = static_cast<int64_t>(cache->num_kv_heads) * cache->head_dim;
+    if (row % kChunk != 0 || row > (1 << 30)) return FP8KV_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return FP8KV_OK;
+    if (!cache->k || !cache->v || !k || !v || !slot_mapping) return FP8KV_ERR_ARG;
+    if (k_tok_stride < row || v_tok_stride < row || (k_tok_stride % 8) || (v_tok_stride % 8))
+        return FP8KV_ERR_ARG;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(cache->k) || !aligned16(cache->v))
+        return FP8KV_ERR_ARG;
+    int sms = 0;
+    fp8kv_status st = check_device(&sms);
+    if (st != FP8KV_OK) return st;
+    uint32_t *err = device_error_word();
+    const int64_t capacity = cache->num_blocks * cache->block_size;
+    const int grid = grid_for(num_tokens * (row / kChunk), sms);
+    kv_store_kernel<<<grid, kStoreThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        k, v, k_tok_stride, v_tok_stride, slot_mapping, num_tokens, static_cast<int32_t>(row),
+        capacity, cache->k, cache->v, k_scale, v_scale, err);
+    if (cudaGetLastError() != cudaSuccess) return FP8KV_ERR_LAUNCH;
+    return FP8KV_OK;
+}
+
+extern "C" fp8kv_status kv_amax_calibrate(const fp8kv_bf16 *k, const fp8kv_bf16 *v,
+                                          int64_t k_tok_stride, int64_t v_tok_stride,
+                                          const int64_t *slot_mapping, int64_t num_tokens,
+                                          int32_t num_kv_heads, int32_t head_dim,
+                                          float *amax_k_inout, float *amax_v_inout,
+                                          void *stream) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0) return FP8KV_ERR_ARG;
+    const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+    if (row % kChunk != 0 || row > (1 << 30)) return FP8KV_ERR_UNSUPPORTED;
+    if (k && (!amax_k_inout || k_tok_stride < row || (k_tok_stride % 8) || !aligned16(k)))
+        return FP8KV_ERR_ARG;
+    if (v && (!amax_v_inout || v_tok_stride < row || (v_tok_stride % 8) || !aligned16(v)))
+        return FP8KV_ERR_ARG;
+    if (num_tokens == 0 || (!k && !v)) return FP8KV_OK;
+    int sms = 0;
+    fp8kv_status st = check_device(&sms);
+    if (st != FP8KV_OK) return st;
+    const int grid = grid_for(num_tokens * (row / kChunk), sms);
+    kv_amax_kernel<<<grid, kStoreThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        k, v, k_tok_stride, v_tok_stride, slot_mapping, num_tokens, static_cast<int32_t>(row),
+        amax_k_inout, amax_v_inout);
+    if (cudaGetLastError() != cudaSuccess) return FP8KV_ERR_LAUNCH;
+    return FP8KV_OK;
+}

@@ -1,0 +1,234 @@
+/*
+ * fp8kv.h -- C ABI of libfp8kv: an FP8 e4m3 paged KV cache and attention
+ * over it, as hand-written CUDA kernels for one NVIDIA GB300 (sm_103).
+ *
+ * The method is the one of vLLM pull request 54705 ("fp8 e4m3 KV cache for
+ * Inkling on SM100"), section "Purpose":
+ *   - quant-on-store: K and V are divided by a per-tensor scale, clamped to
+ *     the e4m3 finite range +-448 and stored as e4m3 bytes in a paged cache;
+ *   - query quantization: q is statically quantized to e4m3 with q_scale;
+ *   - descale handling: the QK descale is folded into softmax_scale
+ *     (softmax_scale * q_scale * k_scale), the scores are descaled before an
+ *     exact bf16 relative-position bias is added, and the output is
+ *     multiplied by v_scale;
+ *   - full-causal or 512-token sliding-window attention layers.
+ * Scale calibration (amax/448) follows the model card "Qwen3.8-27B-FP8-KVcal",
+ * section "What it fixes".
+ *
+ * Conventions for every call:
+ *   - Pointers marked "device" are CUDA device pointers on the current
+ *     device; the caller owns all memory, including workspaces.  The library
+ *     never allocates device memory and never synchronizes the stream.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *     are asynchronous on it.
+ *   - bf16 data is passed as raw 16-bit patterns (fp8kv_bf16).
+ *   - Scales are host floats, passed by value; they must be finite and > 0
+ *     (vLLM PR 54705 "Purpose": loaded scales are validated finite and
+ *     positive; scalar descales stay on the host so the hot path never syncs
+ *     on a GPU scalar).
+ *   - Errors are returned as fp8kv_status; nothing aborts or throws.
+ *     Arguments are checked on the host before any CUDA call.  A kernel that
+ *     meets an inconsistency it can detect (a bounded wait that ran out, a
+ *     block id outside the pool) records a bit in a device error word, skips
+ *     the faulty access and finishes; fp8kv_device_error() reads the word.
+ *   - Only e4m3 (OCP "e4m3fn", max 448) is supported; the gate of vLLM PR
+ *     54705 ("Purpose", first bullet) rejects other fp8 variants and other
+ *     devices, and so does this library (FP8KV_ERR_UNSUPPORTED when the
+ *     device is not compute capability 10.3).
+ *
+ * Cache layout (fp8kv_cache): two byte arrays, K and V, each
+ *   uint8[num_blocks][block_size][num_kv_heads][head_dim]  (row-major),
+ * every byte an e4m3 code.  Token slot s lives in block s / block_size, row
+ * s % block_size.  A sequence's keys are listed by its block-table row:
+ * logical block i of sequence b is physical block block_table[b][i].
+ * Supported: block_size in {16, 32, 64, 128}, head_dim in {128, 256}.
+ */
+#ifndef FP8KV_H
+#define FP8KV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FP8KV_OK = 0,
+    FP8KV_ERR_ARG = 1,          /* null pointer, negative size, bad stride or shape  */
+    FP8KV_ERR_SCALE = 2,        /* a scale that is not finite and > 0                 */
+    FP8KV_ERR_UNSUPPORTED = 3,  /* device not sm_103, head_dim / block size / GQA     */
+    FP8KV_ERR_WORKSPACE = 4,    /* workspace missing or smaller than required        */
+    FP8KV_ERR_LAUNCH = 5,       /* a CUDA runtime call or kernel launch failed       */
+    FP8KV_ERR_DEVICE = 6        /* the device error word is set (see below)          */
+} fp8kv_status;
+
+typedef uint16_t fp8kv_bf16;    /* raw bfloat16 bit pattern */
+
+/* Device error word bits (fp8kv_device_error). */
+#define FP8KV_DEVERR_WAIT_TIMEOUT 0x1u   /* a bounded pipeline wait ran out       */
+#define FP8KV_DEVERR_BAD_BLOCK    0x2u   /* a block id outside [0, num_blocks)     */
+#define FP8KV_DEVERR_BAD_SLOT     0x4u   /* a slot outside the pool                */
+
+typedef struct {
+    uint8_t *k;            /* device, num_blocks*block_size*num_kv_heads*head_dim bytes */
+    uint8_t *v;            /* device, same size as k                                    */
+    int64_t num_blocks;
+    int32_t block_size;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+} fp8kv_cache;
+
+/*
+ * kv_store_e4m3 -- quantize bf16 K and V and scatter them into the cache
+ * (vLLM PR 54705 "Purpose", quant-on-store).
+ *   byte = e4m3_rn_sat( fp32(x) / scale )   -- IEEE fp32 division, clamp to
+ *   +-448 (NaN stays NaN, +-Inf saturates), round to nearest even.
+ * k, v:        device bf16, token t's row of num_kv_heads*head_dim elements
+ *              starts at k + t*k_tok_stride (v + t*v_tok_stride); rows must be
+ *              contiguous, strides are in elements and multiples of 8.
+ * slot_mapping: device int64 [num_tokens]; slot < 0 skips the token; a slot
+ *              >= num_blocks*block_size is skipped and sets
+ *              FP8KV_DEVERR_BAD_SLOT.
+ * num_tokens:  >= 0 (0 is a no-op).
+ */
+fp8kv_status kv_store_e4m3(const fp8kv_cache *cache, const fp8kv_bf16 *k,
+                           const fp8kv_bf16 *v, int64_t k_tok_stride,
+                           int64_t v_tok_stride, const int64_t *slot_mapping,
+                           int64_t num_tokens, float k_scale, float v_scale,
+                           void *stream);
+
+/*
+ * paged_attn_fp8_decode -- one query token per sequence attends over its
+ * cached keys (vLLM PR 54705 "Purpose", descale handling and query
+ * quantization), split over the KV length with a log-sum-exp merge.
+ *   q8    = e4m3_rn_sat(q / q_scale)
+ *   z_j   = (softmax_scale*q_scale*k_scale) * <q8, k8_j> + bias(j)
+ *   out   = bf16( v_scale * sum_j softmax(z)_j * v8_j )
+ * q:            device bf16 [num_seqs][num_q_heads][head_dim], contiguous.
+ * num_q_heads:  a multiple of num_kv_heads with at most 16 query heads per KV
+ *               head (q head h reads KV head h / (num_q_heads/num_kv_heads)).
+ * block_table:  device int32 [num_seqs][max_blocks_per_seq].
+ * seq_lens:     device int32 [num_seqs], keys per sequence,
+ *               0 <= len <= max_blocks_per_seq*block_size.  The query sits at
+ *               position len-1 (it is the newest stored token).  len = 0
+ *               yields zeros.
+ * rel_bias:     NULL, or device bf16; the bias of sequence b, query head h,
+ *               distance d = (len-1) - j is rel_bias[b*bias_tok_stride +
+ *               h*rel_extent + d] for 0 <= d < rel_extent, else 0.  It is
+ *               added after the descale and not multiplied by softmax_scale.
+ * window:       0 = full causal; W > 0 = only keys with (len-1) - j < W.
+ * out:          device bf16 [num_seqs][num_q_heads][head_dim].
+ * workspace:    device, >= fp8kv_decode_workspace_size(...) bytes, 16-byte
+ *               aligned; holds the per-split partial results.
+ */
+fp8kv_status paged_attn_fp8_decode(const fp8kv_cache *cache, const fp8kv_bf16 *q,
+                                   int32_t num_q_heads, const int32_t *block_table,
+                                   int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                                   int32_t num_seqs, float q_scale, float k_scale,
+                                   float v_scale, float softmax_scale,
+                                   const fp8kv_bf16 *rel_bias, int64_t bias_tok_stride,
+                                   int32_t rel_extent, int32_t window, fp8kv_bf16 *out,
+                                   void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * paged_attn_fp8_decode_ex -- paged_attn_fp8_decode with an explicit split
+ * length: split_tokens > 0 (a multiple of 128) makes every split cover that
+ * many keys; 0 chooses it from the device's SM count (the plain call).
+ */
+fp8kv_status paged_attn_fp8_decode_ex(const fp8kv_cache *cache, const fp8kv_bf16 *q,
+                                      int32_t num_q_heads, const int32_t *block_table,
+                                      int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                                      int32_t num_seqs, float q_scale, float k_scale,
+                                      float v_scale, float softmax_scale,
+                                      const fp8kv_bf16 *rel_bias, int64_t bias_tok_stride,
+                                      int32_t rel_extent, int32_t window, fp8kv_bf16 *out,
+                                      void *workspace, size_t workspace_bytes,
+                                      int32_t split_tokens, void *stream);
+
+/* Workspace bytes paged_attn_fp8_decode(_ex) needs for these sizes (split_tokens
+ * as in _ex; 0 = automatic).  Returns 0 for invalid sizes. */
+size_t fp8kv_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads,
+                                   int32_t num_kv_heads, int32_t head_dim,
+                                   int32_t max_blocks_per_seq, int32_t block_size,
+                                   int32_t window, int32_t split_tokens);
+
+/*
+ * attn_fp8_varlen_prefill -- causal (optionally sliding-window) attention of
+ * a chunk of query tokens per sequence over the cached keys, on FP8 tensor
+ * cores (vLLM PR 54705 "Purpose" descale handling; evidence document Tier 0:
+ * P is formed in e4m3 pre-scaled by 2^8 with a lazy-rescale threshold of
+ * 0.75 < log2(448) - 8).
+ * q:             device bf16 [total_q][num_q_heads][head_dim], contiguous;
+ *                sequence b's queries are rows cu_seqlens_q[b] ..
+ *                cu_seqlens_q[b+1]-1.
+ * cu_seqlens_q:  device int32 [num_seqs+1], non-decreasing, starting at 0.
+ * seq_lens_k:    device int32 [num_seqs]; keys per sequence, >= the
+ *                sequence's query count.  The queries are the last ones:
+ *                query i of a chunk of n sits at position seq_len_k - n + i.
+ * max_seqlen_q:  an upper bound of the per-sequence query counts (sizes the
+ *                grid; rows beyond a sequence's count do nothing).
+ * rel_bias:      NULL, or device bf16; bias of query row t (global index),
+ *                head h, distance d = pos_q - pos_k is
+ *                rel_bias[t*bias_tok_stride + h*rel_extent + d] for
+ *                0 <= d < rel_extent, else 0.
+ * window, out:   as for decode; out is [total_q][num_q_heads][head_dim].
+ * workspace:     not used (may be NULL / 0).
+ */
+fp8kv_status attn_fp8_varlen_prefill(const fp8kv_cache *cache, const fp8kv_bf16 *q,
+                                     int32_t num_q_heads, const int32_t *cu_seqlens_q,
+                                     const int32_t *seq_lens_k, const int32_t *block_table,
+                                     int32_t max_blocks_per_seq, int32_t num_seqs,
+                                     int32_t max_seqlen_q, float q_scale, float k_scale,
+                                     float v_scale, float softmax_scale,
+                                     const fp8kv_bf16 *rel_bias, int64_t bias_tok_stride,
+                                     int32_t rel_extent, int32_t window, fp8kv_bf16 *out,
+                                     void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * kv_amax_calibrate -- running max |x| over the tokens that are stored
+ * (model card "Qwen3.8-27B-FP8-KVcal", "What it fixes": amax at the
+ * cache-write point; vLLM PR 54705 Tier 2: only the values at each call's
+ * slot mapping count).
+ *   *amax_k_inout = max(*amax_k_inout, max |k|)   (same for v)
+ * k, v:          device bf16 rows as in kv_store_e4m3; either may be NULL
+ *                (its amax is then left alone).  Strides multiples of 8.
+ * slot_mapping:  NULL (every token counts) or device int64 [num_tokens];
+ *                tokens with slot < 0 are skipped.
+ * amax_*_inout:  device float, >= 0 on entry (e.g. 0 before the first call).
+ * NaN elements are ignored.
+ */
+fp8kv_status kv_amax_calibrate(const fp8kv_bf16 *k, const fp8kv_bf16 *v,
+                               int64_t k_tok_stride, int64_t v_tok_stride,
+                               const int64_t *slot_mapping, int64_t num_tokens,
+                               int32_t num_kv_heads, int32_t head_dim,
+                               float *amax_k_inout, float *amax_v_inout, void *stream);
+
+/*
+ * fp8kv_scale_from_amax -- host-only scale rule.
+ *   rule 0: amax/448                (Qwen3.8-27B-FP8-KVcal, "What it fixes")
+ *   rule 1: ceil_to_bfloat16(amax/448), as fp32
+ *                                   (Qwen3.8-27B-FP8-KVcal, "Rebuild / reproduce")
+ *   rule 2: max(1, amax*1.3/448)    (vLLM PR 54705, calibration paragraph)
+ * Returns FP8KV_ERR_SCALE when amax is negative, NaN or Inf, or the scale
+ * would not be finite and > 0 (amax = 0 under rules 0 and 1),
+ * FP8KV_ERR_ARG for an unknown rule or NULL out.
+ */
+fp8kv_status fp8kv_scale_from_amax(float amax, int32_t rule, float *scale);
+
+/* Bytes of one cache array (K or V): num_blocks*block_size*num_kv_heads*head_dim. */
+size_t fp8kv_cache_bytes(int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                         int32_t head_dim);
+
+/* Reads (and with clear != 0 resets) the current device's error word.
+ * Synchronizes the device. */
+fp8kv_status fp8kv_device_error(uint32_t *flags, int32_t clear);
+
+/* Static text for a status code. */
+const char *fp8kv_status_string(fp8kv_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8KV_H */

@@ -1,0 +1,136 @@
+"""The C-ABI library loads and exports what include/fp8kv.h declares, and its
+host-side checks reject bad arguments before any CUDA call (no GPU needed)."""
+import ctypes
+import math
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp8kv.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z_][a-z0-9_]*)\s*\(",
+                       text, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(
+        "fp8kv_build", os.path.join(ROOT, "fp8_e4m3_kv_gb300", "build.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    mod.build()
+    import fp8_e4m3_kv_gb300 as fk
+    return fk
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("kv_store_e4m3", "paged_attn_fp8_decode", "attn_fp8_varlen_prefill",
+              "kv_amax_calibrate", "fp8kv_scale_from_amax", "fp8kv_decode_workspace_size",
+              "fp8kv_status_string", "fp8kv_device_error", "fp8kv_cache_bytes",
+              "paged_attn_fp8_decode_ex"):
+        assert n in names, n
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", lib.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    for n in declared_functions():
+        assert n in exported, n
+    for n in lib.EXPORTED:
+        assert n in exported, n
+
+
+def test_status_strings(lib):
+    assert lib.status_string(0) == "ok"
+    assert "scale" in lib.status_string(2)
+    assert lib.status_string(99) == "unknown status"
+
+
+def test_scale_rules_match_oracle(lib, oracle_lib):
+    for a in [1272.0, 114.6, 23.1, 11.6, 55.8, 0.37, 1e-3]:
+        for rule in (0, 1, 2):
+            assert lib.scale_from_amax(a, rule) == oracle_lib.scale_from_amax(a, rule)
+    assert lib.scale_from_amax(0.0, 2) == 1.0
+    for bad in (0.0, float("nan"), float("inf"), -1.0):
+        with pytest.raises(lib.Fp8KVError) as e:
+            lib.scale_from_amax(bad, 0)
+        assert e.value.status == lib.ERR_SCALE
+    with pytest.raises(lib.Fp8KVError) as e:
+        lib.scale_from_amax(1.0, 7)
+    assert e.value.status == lib.ERR_ARG
+
+
+def test_cache_bytes(lib):
+    # 4 KV heads x 128 dims: 512 bytes per token per K (1,024 with V)
+    assert lib.cache_bytes(1, 1, 4, 128) * 2 == 1024
+    assert lib.cache_bytes(65536, 16, 4, 128) == 1 << 29
+    assert lib.cache_bytes(-1, 16, 4, 128) == 0
+
+
+def _c(lib):
+    return lib._lib
+
+
+def test_store_rejects_bad_arguments_on_host(lib):
+    L = _c(lib)
+    cache = lib.CacheStruct(16, 16, 4, 16, 1, 128)  # fake, never dereferenced
+    f = L.kv_store_e4m3
+    assert f(None, 16, 16, 128, 128, 16, 1, 1.0, 1.0, None) == lib.ERR_ARG
+    assert f(ctypes.byref(cache), 16, 16, 128, 128, 16, -1, 1.0, 1.0, None) == lib.ERR_ARG
+    for bad in (0.0, -1.0, float("nan"), float("inf")):
+        assert f(ctypes.byref(cache), 16, 16, 128, 128, 16, 1, bad, 1.0, None) == lib.ERR_SCALE
+        assert f(ctypes.byref(cache), 16, 16, 128, 128, 16, 1, 1.0, bad, None) == lib.ERR_SCALE
+    assert f(ctypes.byref(cache), 16, 16, 128, 128, 16, 0, 1.0, 1.0, None) == lib.OK  # no-op
+    assert f(ctypes.byref(cache), None, 16, 128, 128, 16, 1, 1.0, 1.0, None) == lib.ERR_ARG
+    assert f(ctypes.byref(cache), 16, 16, 100, 128, 16, 1, 1.0, 1.0, None) == lib.ERR_ARG
+    assert f(ctypes.byref(cache), 8, 16, 128, 128, 16, 1, 1.0, 1.0, None) == lib.ERR_ARG
+    odd = lib.CacheStruct(16, 16, 4, 16, 1, 100)       # row not a multiple of 16
+    assert f(ctypes.byref(odd), 16, 16, 128, 128, 16, 1, 1.0, 1.0, None) == lib.ERR_UNSUPPORTED
+
+
+def _decode(lib, cache, **kw):
+    a = dict(q=16, Hq=8, bt=16, mb=4, lens=16, B=1, qs=1.0, ks=1.0, vs=1.0, sm=0.1, rel=None,
+             bstride=0, E=0, window=0, out=16, ws=16, wsb=1 << 20, split=0)
+    a.update(kw)
+    return _c(lib).paged_attn_fp8_decode_ex(
+        ctypes.byref(cache) if cache is not None else None, a["q"], a["Hq"], a["bt"], a["mb"],
+        a["lens"], a["B"], a["qs"], a["ks"], a["vs"], a["sm"], a["rel"], a["bstride"], a["E"],
+        a["window"], a["out"], a["ws"], a["wsb"], a["split"], None)
+
+
+def test_decode_rejects_bad_arguments_on_host(lib):
+    cache = lib.CacheStruct(16, 16, 4, 16, 2, 128)
+    assert _decode(lib, None) == lib.ERR_ARG
+    for k in ("qs", "ks", "vs", "sm"):
+        assert _decode(lib, cache, **{k: float("nan")}) == lib.ERR_SCALE
+        assert _decode(lib, cache, **{k: 0.0}) == lib.ERR_SCALE
+    assert _decode(lib, cache, Hq=7) == lib.ERR_ARG                  # not a multiple of Hkv
+    assert _decode(lib, cache, Hq=34) == lib.ERR_UNSUPPORTED         # 17 heads per KV head
+    assert _decode(lib, lib.CacheStruct(16, 16, 4, 16, 2, 64)) == lib.ERR_UNSUPPORTED
+    assert _decode(lib, lib.CacheStruct(16, 16, 4, 24, 2, 128)) == lib.ERR_UNSUPPORTED
+    assert _decode(lib, cache, rel=16, E=0) == lib.ERR_ARG
+    assert _decode(lib, cache, split=100) == lib.ERR_ARG
+    assert _decode(lib, cache, window=-1) == lib.ERR_ARG
+    assert _decode(lib, cache, B=0) == lib.OK                        # nothing to do
+    assert _decode(lib, cache, q=None) == lib.ERR_ARG
+    assert _decode(lib, cache, q=8) == lib.ERR_ARG                   # q not 16-byte aligned
+
+
+def test_workspace_size_is_host_only_with_explicit_splits(lib):
+    # 2 seqs x 8 q heads, max 4 blocks of 16 = 64 keys -> 1 split of 128 keys
+    n = lib.decode_workspace_size(2, 8, 2, 128, 4, 16, 0, 128)
+    assert n == 2 * 8 * 1 * (128 + 2) * 4
+    n = lib.decode_workspace_size(1, 4, 1, 256, 64, 16, 0, 256)        # 1024 keys, 4 splits
+    assert n == 1 * 4 * 4 * (256 + 2) * 4
+    assert lib.decode_workspace_size(1, 4, 1, 64, 4, 16, 0, 128) == 0

@@ -1,0 +1,164 @@
+"""Paged fp8 decode attention on the GPU against the float64 oracle, element
+by element, within 2e-2 abs + 2e-2 rel."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from helpers import assert_close, oracle_decode_rows, to_device
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def fk():
+    import fp8_e4m3_kv_gb300 as m
+    return m
+
+
+def run_case(fk, lens, Hq, Hkv, D, bs, scales=(1.0, 1.0, 1.0), window=0, E=0, bias_bcast=False,
+             v_dist="normal", seed=0, split_tokens=0, fill=0x7F, rows=None, plant=False):
+    spec = workloads.DecodeSpec("case", B=len(lens), Hq=Hq, Hkv=Hkv, D=D, block_size=bs,
+                                ctx_lo=1, ctx_hi=1, v_dist=v_dist, rel_extent=E, plant_v=plant)
+    inp = workloads.make_decode(spec, device="cpu", seed=seed, lens=lens)
+    if E and bias_bcast:   # one learned table per head, broadcast over sequences
+        inp["rel"] = inp["rel"][:1].expand(len(lens), Hq, E)
+    kv = inp["kv"]
+    kd = to_device(kv, DEV)
+    sq, sk, sv = scales
+    # stale NaN codes everywhere the store does not write
+    cache = fk.KVCache.empty(kv.num_blocks, bs, Hkv, D, device=DEV, fill=fill)
+    fk.kv_store_e4m3(cache, kd.k, kd.v, kd.slot_mapping, sk, sv)
+    rel_d = None if inp["rel"] is None else inp["rel"].to(DEV)
+    out = fk.paged_attn_fp8_decode(cache, inp["q"].to(DEV), kd.block_table, kd.seq_lens, sq, sk,
+                                   sv, rel_bias=rel_d, window=window, split_tokens=split_tokens)
+    torch.cuda.synchronize()
+    assert fk.device_error() == 0
+    got = out.float().cpu().numpy()
+    if rows is None:
+        rows = [(b, h) for b in range(len(lens)) for h in range(Hq)]
+    rel_h = None if inp["rel"] is None else inp["rel"]
+    ref = oracle_decode_rows(inp, rows, sq, sk, sv, window=window, rel=rel_h)
+    g = np.stack([got[b, h] for b, h in rows])
+    return assert_close(g, ref, "decode"), got
+
+
+def test_tiny_workload(fk):
+    """1 sequence, 4 q heads / 1 KV head, head_dim 128, context 256, block 16."""
+    run_case(fk, [256], 4, 1, 128, 16)
+
+
+@pytest.mark.parametrize("scales", [(1.0, 1.0, 1.0), (0.5, 0.5, 1.5)])
+def test_ragged_lengths_gqa8_bias(fk, scales):
+    run_case(fk, [1, 2, 15, 16, 17, 127, 128, 129, 255, 300, 1000], 32, 4, 128, 16,
+             scales=scales, E=1024)
+
+
+def test_bias_extent_128_broadcast(fk):
+    run_case(fk, [500, 64, 129], 16, 2, 128, 16, E=128, bias_bcast=True, seed=1)
+
+
+@pytest.mark.parametrize("window", [1, 3, 100, 512])
+def test_sliding_window(fk, window):
+    run_case(fk, [1, 50, 511, 512, 513, 700, 1500], 8, 1, 128, 16, window=window, E=128, seed=2)
+
+
+@pytest.mark.parametrize("bs", [32, 64, 128])
+def test_block_sizes(fk, bs):
+    run_case(fk, [3, 200, 333, 1024], 8, 2, 128, bs, seed=3)
+
+
+def test_head_dim_256_gqa6(fk):
+    run_case(fk, [1, 100, 257, 900], 24, 4, 256, 16, scales=(0.3, 0.05, 0.25), seed=4)
+
+
+def test_head_dim_256_window(fk):
+    run_case(fk, [700, 90], 12, 2, 256, 32, window=512, E=128, seed=5)
+
+
+@pytest.mark.parametrize("G", [1, 3, 16])
+def test_group_sizes(fk, G):
+    run_case(fk, [77, 400], 2 * G, 2, 128, 16, seed=6 + G)
+
+
+@pytest.mark.parametrize("v_scale", [1.0, 3.0])
+def test_heavy_tailed_values(fk, v_scale):
+    """V = 17.47 t(3) with a planted |V| = 1,272: clipped at v_scale 1, not at 3."""
+    run_case(fk, [1024, 2000, 3000], 32, 4, 128, 16, scales=(1.0, 1.0, v_scale), E=1024,
+             v_dist="v_t3", plant=True, seed=9)
+
+
+@pytest.mark.parametrize("split", [128, 256, 896])
+def test_explicit_splits_agree(fk, split):
+    lens = [1, 130, 1000, 2500]
+    _, auto = run_case(fk, lens, 8, 1, 128, 16, seed=11)
+    _, forced = run_case(fk, lens, 8, 1, 128, 16, seed=11, split_tokens=split)
+    # Other split boundaries change each split's running max, hence the
+    # two-term e4m3 rounding of P (relative error <= 2^-8 per weight) and the
+    # fp32 summation order; per row the outputs agree within 2^-8 of the
+    # row's largest value plus one bf16 rounding step.
+    for b in range(len(lens)):
+        for h in range(8):
+            a, f = auto[b, h], forced[b, h]
+            tol = 2.0 ** -8 * np.abs(a).max() + 2.0 ** -7 * np.abs(a)
+            assert (np.abs(f - a) <= tol).all(), (b, h, float(np.abs(f - a).max()))
+
+
+def test_empty_and_single_key(fk):
+    """len 0 gives zeros; len 1 gives v_scale * v8 of the only key (exact)."""
+    err, got = run_case(fk, [0, 1, 5], 4, 1, 128, 16, scales=(1.0, 1.0, 2.0), seed=12,
+                        rows=[(1, 0), (1, 3), (2, 2)])
+    assert (got[0] == 0).all()
+
+
+def _full(fk, spec, rows_per_check, seed=0, scales=(1.0, 1.0, 1.0), calibrate=False):
+    inp = workloads.make_decode(spec, device=DEV, seed=seed)
+    kv = inp["kv"]
+    sq, sk, sv = scales
+    if calibrate:
+        amax = torch.zeros(3, dtype=torch.float32, device=DEV)
+        fk.kv_amax_calibrate(kv.k, kv.v, amax[0:1], amax[1:2], kv.slot_mapping)
+        fk.kv_amax_calibrate(inp["q"], None, amax[2:3], None)
+        ak, av, aq = amax.cpu().tolist()
+        sk, sv, sq = fk.scale_from_amax(ak), fk.scale_from_amax(av), fk.scale_from_amax(aq)
+    cache = fk.KVCache.empty(kv.num_blocks, kv.block_size, spec.Hkv, spec.D, device=DEV)
+    fk.kv_store_e4m3(cache, kv.k, kv.v, kv.slot_mapping, sk, sv)
+    out = fk.paged_attn_fp8_decode(cache, inp["q"], kv.block_table, kv.seq_lens, sq, sk, sv,
+                                   rel_bias=inp["rel"], window=spec.window)
+    torch.cuda.synchronize()
+    assert fk.device_error() == 0
+    got = out.float().cpu().numpy()
+    assert np.isfinite(got).all()
+    lens = inp["lens"]
+    G = spec.Hq // spec.Hkv
+    rng = np.random.default_rng(seed)
+    order = np.argsort(lens)
+    bsel = sorted(set([int(order[0]), int(order[-1])] +
+                      [int(x) for x in rng.choice(len(lens), rows_per_check[0], replace=False)]))
+    rows = []
+    for b in bsel:
+        kvh = int(rng.integers(spec.Hkv))
+        rows += [(b, kvh * G + g) for g in range(G)][: rows_per_check[1]]
+    host = dict(inp)
+    host["kv"] = kv
+    ref = oracle_decode_rows(host, rows, sq, sk, sv, window=spec.window, rel=inp["rel"])
+    return assert_close(np.stack([got[b, h] for b, h in rows]), ref, spec.name)
+
+
+def test_full_decode_64seq_32k(fk):
+    _full(fk, workloads.DECODE_32K, (4, 8))
+
+
+def test_full_decode_64seq_32k_vscale3(fk):
+    _full(fk, workloads.DECODE_32K, (2, 8), scales=(1.0, 1.0, 3.0))
+
+
+def test_full_decode_128k_calibrated_d256(fk):
+    _full(fk, workloads.DECODE_128K_CAL, (1, 6), calibrate=True)
+
+
+def test_full_decode_1m(fk):
+    _full(fk, workloads.DECODE_1M, (0, 8))
