@@ -303,7 +303,7 @@ def oracle_decode_sample(spec, inp, scales, budget_s=15.0):
 # ---------------------------------------------------------------------------
 # secondary workloads
 # ---------------------------------------------------------------------------
-def bench_prefill(fk, dev, steps, warmup, world):
+def bench_prefill(fk, dev, steps, warmup, world, only_group=None):
     spec = workloads.PREFILL_16K
     inp = workloads.make_prefill(spec, device=dev, seed=0)
     kv = inp["kv"]
@@ -323,13 +323,19 @@ def bench_prefill(fk, dev, steps, warmup, world):
                            maxq=max(q_lens[lo:hi])))
     flops = 0
     for gi, (lo, hi) in enumerate([(0, half), (half, spec.n_seqs)]):
+        if only_group is not None and gi != only_group:
+            continue
         w = spec.windows[gi]
         for L in q_lens[lo:hi]:
             flops += sum(min(i + 1, w) if w else i + 1 for i in range(L))
     flops *= 4 * spec.Hq * spec.D
+    if only_group is not None:
+        fk.kv_store_e4m3(cache, kv.k, kv.v, kv.slot_mapping, 1.0, 1.0)
+        groups = [groups[only_group]]
 
     def step():
-        fk.kv_store_e4m3(cache, kv.k, kv.v, kv.slot_mapping, 1.0, 1.0)
+        if only_group is None:
+            fk.kv_store_e4m3(cache, kv.k, kv.v, kv.slot_mapping, 1.0, 1.0)
         for g in groups:
             fk.attn_fp8_varlen_prefill(cache, g["q"], g["cu"], g["lens"], g["bt"], g["maxq"],
                                        1.0, 1.0, 1.0, rel_bias=g["rel"], window=g["window"],
@@ -364,8 +370,31 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extra", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--profile-decode", type=int, default=0, metavar="B",
+                    help="profiling case: only the decode call of the 32K workload cut to B "
+                         "sequences (still larger than L2), no JSON contract line")
+    ap.add_argument("--profile-prefill", type=int, default=0, metavar="GROUP",
+                    help="profiling case: only the prefill call of group GROUP-1 (1 = the "
+                         "causal sequences, 2 = the 512-window ones) of the prefill chunk")
     args = ap.parse_args()
     rank, world = dist_setup(args.gpus)
+    if args.profile_prefill:
+        import fp8_e4m3_kv_gb300 as fk
+        dev = torch.device("cuda", torch.cuda.current_device())
+        res = bench_prefill(fk, dev, args.steps, args.warmup, world,
+                            only_group=args.profile_prefill - 1)
+        print(json.dumps(res))
+        return
+    if args.profile_decode:
+        import dataclasses
+        import fp8_e4m3_kv_gb300 as fk
+        spec = dataclasses.replace(workloads.DECODE_32K, B=args.profile_decode)
+        run = DecodeRun(fk, spec, torch.device("cuda", torch.cuda.current_device()))
+        ms = time_steps(run.decode, args.steps, args.warmup, world)
+        print(json.dumps({"profile_case": spec.name, "seqs": spec.B, "decode_ms": ms,
+                          "decode_bytes": run.decode_bytes,
+                          "decode_gbs": run.decode_bytes / ms / 1e6}))
+        return
     spec = workloads.DECODE_32K
     cfg = {"workload": spec.name, "seqs": spec.B, "q_heads": spec.Hq, "kv_heads": spec.Hkv,
            "head_dim": spec.D, "block_size": spec.block_size,

@@ -34,10 +34,23 @@ constexpr int kDecThreads = 192;   // warps 0-3 softmax, warp 4 producer, warp 5
 constexpr int kNPad = 16;          // query heads per KV head, padded to the MMA N
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Pipeline depth and resident CTAs per SM of the decode kernel (tuning
+// knobs, fixed at build time).
+#ifndef FP8KV_DECODE_STAGES_D128
+#define FP8KV_DECODE_STAGES_D128 3
+#endif
+#ifndef FP8KV_DECODE_CTAS_D128
+#define FP8KV_DECODE_CTAS_D128 2
+#endif
+#ifndef FP8KV_DECODE_STAGES_D256
+#define FP8KV_DECODE_STAGES_D256 3
+#endif
+
 template <int D>
 struct DecCfg {
     static constexpr int kCB = D / 128;               // 128-byte column blocks per row
-    static constexpr int kStages = 3;
+    static constexpr int kStages = D == 128 ? FP8KV_DECODE_STAGES_D128 : FP8KV_DECODE_STAGES_D256;
+    static constexpr int kCtasPerSm = D == 128 ? FP8KV_DECODE_CTAS_D128 : 1;
     static constexpr int kTileBytes = kTile * D;      // one K (or V) tile
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kQBytes = kNPad * D;         // Q8: 16 rows x D bytes
@@ -103,7 +116,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, CtaFai
 }
 
 template <int D, int GMAX>
-__global__ void __launch_bounds__(kDecThreads, D == 128 ? 2 : 1)
+__global__ void __launch_bounds__(kDecThreads, DecCfg<D>::kCtasPerSm)
 decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
               const DecodeParams p) {
     using C = DecCfg<D>;
@@ -131,18 +144,19 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
     }
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffMisc);
-    uint64_t *full = bars;          // [3] TMA landed
-    uint64_t *empty = bars + 3;     // [3] stage consumed (MMA commit)
-    uint64_t *s_full = bars + 6;    // [2] S^T in TMEM
-    uint64_t *s_free = bars + 8;    // [2] S^T read by the softmax warps
-    uint64_t *p_full = bars + 10;   // [2] P written to shared memory
-    uint64_t *o_full = bars + 12;   // [2] O^T in TMEM
-    uint64_t *o_free = bars + 14;   // [2] O^T read by the softmax warps
-    uint64_t *mma_done = bars + 16; // teardown: all MMAs complete
-    uint64_t *red_bar = bars + 17;  // [2] the 4 softmax warps' tile maxima are in `red`
-    uint64_t *l_bar = bars + 19;    // the 4 softmax warps' row sums are in `lred`
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc + 160);
-    CtaFail *fail = reinterpret_cast<CtaFail *>(smem + C::kOffMisc + 164);
+    static_assert(C::kStages <= 4, "barrier area holds at most 4 stages");
+    uint64_t *full = bars;          // [kStages] TMA landed
+    uint64_t *empty = bars + 4;     // [kStages] stage consumed (MMA commit)
+    uint64_t *s_full = bars + 8;    // [2] S^T in TMEM
+    uint64_t *s_free = bars + 10;   // [2] S^T read by the softmax warps
+    uint64_t *p_full = bars + 12;   // [2] P written to shared memory
+    uint64_t *o_full = bars + 14;   // [2] O^T in TMEM
+    uint64_t *o_free = bars + 16;   // [2] O^T read by the softmax warps
+    uint64_t *mma_done = bars + 18; // teardown: all MMAs complete
+    uint64_t *red_bar = bars + 19;  // [2] the 4 softmax warps' tile maxima are in `red`
+    uint64_t *l_bar = bars + 21;    // the 4 softmax warps' row sums are in `lred`
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc + 192);
+    CtaFail *fail = reinterpret_cast<CtaFail *>(smem + C::kOffMisc + 196);
     float *red = reinterpret_cast<float *>(smem + C::kOffMisc + 256);   // [2][4][16]
     float *lred = red + 128;                                             // [4][16]
 
@@ -439,41 +453,68 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
 
 // Merge the splits of one (sequence, query head): m = max m_s,
 // l = sum l_s 2^(m_s - m), o = sum o_s 2^(m_s - m); out = v_scale * o / l.
+// Eight warps take the splits round-robin (lane = 4 consecutive d per 128),
+// then the warp partials are summed in a fixed order.
+constexpr int kMergeWarps = 8;
+
 template <int D>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(kMergeWarps * 32)
 decode_merge_kernel(const float *__restrict__ part_o, const float *__restrict__ part_ml,
                     uint16_t *__restrict__ out, int32_t Hq, int32_t S, float v_scale) {
-    __shared__ float red[4];
+    constexpr int kV = D / 128;   // float4 per lane
+    __shared__ float red_m[kMergeWarps];
+    __shared__ float red_l[kMergeWarps];
+    __shared__ __align__(16) float red_acc[kMergeWarps][D];
     const int h = blockIdx.x, b = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t row = static_cast<int64_t>(b) * Hq + h;
     const float *ml = part_ml + row * S * 2;
     float m = -INFINITY;
-    for (int s = threadIdx.x; s < S; s += 128) m = fmaxf(m, ml[2 * s]);
+    for (int s = threadIdx.x; s < S; s += kMergeWarps * 32) m = fmaxf(m, ml[2 * s]);
     m = warp_max(m);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    if (lane == 0) red_m[warp] = m;
     __syncthreads();
-    m = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-    constexpr int kPer = D / 128;
-    float acc[kPer];
+    m = red_m[0];
 #pragma unroll
-    for (int c = 0; c < kPer; ++c) acc[c] = 0.0f;
+    for (int w = 1; w < kMergeWarps; ++w) m = fmaxf(m, red_m[w]);
+    float4 acc[kV];
+#pragma unroll
+    for (int c = 0; c < kV; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
     float l = 0.0f;
     if (m != -INFINITY) {
-        for (int s = 0; s < S; ++s) {
+#pragma unroll 2
+        for (int s = warp; s < S; s += kMergeWarps) {
             const float ms = ml[2 * s];
             if (ms == -INFINITY) continue;
             const float w = exp2f(ms - m);
             l = fmaf(ml[2 * s + 1], w, l);
-            const float *po = part_o + (row * S + s) * D;
+            const float4 *po = reinterpret_cast<const float4 *>(part_o + (row * S + s) * D);
 #pragma unroll
-            for (int c = 0; c < kPer; ++c) acc[c] = fmaf(po[c * 128 + threadIdx.x], w, acc[c]);
+            for (int c = 0; c < kV; ++c) {
+                const float4 v = po[c * 32 + lane];
+                acc[c].x = fmaf(v.x, w, acc[c].x);
+                acc[c].y = fmaf(v.y, w, acc[c].y);
+                acc[c].z = fmaf(v.z, w, acc[c].z);
+                acc[c].w = fmaf(v.w, w, acc[c].w);
+            }
         }
     }
-    const float f = l > 0.0f ? v_scale / l : 0.0f;
-    uint16_t *o = out + row * D;
 #pragma unroll
-    for (int c = 0; c < kPer; ++c)
-        o[c * 128 + threadIdx.x] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[c] * f));
+    for (int c = 0; c < kV; ++c)
+        reinterpret_cast<float4 *>(red_acc[warp])[c * 32 + lane] = acc[c];
+    if (lane == 0) red_l[warp] = l;
+    __syncthreads();
+    float L = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kMergeWarps; ++w) L += red_l[w];
+    const float f = L > 0.0f ? v_scale / L : 0.0f;
+    uint16_t *o = out + row * D;
+    for (int d = threadIdx.x; d < D; d += kMergeWarps * 32) {
+        float a = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kMergeWarps; ++w) a += red_acc[w][d];
+        o[d] = __bfloat16_as_ushort(__float2bfloat16_rn(a * f));
+    }
 }
 
 struct SplitPlan {
@@ -498,7 +539,7 @@ bool plan_splits(int32_t num_seqs, int32_t num_kv_heads, int32_t head_dim,
         if (split_tokens % kTile) return false;
         st = split_tokens / kTile;
     } else {
-        const int64_t ctas_per_sm = head_dim == 128 ? 2 : 1;
+        const int64_t ctas_per_sm = head_dim == 128 ? DecCfg<128>::kCtasPerSm : 1;
         const int64_t target = static_cast<int64_t>(num_sms) * ctas_per_sm * 8;
         int64_t pairs = static_cast<int64_t>(num_seqs) * num_kv_heads;
         if (pairs < 1) pairs = 1;
@@ -622,10 +663,10 @@ extern "C" fp8kv_status paged_attn_fp8_decode_ex(
                     : launch_decode<256, 16>(km, vm, p, Hkv, num_seqs, s);
     if (st != FP8KV_OK) return st;
     if (D == 128)
-        decode_merge_kernel<128><<<dim3(num_q_heads, num_seqs), 128, 0, s>>>(
+        decode_merge_kernel<128><<<dim3(num_q_heads, num_seqs), kMergeWarps * 32, 0, s>>>(
             p.part_o, p.part_ml, out, num_q_heads, plan.num_splits, v_scale);
     else
-        decode_merge_kernel<256><<<dim3(num_q_heads, num_seqs), 128, 0, s>>>(
+        decode_merge_kernel<256><<<dim3(num_q_heads, num_seqs), kMergeWarps * 32, 0, s>>>(
             p.part_o, p.part_ml, out, num_q_heads, plan.num_splits, v_scale);
     if (cudaGetLastError() != cudaSuccess) return FP8KV_ERR_LAUNCH;
     return FP8KV_OK;

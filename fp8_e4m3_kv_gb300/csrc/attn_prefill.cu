@@ -1,6 +1,456 @@
-// attn_prefill.cu -- varlen prefill attention over the e4m3 cache (kernel to
-// follow; the entry point validates and reports the path as unsupported).
+// attn_prefill.cu -- varlen causal / sliding-window prefill attention over
+// the e4m3 paged cache on FP8 tensor cores (vLLM PR 54705: "Purpose",
+// descale handling; evidence document Tier 0: P formed in e4m3 pre-scaled by
+// 2^max_offset with max_offset = 8 and a lazy-rescale threshold of 0.75,
+// below the log2(448) - 8 = 0.807 slack that keeps P from clipping).
+//
+// One CTA computes one tile of 128 query rows of one query head of one
+// sequence.  Keys stream in tiles of 128 from the paged cache:
+//   warp 4  (producer)  TMA-loads the K and V tiles (one box per block and
+//                       128-byte column) into a 3-stage ring (2 for D = 256);
+//   warp 5  (MMA)       one thread issues tcgen05 kind::f8f6f4 MMAs:
+//                       S  = Q8 . K_tile^T            (128 x 128, fp32 in TMEM,
+//                                                      double-buffered)
+//                       O += P_hi . V_tile + P_lo . V_tile   (128 x D in TMEM)
+//   warps 0-3 (softmax) thread r owns query row r (TMEM lane r): folded
+//                       descale, exact bf16 relative bias, causal / window
+//                       mask, running max with the lazy rescale, P, row sum,
+//                       and at the end out = v_scale * O / l in bf16.
+// P = exp2(z - m + 8) <= 2^(8 + 0.75) < 448 is stored as two e4m3 terms,
+// P_hi = e4m3(P) and P_lo = e4m3(P - P_hi), so that the PV product stays on
+// the FP8 tensor cores while the weights keep about 8 significant bits.
+#include <math.h>
+
 #include "common.cuh"
+
+namespace fp8kv {
+namespace {
+
+constexpr int kPreThreads = 192;
+constexpr float kLog2eP = 1.4426950408889634f;
+constexpr float kRescaleTau = 0.75f;   // lazy-rescale threshold (log2 units)
+constexpr float kPOffset = 8.0f;       // P pre-scale 2^8
+
+template <int D>
+struct PreCfg {
+    static constexpr int kCB = D / 128;
+    static constexpr int kStages = D == 128 ? 3 : 2;
+    static constexpr int kTileBytes = kTile * D;
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kQBytes = kTile * D;
+    static constexpr int kPBytes = kTile * kTile;          // one P term, 16 KB
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffStages = kQBytes;
+    static constexpr int kOffP = kOffStages + kStages * kStageBytes;   // [hi, lo]
+    static constexpr int kOffMisc = kOffP + 2 * kPBytes;
+    static constexpr int kSmemBytes = kOffMisc + 1024 + 1024;
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kColS = 0;                   // S buffers: cols 0, 128
+    static constexpr uint32_t kColO = 256;                 // O: cols 256 .. 256 + D
+};
+
+struct PrefillParams {
+    const uint16_t *q;
+    const int32_t *cu_q;
+    const int32_t *lens_k;
+    const int32_t *block_table;
+    const uint16_t *rel;
+    uint16_t *out;
+    uint32_t *err;
+    int64_t bias_tok_stride;
+    int64_t num_blocks;
+    int32_t max_blocks;
+    int32_t Hq;
+    int32_t G;
+    int32_t block_size;
+    int32_t rel_extent;
+    int32_t window;
+    int32_t n_qtiles;
+    float q_scale;
+    float score_log2;   // softmax_scale * q_scale * k_scale * log2(e)
+    float v_scale;
+};
+
+__device__ __forceinline__ void mbar_drain_p(uint64_t *bar, uint32_t parity, uint32_t *err) {
+    CtaFail never{0};
+    mbar_wait(bar, parity, &never, err);
+}
+
+__device__ __forceinline__ bool warp_wait_p(uint64_t *bar, uint32_t parity, CtaFail *fail,
+                                            uint32_t *err) {
+    const bool ok = mbar_wait(bar, parity, fail, err);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// 16 consecutive P values of one row -> 16 e4m3 bytes of P_hi and of P_lo
+// (P_lo = e4m3(P - P_hi), the difference taken in fp16).
+__device__ __forceinline__ void split_p16(const float *pv, uint4 &hi, uint4 &lo) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        uint32_t hw = 0, lw = 0;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const __half2 ph = __floats2half2_rn(pv[4 * w + 2 * k], pv[4 * w + 2 * k + 1]);
+            const __half2_raw phr = ph;
+            const uint32_t h8 = __nv_cvt_halfraw2_to_fp8x2(phr, __NV_SATFINITE, __NV_E4M3);
+            const __half2 hh = e4m3x2_to_half2(static_cast<uint16_t>(h8));
+            const __half2_raw rr = __hsub2(ph, hh);
+            const uint32_t l8 = __nv_cvt_halfraw2_to_fp8x2(rr, __NV_SATFINITE, __NV_E4M3);
+            hw |= (h8 & 0xFFFFu) << (16 * k);
+            lw |= (l8 & 0xFFFFu) << (16 * k);
+        }
+        h[w] = hw;
+        l[w] = lw;
+    }
+    hi = make_uint4(h[0], h[1], h[2], h[3]);
+    lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kPreThreads, 1)
+prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+               const PrefillParams p) {
+    using C = PreCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int qt = p.n_qtiles - 1 - static_cast<int>(blockIdx.x);   // longest tiles first
+    const int h = blockIdx.y, b = blockIdx.z;
+    const int kvh = h / p.G;
+    const int q_first = p.cu_q[b];
+    const int len_q = p.cu_q[b + 1] - q_first;
+    if (qt * kTile >= len_q) return;
+    const int64_t len_k = p.lens_k[b];
+    const int n_rows = min(kTile, len_q - qt * kTile);
+    const int64_t P0 = len_k - len_q + static_cast<int64_t>(qt) * kTile;   // position of row 0
+    const int64_t pos_last = P0 + n_rows - 1;
+    int64_t key_lo = 0;
+    if (p.window > 0 && P0 - p.window + 1 > 0) key_lo = P0 - p.window + 1;
+    const int64_t kt0 = key_lo / kTile;
+    const int ntiles = static_cast<int>((pos_last + 1 + kTile - 1) / kTile - kt0);
+    if (ntiles <= 0 || P0 < 0) return;   // (seq_lens_k smaller than the query count)
+
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffMisc);
+    uint64_t *full = bars;              // [3]
+    uint64_t *empty = bars + 3;         // [3]
+    uint64_t *s_full = bars + 6;        // [2]
+    uint64_t *s_free = bars + 8;        // [2]
+    uint64_t *p_full = bars + 10;       // P of the current tile written
+    uint64_t *o_done = bars + 11;       // PV of a tile complete
+    uint64_t *mma_done = bars + 12;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc + 128);
+    CtaFail *fail = reinterpret_cast<CtaFail *>(smem + C::kOffMisc + 132);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_free[i], 4);
+        }
+        mbar_init(p_full, 4);
+        mbar_init(o_done, 1);
+        mbar_init(mma_done, 1);
+        fail->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 5) tmem_alloc(tmem_slot, C::kTmemCols);
+    if (warp < 4) {
+        // Q8 row r = e4m3(q / q_scale), 128-byte swizzled K-major; rows past
+        // the sequence's queries are zero.
+        const int r = threadIdx.x;
+        const uint16_t *qrow = p.q + (static_cast<int64_t>(q_first) + qt * kTile + r) * p.Hq * D +
+                               static_cast<int64_t>(h) * D;
+#pragma unroll
+        for (int c = 0; c < D / 16; ++c) {
+            uint4 packed = make_uint4(0, 0, 0, 0);
+            if (r < n_rows) {
+                const uint4 w0 = *reinterpret_cast<const uint4 *>(qrow + c * 16);
+                const uint4 w1 = *reinterpret_cast<const uint4 *>(qrow + c * 16 + 8);
+                packed.x = quantize_bf16x2(w0.x, p.q_scale) | (quantize_bf16x2(w0.y, p.q_scale) << 16);
+                packed.y = quantize_bf16x2(w0.z, p.q_scale) | (quantize_bf16x2(w0.w, p.q_scale) << 16);
+                packed.z = quantize_bf16x2(w1.x, p.q_scale) | (quantize_bf16x2(w1.y, p.q_scale) << 16);
+                packed.w = quantize_bf16x2(w1.z, p.q_scale) | (quantize_bf16x2(w1.w, p.q_scale) << 16);
+            }
+            const int cb = c / 8, cc = c % 8;
+            *reinterpret_cast<uint4 *>(smem + C::kOffQ + cb * (kTile * 128) + r * 128 +
+                                       ((cc ^ (r & 7)) << 4)) = packed;
+        }
+        fence_proxy_async_smem();
+    }
+    if (warp == 4 && lane == 0) {
+        tma_prefetch_map(&kmap);
+        tma_prefetch_map(&vmap);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ producer
+        const uint64_t pol = l2_policy_evict_first();
+        const int nb = kTile / p.block_size;
+        int last_issued[C::kStages];
+#pragma unroll
+        for (int s = 0; s < C::kStages; ++s) last_issued[s] = -1;
+        for (int i = 0; i < ntiles; ++i) {
+            const int s = i % C::kStages;
+            int32_t phys = static_cast<int32_t>(p.num_blocks);   // out of range: zero fill
+            if (lane < nb) {
+                const int64_t lb = (kt0 + i) * nb + lane;
+                if (lb * p.block_size < len_k && lb < p.max_blocks) {
+                    const int32_t id =
+                        __ldg(p.block_table + static_cast<int64_t>(b) * p.max_blocks + lb);
+                    if (id >= 0 && id < p.num_blocks)
+                        phys = id;
+                    else
+                        atomicOr(p.err, FP8KV_DEVERR_BAD_BLOCK);
+                }
+            }
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait(&empty[s], ((i / C::kStages) & 1) ^ 1, fail, p.err);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            if (lane == 0) mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+            __syncwarp();
+            if (lane < nb) {
+                uint8_t *kdst = smem + C::kOffStages + s * C::kStageBytes + lane * p.block_size * 128;
+                uint8_t *vdst = kdst + C::kTileBytes;
+#pragma unroll
+                for (int cb = 0; cb < C::kCB; ++cb) {
+                    tma_load_4d(kdst + cb * (kTile * 128), &kmap, &full[s], cb * 128, kvh, 0, phys, pol);
+                    tma_load_4d(vdst + cb * (kTile * 128), &vmap, &full[s], cb * 128, kvh, 0, phys, pol);
+                }
+            }
+            last_issued[s] = i;
+        }
+        if (lane == 0 && fail->abort) {
+            for (int s = 0; s < C::kStages; ++s)
+                if (last_issued[s] >= 0)
+                    mbar_drain_p(&full[s], (last_issued[s] / C::kStages) & 1, p.err);
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc_qk = idesc_e4m3_f32(128, 128, false, false);
+            const uint32_t idesc_pv = idesc_e4m3_f32(128, 128, false, true);
+            const uint32_t q_addr = smem_u32(smem + C::kOffQ);
+            const uint32_t p_addr = smem_u32(smem + C::kOffP);
+            for (int i = 0; i <= ntiles; ++i) {
+                if (i < ntiles) {
+                    const int s = i % C::kStages, sb = i & 1;
+                    if (!mbar_wait(&full[s], (i / C::kStages) & 1, fail, p.err)) break;
+                    if (!mbar_wait(&s_free[sb], ((i >> 1) & 1) ^ 1, fail, p.err)) break;
+                    tc_fence_after_sync();
+                    const uint32_t k_addr = smem_u32(smem + C::kOffStages + s * C::kStageBytes);
+#pragma unroll
+                    for (int kk = 0; kk < D / 32; ++kk) {
+                        const uint32_t cb = kk / 4, ko = (kk % 4) * 32;
+                        const uint64_t a = sdesc_sw128(q_addr + cb * (kTile * 128) + ko, 16, 1024);
+                        const uint64_t bd = sdesc_sw128(k_addr + cb * (kTile * 128) + ko, 16, 1024);
+                        mma_e4m3(tmem + C::kColS + sb * 128, a, bd, idesc_qk, kk > 0);
+                    }
+                    tc_commit(&s_full[sb]);
+                }
+                if (i >= 1) {
+                    const int j = i - 1, s = j % C::kStages;
+                    if (!mbar_wait(p_full, j & 1, fail, p.err)) break;
+                    tc_fence_after_sync();
+                    const uint32_t v_addr =
+                        smem_u32(smem + C::kOffStages + s * C::kStageBytes + C::kTileBytes);
+#pragma unroll
+                    for (int cb = 0; cb < C::kCB; ++cb) {
+#pragma unroll
+                        for (int part = 0; part < 2; ++part) {
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk) {
+                                // A = P (K-major, 128 keys per row); B = V tile
+                                // (MN-major: key rows of 128 d-bytes, 8-row groups
+                                // 1024 bytes apart), 32 keys per MMA.
+                                const uint64_t a =
+                                    sdesc_sw128(p_addr + part * C::kPBytes + kk * 32, 16, 1024);
+                                const uint64_t bd = sdesc_sw128(
+                                    v_addr + cb * (kTile * 128) + kk * 32 * 128, kTile * 128, 1024);
+                                mma_e4m3(tmem + C::kColO + cb * 128, a, bd, idesc_pv,
+                                         (j > 0 || part > 0 || kk > 0) ? 1u : 0u);
+                            }
+                        }
+                    }
+                    tc_commit(o_done);
+                    tc_commit(&empty[s]);
+                }
+            }
+            tc_commit(mma_done);
+            mbar_drain_p(mma_done, 0, p.err);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax
+        const int r = threadIdx.x;
+        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+        const int64_t pos = P0 + r;
+        const bool row_ok = r < n_rows;
+        const uint16_t *bias_row =
+            (p.rel && row_ok) ? p.rel + (static_cast<int64_t>(q_first) + qt * kTile + r) *
+                                            p.bias_tok_stride + static_cast<int64_t>(h) * p.rel_extent
+                              : nullptr;
+        uint8_t *p_hi = smem + C::kOffP;
+        uint8_t *p_lo = p_hi + C::kPBytes;
+        float m_used = -INFINITY, l = 0.0f;
+        bool ok = true;
+        for (int i = 0; i < ntiles; ++i) {
+            const int sb = i & 1;
+            if (!warp_wait_p(&s_full[sb], (i >> 1) & 1, fail, p.err)) { ok = false; break; }
+            tc_fence_after_sync();
+            float z[128];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                tmem_ld_x32(tmem + lane_base + C::kColS + sb * 128 + c * 32, z + c * 32);
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_free[sb]);
+
+            const int64_t k0 = (kt0 + i) * kTile;
+            const bool full_tile = (k0 + kTile - 1 <= P0) &&
+                                   (p.window == 0 || pos_last - k0 < p.window) &&
+                                   (k0 + kTile - 1 < len_k);
+            const bool bias_tile = bias_row != nullptr && pos - k0 >= 0 &&
+                                   pos - k0 - (kTile - 1) < p.rel_extent;
+            float mx = -INFINITY;
+            if (full_tile && !bias_tile) {
+#pragma unroll
+                for (int c = 0; c < 128; ++c) {
+                    z[c] *= p.score_log2;
+                    mx = fmaxf(mx, z[c]);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 128; ++c) {
+                    const int64_t kidx = k0 + c;
+                    float zz = z[c] * p.score_log2;
+                    const int64_t d = pos - kidx;
+                    if (bias_tile && d >= 0 && d < p.rel_extent)
+                        zz = fmaf(bf16_bits_to_float(__ldg(bias_row + d)), kLog2eP, zz);
+                    const bool valid = d >= 0 && (p.window == 0 || d < p.window) && kidx < len_k;
+                    zz = valid ? zz : -INFINITY;
+                    z[c] = zz;
+                    mx = fmaxf(mx, zz);
+                }
+            }
+            // lazy rescale: move the reference max only when the row max grew
+            // by more than tau, so P <= 2^(8 + tau) stays below 448
+            const bool resc = mx > m_used + kRescaleTau;
+            const float m_new = resc ? mx : m_used;
+            const float alpha = (resc && m_used != -INFINITY) ? exp2f(m_used - m_new) : 1.0f;
+            if (i >= 1) {
+                if (!warp_wait_p(o_done, (i - 1) & 1, fail, p.err)) { ok = false; break; }
+                tc_fence_after_sync();
+                if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        float o[32];
+                        const uint32_t ta = tmem + lane_base + C::kColO + c * 32;
+                        tmem_ld_x32(ta, o);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] *= alpha;
+                        tmem_st_x32(ta, o);
+                    }
+                }
+            }
+            l *= alpha;
+            m_used = m_new;
+            const float m8 = (m_used == -INFINITY) ? 0.0f : m_used - kPOffset;
+            const int sw = r & 7;
+#pragma unroll
+            for (int c16 = 0; c16 < 8; ++c16) {
+                float pv[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    pv[e] = exp2f(z[c16 * 16 + e] - m8);
+                    l += pv[e];
+                }
+                uint4 hi, lo;
+                split_p16(pv, hi, lo);
+                const uint32_t off = r * 128 + ((c16 ^ sw) << 4);
+                *reinterpret_cast<uint4 *>(p_hi + off) = hi;
+                *reinterpret_cast<uint4 *>(p_lo + off) = lo;
+            }
+            // keys past the end of the sequence may hold stale bytes (NaN codes
+            // included): zero their V rows so that 0 * V stays 0 in the MMA
+            if (k0 + r >= len_k) {
+                uint8_t *vrow = smem + C::kOffStages + (i % C::kStages) * C::kStageBytes +
+                                C::kTileBytes + r * 128;
+#pragma unroll
+                for (int cb = 0; cb < C::kCB; ++cb) {
+                    uint4 *q4 = reinterpret_cast<uint4 *>(vrow + cb * (kTile * 128));
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) q4[c] = make_uint4(0, 0, 0, 0);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full);
+        }
+        if (ok && warp_wait_p(o_done, (ntiles - 1) & 1, fail, p.err)) {
+            tc_fence_after_sync();
+            const float f = (l > 0.0f) ? p.v_scale / l : 0.0f;
+            uint16_t *orow = p.out + (static_cast<int64_t>(q_first) + qt * kTile + r) * p.Hq * D +
+                             static_cast<int64_t>(h) * D;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                float o[32];
+                tmem_ld_x32(tmem + lane_base + C::kColO + c * 32, o);
+                if (row_ok) {
+                    uint32_t w[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const __nv_bfloat162 v2 = __floats2bfloat162_rn(o[2 * e] * f, o[2 * e + 1] * f);
+                        w[e] = *reinterpret_cast<const uint32_t *>(&v2);
+                    }
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+                }
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+template <int D>
+fp8kv_status launch_prefill(const CUtensorMap &km, const CUtensorMap &vm, const PrefillParams &p,
+                            int num_seqs, cudaStream_t stream) {
+    using C = PreCfg<D>;
+    auto kern = prefill_kernel<D>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return FP8KV_ERR_LAUNCH;
+    }
+    dim3 grid(p.n_qtiles, p.Hq, num_seqs);
+    kern<<<grid, kPreThreads, C::kSmemBytes, stream>>>(km, vm, p);
+    if (cudaGetLastError() != cudaSuccess) return FP8KV_ERR_LAUNCH;
+    return FP8KV_OK;
+}
+
+}  // namespace
+}  // namespace fp8kv
+
+using namespace fp8kv;
 
 extern "C" fp8kv_status attn_fp8_varlen_prefill(
     const fp8kv_cache *cache, const fp8kv_bf16 *q, int32_t num_q_heads,
@@ -9,10 +459,54 @@ extern "C" fp8kv_status attn_fp8_varlen_prefill(
     float k_scale, float v_scale, float softmax_scale, const fp8kv_bf16 *rel_bias,
     int64_t bias_tok_stride, int32_t rel_extent, int32_t window, fp8kv_bf16 *out, void *workspace,
     size_t workspace_bytes, void *stream) {
-    (void)cache; (void)q; (void)num_q_heads; (void)cu_seqlens_q; (void)seq_lens_k;
-    (void)block_table; (void)max_blocks_per_seq; (void)num_seqs; (void)max_seqlen_q;
-    (void)q_scale; (void)k_scale; (void)v_scale; (void)softmax_scale; (void)rel_bias;
-    (void)bias_tok_stride; (void)rel_extent; (void)window; (void)out; (void)workspace;
-    (void)workspace_bytes; (void)stream;
-    return FP8KV_ERR_UNSUPPORTED;
+    (void)workspace;
+    (void)workspace_bytes;
+    if (!cache || num_seqs < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || window < 0 ||
+        max_seqlen_q < 0)
+        return FP8KV_ERR_ARG;
+    if (!scale_ok(q_scale) || !scale_ok(k_scale) || !scale_ok(v_scale) || !scale_ok(softmax_scale))
+        return FP8KV_ERR_SCALE;
+    const int D = cache->head_dim, bs = cache->block_size, Hkv = cache->num_kv_heads;
+    if (Hkv <= 0 || cache->num_blocks < 0 || num_q_heads % Hkv != 0) return FP8KV_ERR_ARG;
+    if ((D != 128 && D != 256) || (bs != 16 && bs != 32 && bs != 64 && bs != 128) ||
+        num_seqs > 65535 || num_q_heads > 65535 || cache->num_blocks >= (1ll << 31))
+        return FP8KV_ERR_UNSUPPORTED;
+    if (rel_bias && (rel_extent <= 0 || bias_tok_stride < 0)) return FP8KV_ERR_ARG;
+    if (num_seqs == 0 || max_seqlen_q == 0) return FP8KV_OK;
+    if (!q || !cu_seqlens_q || !seq_lens_k || !block_table || !out || !cache->k || !cache->v)
+        return FP8KV_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(out) & 15) ||
+        (reinterpret_cast<uintptr_t>(cache->k) & 15) || (reinterpret_cast<uintptr_t>(cache->v) & 15))
+        return FP8KV_ERR_ARG;
+    int sms = 0;
+    fp8kv_status st = check_device(&sms);
+    if (st != FP8KV_OK) return st;
+    CUtensorMap km, vm;
+    if (!make_cache_map(&km, cache->k, cache->num_blocks, bs, Hkv, D) ||
+        !make_cache_map(&vm, cache->v, cache->num_blocks, bs, Hkv, D))
+        return FP8KV_ERR_LAUNCH;
+    PrefillParams p;
+    p.q = q;
+    p.cu_q = cu_seqlens_q;
+    p.lens_k = seq_lens_k;
+    p.block_table = block_table;
+    p.rel = rel_bias;
+    p.out = out;
+    p.err = device_error_word();
+    p.bias_tok_stride = bias_tok_stride;
+    p.num_blocks = cache->num_blocks;
+    p.max_blocks = max_blocks_per_seq;
+    p.Hq = num_q_heads;
+    p.G = num_q_heads / Hkv;
+    p.block_size = bs;
+    p.rel_extent = rel_bias ? rel_extent : 0;
+    p.window = window;
+    p.n_qtiles = (max_seqlen_q + kTile - 1) / kTile;
+    p.q_scale = q_scale;
+    p.score_log2 = static_cast<float>(static_cast<double>(softmax_scale) * q_scale * k_scale *
+                                      1.4426950408889634);
+    p.v_scale = v_scale;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return D == 128 ? launch_prefill<128>(km, vm, p, num_seqs, s)
+                    : launch_prefill<256>(km, vm, p, num_seqs, s);
 }

@@ -86,3 +86,31 @@ def to_device(kv, dev):
                              tok_start=kv.tok_start.to(dev), block_table=kv.block_table.to(dev),
                              slot_mapping=kv.slot_mapping.to(dev), num_blocks=kv.num_blocks,
                              block_size=kv.block_size)
+
+
+def oracle_prefill_rows(inp, rows, q_scale, k_scale, v_scale, softmax_scale=None, window=0,
+                        rel=None):
+    """Oracle output rows for prefill rows (t, h): query token t (global index
+    into q) of head h; its sequence's queries are the last q_len of k_len keys."""
+    kv = inp["kv"]
+    q = inp["q"]
+    Tq, Hq, D = q.shape
+    Hkv = kv.k.shape[1]
+    G = Hq // Hkv
+    sigma = softmax_scale if softmax_scale is not None else 1 / math.sqrt(D)
+    cu = inp["cu_seqlens_q"].cpu().tolist()
+    okv = OracleKV(kv, k_scale, v_scale)
+    q_lens, k_lens = inp["q_lens"], inp["k_lens"]
+    res = {}
+    seq_of = np.searchsorted(np.asarray(cu), np.asarray([t for t, _ in rows]), side="right") - 1
+    order = sorted(range(len(rows)), key=lambda i: (seq_of[i], rows[i][1] // G))
+    for i in order:
+        t, h = rows[i]
+        b = int(seq_of[i])
+        k8, v8 = okv.seq(b, h // G)
+        pos = k_lens[b] - q_lens[b] + (t - cu[b])
+        q8 = oracle.quantize(bits(q[t, h].contiguous()), q_scale)
+        bias = None if rel is None else bits(rel[t, h].contiguous())
+        res[i] = oracle.attend_row(q8, k8, v8, pos, sigma, q_scale, k_scale, v_scale, bias=bias,
+                                   window=window)
+    return np.stack([res[i] for i in range(len(rows))]) if rows else np.zeros((0, D))

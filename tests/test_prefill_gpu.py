@@ -1,0 +1,143 @@
+"""Varlen fp8 prefill attention (tcgen05) on the GPU against the float64
+oracle, element by element, within 2e-2 abs + 2e-2 rel."""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from helpers import assert_close, oracle_prefill_rows, to_device
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def fk():
+    import fp8_e4m3_kv_gb300 as m
+    return m
+
+
+def run_case(fk, q_lens, k_lens=None, Hq=8, Hkv=2, D=128, bs=16, scales=(1.0, 1.0, 1.0),
+             window=0, E=0, seed=0, rows=None, bias_std=0.5, rel_override=None):
+    spec = workloads.PrefillSpec("case", q_lens=q_lens, q_lo=0, q_hi=0, n_seqs=len(q_lens),
+                                 Hq=Hq, Hkv=Hkv, D=D, block_size=bs, rel_extent=E,
+                                 bias_std=bias_std)
+    inp = workloads.make_prefill(spec, device="cpu", seed=seed, q_lens=q_lens, k_lens=k_lens)
+    if rel_override is not None:
+        inp["rel"] = rel_override(inp)
+    kv = inp["kv"]
+    kd = to_device(kv, DEV)
+    sq, sk, sv = scales
+    cache = fk.KVCache.empty(kv.num_blocks, bs, Hkv, D, device=DEV, fill=0x7F)
+    fk.kv_store_e4m3(cache, kd.k, kd.v, kd.slot_mapping, sk, sv)
+    rel_d = None if inp["rel"] is None else inp["rel"].to(DEV)
+    out = fk.attn_fp8_varlen_prefill(cache, inp["q"].to(DEV), inp["cu_seqlens_q"].to(DEV),
+                                     kd.seq_lens, kd.block_table, max(q_lens), sq, sk, sv,
+                                     rel_bias=rel_d, window=window)
+    torch.cuda.synchronize()
+    assert fk.device_error() == 0
+    got = out.float().cpu().numpy()
+    if rows is None:
+        rows = [(t, h) for t in range(sum(q_lens)) for h in range(Hq)]
+    ref = oracle_prefill_rows(inp, rows, sq, sk, sv, window=window, rel=inp["rel"])
+    return assert_close(np.stack([got[t, h] for t, h in rows]), ref, "prefill"), got
+
+
+def test_single_tile(fk):
+    run_case(fk, [100])
+
+
+@pytest.mark.parametrize("scales", [(1.0, 1.0, 1.0), (0.5, 0.5, 1.5)])
+def test_ragged_fresh_chunks(fk, scales):
+    run_case(fk, [1, 127, 128, 129, 300], scales=scales, E=128, seed=1)
+
+
+def test_chunk_over_cached_prefix(fk):
+    """queries are the last q_len of k_len keys (bottom-right causal)"""
+    run_case(fk, [1, 64, 128, 200], k_lens=[1, 500, 129, 777], E=1024, seed=2)
+
+
+@pytest.mark.parametrize("window", [1, 100, 512])
+def test_sliding_window(fk, window):
+    run_case(fk, [700, 50, 513], k_lens=[900, 50, 1300], window=window, E=128, seed=3)
+
+
+@pytest.mark.parametrize("bs", [32, 64, 128])
+def test_block_sizes(fk, bs):
+    run_case(fk, [130, 257], bs=bs, seed=4)
+
+
+def test_head_dim_256(fk):
+    run_case(fk, [90, 300], k_lens=[90, 450], Hq=6, Hkv=1, D=256, scales=(0.5, 0.25, 1.5),
+             E=128, seed=5)
+
+
+def test_gqa_16(fk):
+    run_case(fk, [200], Hq=16, Hkv=1, seed=6)
+
+
+def test_large_bias_row_max_jumps(fk):
+    """A bias that grows towards the diagonal makes the row maximum jump at
+    every key tile: the lazy rescale must keep P below 448 (threshold 0.75 <
+    log2(448) - 8); at the 4.0 threshold P would clip."""
+    def ramp(inp):
+        T, H, E = inp["rel"].shape
+        d = torch.arange(E, dtype=torch.float32)
+        r = (6.0 * (1.0 - d / E)).expand(T, H, E)
+        return r.to(torch.bfloat16).contiguous()
+    run_case(fk, [600, 260], k_lens=[600, 900], E=1024, seed=7, rel_override=ramp)
+
+
+def test_heavy_bias(fk):
+    run_case(fk, [400], E=512, bias_std=3.0, seed=8)
+
+
+def _full_group(fk, which):
+    spec = workloads.PREFILL_16K
+    inp = workloads.make_prefill(spec, device=DEV, seed=0)
+    kv = inp["kv"]
+    cache = fk.KVCache.empty(kv.num_blocks, kv.block_size, spec.Hkv, spec.D, device=DEV)
+    fk.kv_store_e4m3(cache, kv.k, kv.v, kv.slot_mapping, 1.0, 1.0)
+    half = spec.n_seqs // 2
+    lo, hi = (0, half) if which == 0 else (half, spec.n_seqs)
+    window = spec.windows[which]
+    cu = inp["cu_seqlens_q"].tolist()
+    cu_g = torch.tensor([c - cu[lo] for c in cu[lo:hi + 1]], dtype=torch.int32, device=DEV)
+    q_g = inp["q"][cu[lo]:cu[hi]]
+    rel_g = inp["rel"][cu[lo]:cu[hi]]
+    out = fk.attn_fp8_varlen_prefill(cache, q_g, cu_g, kv.seq_lens[lo:hi].contiguous(),
+                                     kv.block_table[lo:hi].contiguous(), max(inp["q_lens"][lo:hi]),
+                                     1.0, 1.0, 1.0, rel_bias=rel_g, window=window)
+    torch.cuda.synchronize()
+    assert fk.device_error() == 0
+    got = out.float().cpu().numpy()
+    assert np.isfinite(got).all()
+    rng = np.random.default_rng(which)
+    rows = []
+    for b in range(lo, hi):
+        s, n = cu[b] - cu[lo], inp["q_lens"][b]
+        picks = {0, 1, 127, 128, 129, n - 1, n - 2} | set(int(x) for x in rng.integers(0, n, 12))
+        rows += [(s + i, int(rng.integers(spec.Hq))) for i in sorted(picks) if 0 <= i < n]
+    g_inp = dict(inp)
+    g_inp["q"] = q_g
+    g_inp["rel"] = rel_g
+    g_inp["cu_seqlens_q"] = cu_g
+    g_inp["q_lens"] = inp["q_lens"][lo:hi]
+    g_inp["k_lens"] = inp["k_lens"][lo:hi]
+    sub = workloads.PagedKV(k=kv.k[int(kv.tok_start[lo]):int(kv.tok_start[hi])],
+                            v=kv.v[int(kv.tok_start[lo]):int(kv.tok_start[hi])],
+                            seq_lens=kv.seq_lens[lo:hi], tok_start=kv.tok_start[lo:hi + 1] -
+                            kv.tok_start[lo], block_table=kv.block_table[lo:hi],
+                            slot_mapping=kv.slot_mapping, num_blocks=kv.num_blocks,
+                            block_size=kv.block_size)
+    g_inp["kv"] = sub
+    ref = oracle_prefill_rows(g_inp, rows, 1.0, 1.0, 1.0, window=window, rel=rel_g)
+    return assert_close(np.stack([got[t, h] for t, h in rows]), ref, spec.name)
+
+
+def test_full_prefill_causal_group(fk):
+    _full_group(fk, 0)
+
+
+def test_full_prefill_window_group(fk):
+    _full_group(fk, 1)
