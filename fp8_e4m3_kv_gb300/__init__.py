@@ -54,6 +54,9 @@ _decode_ex = _sig("paged_attn_fp8_decode_ex", ctypes.c_int,
 _decode = _sig("paged_attn_fp8_decode", ctypes.c_int,
                [ctypes.POINTER(CacheStruct), P, i32, P, i32, P, i32, f32, f32, f32, f32, P,
                 i64, i32, i32, P, P, sz, P])
+_decode_noalloc = _sig("paged_attn_fp8_decode_noalloc", ctypes.c_int,
+                       [ctypes.POINTER(CacheStruct), P, i32, P, i32, P, i32, f32, f32, f32, f32,
+                        P, i64, i32, i32, P, P])
 _ws_size = _sig("fp8kv_decode_workspace_size", sz, [i32, i32, i32, i32, i32, i32, i32, i32])
 _prefill = _sig("attn_fp8_varlen_prefill", ctypes.c_int,
                 [ctypes.POINTER(CacheStruct), P, i32, P, P, P, i32, i32, i32, f32, f32, f32,
@@ -65,6 +68,7 @@ _device_error = _sig("fp8kv_device_error", ctypes.c_int, [ctypes.POINTER(ctypes.
 _status_string = _sig("fp8kv_status_string", ctypes.c_char_p, [ctypes.c_int])
 
 EXPORTED = ("kv_store_e4m3", "paged_attn_fp8_decode", "paged_attn_fp8_decode_ex",
+            "paged_attn_fp8_decode_noalloc",
             "fp8kv_decode_workspace_size", "attn_fp8_varlen_prefill", "kv_amax_calibrate",
             "fp8kv_scale_from_amax", "fp8kv_cache_bytes", "fp8kv_device_error",
             "fp8kv_status_string")
@@ -240,6 +244,30 @@ def paged_attn_fp8_decode(cache: KVCache, q: torch.Tensor, block_table: torch.Te
     return out
 
 
+def paged_attn_fp8_decode_noalloc(cache: KVCache, q: torch.Tensor, block_table: torch.Tensor,
+                                  seq_lens: torch.Tensor, q_scale: float, k_scale: float,
+                                  v_scale: float, softmax_scale: Optional[float] = None,
+                                  rel_bias: Optional[torch.Tensor] = None, window: int = 0,
+                                  out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """paged_attn_fp8_decode for callers that cannot supply a workspace: the
+    split partials go to the library's fixed 16 MiB device buffer (see
+    include/fp8kv.h).  Calls that may overlap on the GPU race on that buffer."""
+    _need(q, torch.bfloat16, "q", cache.device)
+    if q.dim() != 3 or not q.is_contiguous() or q.shape[2] != cache.head_dim:
+        raise ValueError("q must be contiguous [B][Hq][D]")
+    B, Hq, D = q.shape
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    rel, bstride, E = _bias_args(rel_bias, Hq)
+    if out is None:
+        out = torch.empty_like(q)
+    _check(_decode_noalloc(cache.c(), _ptr(q), Hq, _ptr(block_table), block_table.shape[1],
+                           _ptr(seq_lens), B, q_scale, k_scale, v_scale, softmax_scale,
+                           _ptr(rel), bstride, E, window, _ptr(out), _stream(stream)),
+           "paged_attn_fp8_decode_noalloc")
+    return out
+
+
 def attn_fp8_varlen_prefill(cache: KVCache, q: torch.Tensor, cu_seqlens_q: torch.Tensor,
                             seq_lens_k: torch.Tensor, block_table: torch.Tensor,
                             max_seqlen_q: int, q_scale: float, k_scale: float, v_scale: float,
@@ -280,5 +308,6 @@ def device_error(clear: bool = True) -> int:
 
 
 __all__ = ["KVCache", "Fp8KVError", "kv_store_e4m3", "kv_amax_calibrate", "scale_from_amax",
-           "paged_attn_fp8_decode", "attn_fp8_varlen_prefill", "decode_workspace_size",
+           "paged_attn_fp8_decode", "paged_attn_fp8_decode_noalloc", "attn_fp8_varlen_prefill",
+           "decode_workspace_size",
            "cache_bytes", "device_error", "status_string", "LIB_PATH", "EXPORTED"]

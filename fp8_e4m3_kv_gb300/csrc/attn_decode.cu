@@ -25,6 +25,8 @@
 // splits with the log-sum-exp rule and writes v_scale * o / l in bf16.
 #include <math.h>
 
+#include <mutex>
+
 #include "common.cuh"
 
 namespace fp8kv {
@@ -682,4 +684,70 @@ extern "C" fp8kv_status paged_attn_fp8_decode(
                                     seq_lens, num_seqs, q_scale, k_scale, v_scale, softmax_scale,
                                     rel_bias, bias_tok_stride, rel_extent, window, out, workspace,
                                     workspace_bytes, 0, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Decode without a caller-supplied workspace.
+//
+// Some callers cannot give the library scratch memory: an engine that hands
+// all free device memory to its KV-cache pool at start-up has none left, and a
+// latency-critical decode loop must not call cudaMalloc, which can
+// synchronize the whole device.  For them the per-split partial results live
+// in one fixed buffer compiled into the library: kNoAllocScratchBytes on every
+// GPU that loads the library, held until the process exits.
+// ---------------------------------------------------------------------------
+namespace {
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;   // 16 MiB
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void *g_noalloc_addr[kNoAllocMaxDevices];
+}  // namespace
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of the scratch buffer on the current device.  The host-side
+// name g_noalloc_scratch is only a stand-in, so the address is looked up once
+// per device (with that device current) and cached.
+static fp8kv_status noalloc_scratch(void **addr) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) {
+        cudaGetLastError();
+        return FP8KV_ERR_LAUNCH;
+    }
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+            cudaGetLastError();
+            return FP8KV_ERR_LAUNCH;
+        }
+        g_noalloc_addr[dev] = p;
+    }
+    *addr = g_noalloc_addr[dev];
+    return FP8KV_OK;
+}
+
+extern "C" fp8kv_status paged_attn_fp8_decode_noalloc(
+    const fp8kv_cache *cache, const fp8kv_bf16 *q, int32_t num_q_heads, const int32_t *block_table,
+    int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t num_seqs, float q_scale,
+    float k_scale, float v_scale, float softmax_scale, const fp8kv_bf16 *rel_bias,
+    int64_t bias_tok_stride, int32_t rel_extent, int32_t window, fp8kv_bf16 *out, void *stream) {
+    // Argument and device checks of the regular entry point: with no workspace
+    // it stops at the workspace check when everything else is valid.
+    fp8kv_status st = paged_attn_fp8_decode_ex(
+        cache, q, num_q_heads, block_table, max_blocks_per_seq, seq_lens, num_seqs, q_scale,
+        k_scale, v_scale, softmax_scale, rel_bias, bias_tok_stride, rel_extent, window, out,
+        nullptr, 0, 0, stream);
+    if (st != FP8KV_ERR_WORKSPACE) return st;   // an error, or nothing to do
+    const size_t need = fp8kv_decode_workspace_size(num_seqs, num_q_heads, cache->num_kv_heads,
+                                                    cache->head_dim, max_blocks_per_seq,
+                                                    cache->block_size, window, 0);
+    if (need == 0 || need > kNoAllocScratchBytes) return FP8KV_ERR_WORKSPACE;
+    void *scratch = nullptr;
+    st = noalloc_scratch(&scratch);
+    if (st != FP8KV_OK) return st;
+    return paged_attn_fp8_decode_ex(cache, q, num_q_heads, block_table, max_blocks_per_seq,
+                                    seq_lens, num_seqs, q_scale, k_scale, v_scale, softmax_scale,
+                                    rel_bias, bias_tok_stride, rel_extent, window, out, scratch,
+                                    kNoAllocScratchBytes, 0, stream);
 }

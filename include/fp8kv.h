@@ -146,6 +146,36 @@ fp8kv_status paged_attn_fp8_decode_ex(const fp8kv_cache *cache, const fp8kv_bf16
                                       void *workspace, size_t workspace_bytes,
                                       int32_t split_tokens, void *stream);
 
+/*
+ * paged_attn_fp8_decode_noalloc -- paged_attn_fp8_decode for callers that
+ * cannot provide a workspace.  (The pages describe no such call; it exists
+ * for users of this library.)  Some callers cannot allocate device memory at
+ * all: an engine that gives every free byte of HBM to its KV-cache pool at
+ * start-up has nothing left to lend, and a latency-critical decode loop must
+ * not call cudaMalloc, which can synchronize the device.  This entry point
+ * keeps the per-split partial results in one fixed 16 MiB buffer that is part
+ * of the library's device image (every GPU that loads the library holds it
+ * until the process exits) and allocates nothing.
+ *   - Arguments, layout and results are those of paged_attn_fp8_decode.
+ *   - Returns FP8KV_ERR_WORKSPACE when the sizes would need more than the
+ *     16 MiB buffer (fp8kv_decode_workspace_size(..., split_tokens = 0)
+ *     larger than 16 MiB).
+ *   - The first call on a device looks up the buffer's device address (a
+ *     CUDA runtime query); make that first call before any stream capture.
+ *   - Every call on a device shares the one buffer and may overwrite what
+ *     the previous call left there; nothing in it needs clearing between
+ *     calls.  Calls that can overlap on the GPU (on different streams, or
+ *     from different threads) race on it: serialize them.
+ */
+fp8kv_status paged_attn_fp8_decode_noalloc(const fp8kv_cache *cache, const fp8kv_bf16 *q,
+                                           int32_t num_q_heads, const int32_t *block_table,
+                                           int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                                           int32_t num_seqs, float q_scale, float k_scale,
+                                           float v_scale, float softmax_scale,
+                                           const fp8kv_bf16 *rel_bias, int64_t bias_tok_stride,
+                                           int32_t rel_extent, int32_t window, fp8kv_bf16 *out,
+                                           void *stream);
+
 /* Workspace bytes paged_attn_fp8_decode(_ex) needs for these sizes (split_tokens
  * as in _ex; 0 = automatic).  Returns 0 for invalid sizes. */
 size_t fp8kv_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads,
