@@ -108,24 +108,24 @@ def _need(t: torch.Tensor, dtype, name: str, device=None):
 
 class KVCache:
     """The paged e4m3 cache: K and V uint8 tensors
-    [num_blocks][block_size][num_kv_heads][head_dim], each byte an e4m3 code."""
+    [num_blocks][num_kv_heads][block_size][head_dim], each byte an e4m3 code."""
 
     def __init__(self, k: torch.Tensor, v: torch.Tensor):
         if k.shape != v.shape or k.dim() != 4:
-            raise ValueError("k and v must be [num_blocks][block_size][num_kv_heads][head_dim]")
+            raise ValueError("k and v must be [num_blocks][num_kv_heads][block_size][head_dim]")
         _need(k, torch.uint8, "cache k")
         _need(v, torch.uint8, "cache v")
         if not (k.is_contiguous() and v.is_contiguous()):
             raise ValueError("cache arrays must be contiguous")
         self.k, self.v = k, v
-        self.num_blocks, self.block_size, self.num_kv_heads, self.head_dim = k.shape
+        self.num_blocks, self.num_kv_heads, self.block_size, self.head_dim = k.shape
         self._c = CacheStruct(k.data_ptr(), v.data_ptr(), self.num_blocks, self.block_size,
                               self.num_kv_heads, self.head_dim)
 
     @classmethod
     def empty(cls, num_blocks, block_size, num_kv_heads, head_dim, device="cuda",
               fill: int = 0) -> "KVCache":
-        shape = (num_blocks, block_size, num_kv_heads, head_dim)
+        shape = (num_blocks, num_kv_heads, block_size, head_dim)
         k = torch.full(shape, fill, dtype=torch.uint8, device=device)
         v = torch.full(shape, fill, dtype=torch.uint8, device=device)
         return cls(k, v)

@@ -91,11 +91,13 @@ bool make_cache_map(CUtensorMap *map, const uint8_t *base, int64_t num_blocks, i
             cudaGetLastError();
     });
     if (!g_encode_tiled) return false;
-    const cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)num_kv_heads,
-                                (cuuint64_t)block_size, (cuuint64_t)num_blocks};
-    const cuuint64_t strides[3] = {(cuuint64_t)head_dim, (cuuint64_t)num_kv_heads * head_dim,
-                                   (cuuint64_t)block_size * num_kv_heads * head_dim};
-    const cuuint32_t box[4] = {128u, 1u, (cuuint32_t)block_size, 1u};
+    // cache[block][head][row][d] as (d, row, head, block); one box is one
+    // head's block_size rows x 128 bytes, a contiguous run of the cache
+    const cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)block_size,
+                                (cuuint64_t)num_kv_heads, (cuuint64_t)num_blocks};
+    const cuuint64_t strides[3] = {(cuuint64_t)head_dim, (cuuint64_t)block_size * head_dim,
+                                   (cuuint64_t)num_kv_heads * block_size * head_dim};
+    const cuuint32_t box[4] = {128u, (cuuint32_t)block_size, 1u, 1u};
     const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
     CUresult r = g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<uint8_t *>(base),
                                 dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,

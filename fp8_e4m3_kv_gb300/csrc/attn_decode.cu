@@ -4,25 +4,28 @@
 // full-causal or sliding-window layers).
 //
 // One CTA handles one (split of the key range, KV head, sequence) and all
-// query heads of that KV head (the GQA group, padded to 16).  The work is
-// streamed in tiles of 128 keys:
-//   warp 4  (producer)  TMA-loads the K and V tiles of the split's blocks
-//                       (one box of block_size rows x 128 bytes per block and
-//                       128-byte column) into a 3-stage ring;
-//   warp 5  (MMA)       one thread issues the tcgen05 FP8 MMAs:
-//                       S^T[key][head] = K_tile . Q8^T             (M=128, N=16)
-//                       O^T[d][head]  = V_tile^T . (P_hi + P_lo)^T  (M=128, N=16)
-//                       into TMEM (S and O double-buffered);
-//   warps 0-3 (softmax) thread t owns key row t of S^T and value row d = t of
-//                       O^T: it applies the folded descale and the bias,
-//                       masks, keeps the running max per head (block-wide
-//                       max through warp shuffles), forms P, and
-//                       accumulates O in registers with the online rescale.
-// P is exp2(z - m + 8) (at most 256) split into two e4m3 terms,
-// P_hi = e4m3(P) and P_lo = e4m3(P - P_hi), so the PV product runs on the FP8
-// tensor cores while the weights keep ~8 significant bits.  The partial
-// (o, m, l) of each split go to the workspace; a second kernel merges the
-// splits with the log-sum-exp rule and writes v_scale * o / l in bf16.
+// query heads of that KV head (the GQA group, padded to 16).  Keys stream in
+// tiles of 128:
+//   producer warp   TMA-loads the K and V tiles of the split's blocks (one box
+//                   of block_size rows x 128 bytes per block and 128-byte
+//                   column) into a ring of stages;
+//   MMA warp        one thread issues the tcgen05 FP8 MMAs:
+//                     S^T[key][head] = K_tile . Q8^T              (M=128, N=16)
+//                     O^T[d][head]  = V_tile^T . (P_hi + P_lo)^T   (M=128, N=16)
+//                   into TMEM (S^T double-, O^T triple-buffered);
+//   consumer        thread t owns key row t of S^T and value row d = t of
+//   warpgroups      O^T; warpgroup hs takes its share of the query heads:
+//                   folded descale, bias, mask, block-wide max per head
+//                   (warp shuffles and a 4-warp exchange), P, and O
+//                   accumulated in registers with the online rescale, two
+//                   tiles behind the MMAs.
+// The per-tile chain is latency-bound; splitting the heads over warpgroups
+// halves each thread's serial work.  P is exp2(z - m + 8) (at most 256) split
+// into two e4m3 terms, P_hi = e4m3(P) and P_lo = e4m3(P - P_hi), so the PV
+// product runs on the FP8 tensor cores while the weights keep ~8 significant
+// bits.  The partial (o, m, l) of each split goes to the workspace; a second
+// kernel merges the splits with the log-sum-exp rule and writes
+// v_scale * o / l in bf16.
 #include <math.h>
 
 #include <mutex>
@@ -32,17 +35,22 @@
 namespace fp8kv {
 namespace {
 
-constexpr int kDecThreads = 192;   // warps 0-3 softmax, warp 4 producer, warp 5 MMA
 constexpr int kNPad = 16;          // query heads per KV head, padded to the MMA N
 constexpr float kLog2e = 1.4426950408889634f;
 
-// Pipeline depth and resident CTAs per SM of the decode kernel (tuning
-// knobs, fixed at build time).
+// Consumer warpgroups, pipeline depth, keys per tile and resident CTAs per SM
+// (tuning knobs, fixed at build time).
+#ifndef FP8KV_DECODE_HS
+#define FP8KV_DECODE_HS 2
+#endif
 #ifndef FP8KV_DECODE_STAGES_D128
 #define FP8KV_DECODE_STAGES_D128 3
 #endif
 #ifndef FP8KV_DECODE_CTAS_D128
 #define FP8KV_DECODE_CTAS_D128 2
+#endif
+#ifndef FP8KV_DECODE_KEYS_D128
+#define FP8KV_DECODE_KEYS_D128 128
 #endif
 #ifndef FP8KV_DECODE_STAGES_D256
 #define FP8KV_DECODE_STAGES_D256 3
@@ -51,20 +59,41 @@ constexpr float kLog2e = 1.4426950408889634f;
 template <int D>
 struct DecCfg {
     static constexpr int kCB = D / 128;               // 128-byte column blocks per row
+    // consumer warpgroups; warpgroup hs owns query heads [hs*GH, (hs+1)*GH) of
+    // the group, GH = GMAX / kHS, for every key of the tile
+    static constexpr int kHS = FP8KV_DECODE_HS;
     static constexpr int kStages = D == 128 ? FP8KV_DECODE_STAGES_D128 : FP8KV_DECODE_STAGES_D256;
     static constexpr int kCtasPerSm = D == 128 ? FP8KV_DECODE_CTAS_D128 : 1;
-    static constexpr int kTileBytes = kTile * D;      // one K (or V) tile
+    static constexpr int kConsumers = kHS * 128;
+    static constexpr int kThreads = kConsumers + 64;
+    static constexpr int kProducerWarp = kHS * 4;
+    static constexpr int kMmaWarp = kHS * 4 + 1;
+    // keys per tile (a multiple of 128: one QK MMA with M = 128 per 128 keys)
+    static constexpr int kKeys = D == 128 ? FP8KV_DECODE_KEYS_D128 : 128;
+    static constexpr int kKB = kKeys / 128;           // 128-key sub-tiles (QK MMAs, M = 128)
+    static constexpr int kCBBytes = kKeys * 128;      // one 128-byte column block of a tile
+    static constexpr int kTileBytes = kKeys * D;      // one K (or V) tile
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kQBytes = kNPad * D;         // Q8: 16 rows x D bytes
-    static constexpr int kPBytes = kNPad * kTile;     // one P term: 16 rows x 128 keys
+    static constexpr int kPBytes = kNPad * kKeys;     // one P term: 16 rows x kKeys keys
+    // P and O^T buffers: a tile's O^T is read back two tiles later, so the
+    // PV latency stays off the softmax chain
+    static constexpr int kOBuf = 3;
     static constexpr int kOffQ = kStages * kStageBytes;
-    static constexpr int kOffP = kOffQ + kQBytes;     // [2 buffers][hi, lo]
-    static constexpr int kOffMisc = kOffP + 4 * kPBytes;
-    static constexpr int kMiscBytes = 1024;
+    static constexpr int kOffP = kOffQ + kQBytes;     // [kOBuf][hi, lo]
+    static constexpr int kOffMisc = kOffP + kOBuf * 2 * kPBytes;
+    // misc: barriers, tmem slot, abort flag, then per warpgroup the tile-max
+    // exchange [2][4][16] and row-sum exchange [4][16] floats
+    static constexpr int kOffRed = 512;
+    static constexpr int kMiscBytes = kOffRed + kHS * 768;
     static constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;   // + alignment slack
-    static constexpr uint32_t kTmemCols = 128;
-    static constexpr uint32_t kColS = 0;              // S^T buffers: cols 0, 16
-    static constexpr uint32_t kColO = 32;             // O^T buffers: 32 + buf*16*kCB + half*16
+    // TMEM: S^T 2 buffers x kKB x 16 columns, then O^T kOBuf buffers x kCB x 16
+    static constexpr uint32_t kColO = 2 * kKB * kNPad;
+    static constexpr uint32_t kCols = kColO + kOBuf * kCB * kNPad + kNPad;   // + over-read room
+    static constexpr uint32_t kTmemCols = kCols <= 64 ? 64 : kCols <= 128 ? 128 : 256;
+    static_assert(kCols <= 256, "TMEM columns");
+    static_assert(kStages >= 2 && kStages <= 8, "stages");
+    static_assert(kHS >= 1 && kHS <= 4, "head split");
 };
 
 struct DecodeParams {
@@ -84,7 +113,7 @@ struct DecodeParams {
     int32_t rel_extent;
     int32_t window;
     int32_t split_tiles;
-    int32_t num_splits;
+    int32_t num_slots;      // partial slots per (sequence, head) = splits
     float q_scale;
     float score_log2;       // softmax_scale * q_scale * k_scale * log2(e)
 };
@@ -118,27 +147,32 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, CtaFai
 }
 
 template <int D, int GMAX>
-__global__ void __launch_bounds__(kDecThreads, DecCfg<D>::kCtasPerSm)
+__global__ void __launch_bounds__(DecCfg<D>::kThreads, DecCfg<D>::kCtasPerSm)
 decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
               const DecodeParams p) {
     using C = DecCfg<D>;
+    constexpr int HS = C::kHS;
+    constexpr int GH = GMAX / HS;                      // heads per consumer warpgroup
+    static_assert(GH * HS == GMAX && GH >= 1, "head split");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    // KV heads fastest: the CTAs of one split read neighbouring cache blocks
+    // at about the same time
+    const int kvh = blockIdx.x, split = blockIdx.y, b = blockIdx.z;
     const int h0 = kvh * p.G;
     const int64_t len = p.seq_lens[b];
     const int64_t lo = (p.window > 0 && len > p.window) ? len - p.window : 0;
-    const int64_t t0 = lo / kTile + static_cast<int64_t>(split) * p.split_tiles;
-    const int64_t t_end = (len + kTile - 1) / kTile;
+    const int64_t t0 = lo / C::kKeys + static_cast<int64_t>(split) * p.split_tiles;
+    const int64_t t_end = (len + C::kKeys - 1) / C::kKeys;
     const int ntiles = static_cast<int>(t_end - t0 < p.split_tiles ? t_end - t0 : p.split_tiles);
 
     if (ntiles <= 0) {   // nothing to attend in this split: mark it empty
         if (threadIdx.x < p.G) {
             float *ml = p.part_ml + ((static_cast<int64_t>(b) * p.Hq + h0 + threadIdx.x) *
-                                         p.num_splits + split) * 2;
+                                         p.num_slots + split) * 2;
             ml[0] = -INFINITY;
             ml[1] = 0.0f;
         }
@@ -146,21 +180,18 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
     }
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffMisc);
-    static_assert(C::kStages <= 4, "barrier area holds at most 4 stages");
     uint64_t *full = bars;          // [kStages] TMA landed
-    uint64_t *empty = bars + 4;     // [kStages] stage consumed (MMA commit)
-    uint64_t *s_full = bars + 8;    // [2] S^T in TMEM
-    uint64_t *s_free = bars + 10;   // [2] S^T read by the softmax warps
-    uint64_t *p_full = bars + 12;   // [2] P written to shared memory
-    uint64_t *o_full = bars + 14;   // [2] O^T in TMEM
-    uint64_t *o_free = bars + 16;   // [2] O^T read by the softmax warps
-    uint64_t *mma_done = bars + 18; // teardown: all MMAs complete
-    uint64_t *red_bar = bars + 19;  // [2] the 4 softmax warps' tile maxima are in `red`
-    uint64_t *l_bar = bars + 21;    // the 4 softmax warps' row sums are in `lred`
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc + 192);
-    CtaFail *fail = reinterpret_cast<CtaFail *>(smem + C::kOffMisc + 196);
-    float *red = reinterpret_cast<float *>(smem + C::kOffMisc + 256);   // [2][4][16]
-    float *lred = red + 128;                                             // [4][16]
+    uint64_t *empty = bars + 8;     // [kStages] stage consumed (PV committed)
+    uint64_t *s_full = bars + 16;   // [2] S^T in TMEM
+    uint64_t *s_free = bars + 18;   // [2] S^T read by all consumer warps
+    uint64_t *p_full = bars + 20;   // [3] P in shared memory
+    uint64_t *o_full = bars + 23;   // [3] O^T in TMEM
+    uint64_t *o_free = bars + 26;   // [3] O^T read by all consumer warps
+    uint64_t *mma_done = bars + 29; // teardown: all MMAs complete
+    // per warpgroup hs: red_bar[2] at bars + 30 + 3*hs, l_bar at + 2
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc + 480);
+    CtaFail *fail = reinterpret_cast<CtaFail *>(smem + C::kOffMisc + 484);
+    static_assert(30 + 3 * 4 <= 60, "barrier area");
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
@@ -169,23 +200,28 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
-            mbar_init(&s_free[i], 4);
-            mbar_init(&p_full[i], 4);
+            mbar_init(&s_free[i], 4 * HS);
+        }
+        for (int i = 0; i < 3; ++i) {
+            mbar_init(&p_full[i], 4 * HS);
             mbar_init(&o_full[i], 1);
-            mbar_init(&o_free[i], 4);
-            mbar_init(&red_bar[i], 4);
+            mbar_init(&o_free[i], 4 * HS);
         }
         mbar_init(mma_done, 1);
-        mbar_init(l_bar, 4);
+        for (int hs = 0; hs < HS; ++hs) {
+            mbar_init(bars + 30 + 3 * hs, 4);
+            mbar_init(bars + 31 + 3 * hs, 4);
+            mbar_init(bars + 32 + 3 * hs, 4);
+        }
         fail->abort = 0;
         fence_mbar_init();
     }
-    if (warp == 5) tmem_alloc(tmem_slot, C::kTmemCols);
-    if (warp < 4) {
+    if (warp == C::kMmaWarp) tmem_alloc(tmem_slot, C::kTmemCols);
+    if (warp < 4 * HS) {
         // Q8 = e4m3(q / q_scale) for the group's heads, rows >= G zero;
         // 128-byte swizzled, K-major (row = head, D bytes per row).
         uint8_t *q8 = smem + C::kOffQ;
-        for (int e = threadIdx.x * 8; e < kNPad * D; e += 128 * 8) {
+        for (int e = threadIdx.x * 8; e < kNPad * D; e += C::kConsumers * 8) {
             const int g = e / D, d = e % D;
             uint2 packed = make_uint2(0u, 0u);
             if (g < p.G) {
@@ -197,23 +233,26 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
             *reinterpret_cast<uint2 *>(q8 + (d / 128) * (kNPad * 128) + sw128_offset(g, d % 128)) =
                 packed;
         }
+    }
+    if (warp == C::kProducerWarp) {
+        // zero the P buffers: rows past the group are never written
         uint4 *pz = reinterpret_cast<uint4 *>(smem + C::kOffP);
-        for (int i = threadIdx.x; i < 4 * C::kPBytes / 16; i += 128) pz[i] = make_uint4(0, 0, 0, 0);
-        fence_proxy_async_smem();
+        for (int i = lane; i < C::kOBuf * 2 * C::kPBytes / 16; i += 32) pz[i] = make_uint4(0, 0, 0, 0);
+        if (lane == 0) {
+            tma_prefetch_map(&kmap);
+            tma_prefetch_map(&vmap);
+        }
     }
-    if (warp == 4 && lane == 0) {
-        tma_prefetch_map(&kmap);
-        tma_prefetch_map(&vmap);
-    }
+    fence_proxy_async_smem();
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 4) {
+    if (warp == C::kProducerWarp) {
         // ------------------------------------------------------------ producer
         const uint64_t pol = l2_policy_evict_first();
-        const int nb = kTile / p.block_size;   // blocks per tile (1..8)
+        const int nb = C::kKeys / p.block_size;   // blocks per tile (<= 16)
         int last_issued[C::kStages];
 #pragma unroll
         for (int s = 0; s < C::kStages; ++s) last_issued[s] = -1;
@@ -241,8 +280,8 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
                 uint8_t *vdst = kdst + C::kTileBytes;
 #pragma unroll
                 for (int cb = 0; cb < C::kCB; ++cb) {
-                    tma_load_4d(kdst + cb * (kTile * 128), &kmap, &full[s], cb * 128, kvh, 0, phys, pol);
-                    tma_load_4d(vdst + cb * (kTile * 128), &vmap, &full[s], cb * 128, kvh, 0, phys, pol);
+                    tma_load_4d(kdst + cb * C::kCBBytes, &kmap, &full[s], cb * 128, 0, kvh, phys, pol);
+                    tma_load_4d(vdst + cb * C::kCBBytes, &vmap, &full[s], cb * 128, 0, kvh, phys, pol);
                 }
             }
             last_issued[s] = i;
@@ -251,8 +290,10 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
             for (int s = 0; s < C::kStages; ++s)
                 if (last_issued[s] >= 0) mbar_drain(&full[s], (last_issued[s] / C::kStages) & 1, p.err);
         }
-    } else if (warp == 5) {
+    } else if (warp == C::kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
+        // Step i issues QK of tile i, then PV of tile i - 1 (whose P the
+        // consumers produced while QK of tile i was in flight).
         if (lane == 0) {
             const uint32_t idesc_qk = idesc_e4m3_f32(128, kNPad, false, false);
             const uint32_t idesc_pv = idesc_e4m3_f32(128, kNPad, true, false);
@@ -265,34 +306,44 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
                     tc_fence_after_sync();
                     const uint32_t k_addr = smem_u32(smem + s * C::kStageBytes);
 #pragma unroll
-                    for (int kk = 0; kk < D / 32; ++kk) {
-                        const uint32_t cb = kk / 4, ko = (kk % 4) * 32;
-                        const uint64_t a = sdesc_sw128(k_addr + cb * (kTile * 128) + ko, 16, 1024);
-                        const uint64_t bd = sdesc_sw128(q_addr + cb * (kNPad * 128) + ko, 16, 1024);
-                        mma_e4m3(tmem + C::kColS + sb * kNPad, a, bd, idesc_qk, kk > 0);
+                    for (int kb = 0; kb < C::kKB; ++kb) {
+                        const uint32_t dcol = tmem + (sb * C::kKB + kb) * kNPad;
+#pragma unroll
+                        for (int kk = 0; kk < D / 32; ++kk) {
+                            const uint32_t cb = kk / 4, ko = (kk % 4) * 32;
+                            const uint64_t a = sdesc_sw128(
+                                k_addr + cb * C::kCBBytes + kb * (128 * 128) + ko, 16, 1024);
+                            const uint64_t bd =
+                                sdesc_sw128(q_addr + cb * (kNPad * 128) + ko, 16, 1024);
+                            mma_e4m3(dcol, a, bd, idesc_qk, kk > 0);
+                        }
                     }
                     tc_commit(&s_full[sb]);
                 }
                 if (i >= 1) {
-                    const int j = i - 1, s = j % C::kStages, pb = j & 1;
-                    if (!mbar_wait(&p_full[pb], (j >> 1) & 1, fail, p.err)) break;
-                    if (!mbar_wait(&o_free[pb], ((j >> 1) & 1) ^ 1, fail, p.err)) break;
+                    const int j = i - 1, s = j % C::kStages;
+                    const int pb = j % C::kOBuf, ph = (j / C::kOBuf) & 1;
+                    if (!mbar_wait(&p_full[pb], ph, fail, p.err)) break;
+                    if (!mbar_wait(&o_free[pb], ph ^ 1, fail, p.err)) break;
                     tc_fence_after_sync();
                     const uint32_t v_addr = smem_u32(smem + s * C::kStageBytes + C::kTileBytes);
                     const uint32_t p_addr = smem_u32(smem + C::kOffP + pb * 2 * C::kPBytes);
 #pragma unroll
                     for (int mh = 0; mh < C::kCB; ++mh) {
-                        const uint32_t dcol = tmem + C::kColO + pb * kNPad * C::kCB + mh * kNPad;
+                        const uint32_t dcol = tmem + C::kColO + (pb * C::kCB + mh) * kNPad;
 #pragma unroll
                         for (int part = 0; part < 2; ++part) {
 #pragma unroll
-                            for (int kk = 0; kk < 4; ++kk) {
-                                // V tile, MN-major: rows are keys (128 bytes of d each),
-                                // 8-row groups 1024 bytes apart; 32 keys per MMA.
+                            for (int kk = 0; kk < C::kKeys / 32; ++kk) {
+                                // V tile, MN-major: rows are keys (128 bytes of d
+                                // each), 8-row groups 1024 bytes apart; 32 keys per
+                                // MMA.  P: 16 rows of kKeys bytes in 128-byte
+                                // column blocks of 2 KB.
                                 const uint64_t a = sdesc_sw128(
-                                    v_addr + mh * (kTile * 128) + kk * 32 * 128, kTile * 128, 1024);
-                                const uint64_t bd =
-                                    sdesc_sw128(p_addr + part * C::kPBytes + kk * 32, 16, 1024);
+                                    v_addr + mh * C::kCBBytes + kk * 32 * 128, C::kCBBytes, 1024);
+                                const uint64_t bd = sdesc_sw128(
+                                    p_addr + part * C::kPBytes + (kk / 4) * (kNPad * 128) + (kk % 4) * 32,
+                                    16, 1024);
                                 mma_e4m3(dcol, a, bd, idesc_pv, (part | kk) != 0);
                             }
                         }
@@ -306,139 +357,175 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------------------ softmax
-        const int t = threadIdx.x;                       // key row / value row
-        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+        // ------------------------------------------------------------ consumers
+        const int hs = warp >> 2, wq = warp & 3;            // warpgroup (head half), TMEM quadrant
+        const int t = threadIdx.x & 127;                    // key row / value row
+        const int gbase = hs * GH;                          // this warpgroup's first head
+        uint64_t *red_bar = bars + 30 + 3 * hs, *l_bar = bars + 32 + 3 * hs;
+        float *red = reinterpret_cast<float *>(smem + C::kOffMisc + C::kOffRed + hs * 768);  // [2][4][16]
+        float *lred = red + 128;                                                          // [4][16]
+        const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
         const uint16_t *bias = p.rel ? p.rel + static_cast<int64_t>(b) * p.bias_tok_stride +
-                                           static_cast<int64_t>(h0) * p.rel_extent
+                                           static_cast<int64_t>(h0 + gbase) * p.rel_extent
                                      : nullptr;
-        float m_run[GMAX], l_part[GMAX], alpha_prev[GMAX], o_acc[C::kCB][GMAX];
+        bool ok = true;
+
+        // rescale factors of the two previous tiles (a tile's O^T is taken two
+        // tiles later): alpha_1 of tile j - 1, alpha_2 of tile j - 2
+        float m_run[GH], l_part[GH], alpha_1[GH], alpha_2[GH], o_acc[C::kCB][GH];
 #pragma unroll
-        for (int g = 0; g < GMAX; ++g) {
+        for (int g = 0; g < GH; ++g) {
             m_run[g] = -INFINITY;
             l_part[g] = 0.0f;
-            alpha_prev[g] = 1.0f;
+            alpha_1[g] = alpha_2[g] = 1.0f;
 #pragma unroll
             for (int mh = 0; mh < C::kCB; ++mh) o_acc[mh][g] = 0.0f;
         }
-        bool ok = true;
-        // Accumulate O^T of tile j (rescaled by alpha) into the registers.
+        // Accumulate this warpgroup's heads of O^T of tile j (rescaled) into
+        // the registers.
         auto take_o = [&](int j, const float *alpha) -> bool {
-            const int pb = j & 1;
-            if (!warp_wait(&o_full[pb], (j >> 1) & 1, fail, p.err)) return false;
+            const int ob = j % C::kOBuf;
+            if (!warp_wait(&o_full[ob], (j / C::kOBuf) & 1, fail, p.err)) return false;
             tc_fence_after_sync();
 #pragma unroll
             for (int mh = 0; mh < C::kCB; ++mh) {
                 float o[16];
-                tmem_ld_x16(tmem + lane_base + C::kColO + pb * kNPad * C::kCB + mh * kNPad, o);
+                tmem_ld_x16(tmem + lane_base + C::kColO + (ob * C::kCB + mh) * kNPad + gbase, o);
 #pragma unroll
-                for (int g = 0; g < GMAX; ++g) o_acc[mh][g] = fmaf(o_acc[mh][g], alpha[g], o[g]);
+                for (int g = 0; g < GH; ++g) o_acc[mh][g] = fmaf(o_acc[mh][g], alpha[g], o[g]);
             }
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&o_free[pb]);
+            if (lane == 0) mbar_arrive(&o_free[ob]);
             return true;
         };
+
         for (int i = 0; i < ntiles; ++i) {
-            const int sb = i & 1;
-            if (!warp_wait(&s_full[sb], (i >> 1) & 1, fail, p.err)) { ok = false; break; }
+            if (!warp_wait(&s_full[i & 1], (i >> 1) & 1, fail, p.err)) { ok = false; break; }
             tc_fence_after_sync();
-            float sc[16];
-            tmem_ld_x16(tmem + lane_base + C::kColS + sb * kNPad, sc);
+            float sc[C::kKB][16];
+#pragma unroll
+            for (int kb = 0; kb < C::kKB; ++kb)
+                tmem_ld_x16(tmem + lane_base + ((i & 1) * C::kKB + kb) * kNPad + gbase, sc[kb]);
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&s_free[sb]);
+            if (lane == 0) mbar_arrive(&s_free[i & 1]);
 
-            const int64_t j = (t0 + i) * kTile + t;       // key position
-            const bool valid = j < len && j >= lo;
-            const int64_t dist = len - 1 - j;
-            const bool has_bias = bias && valid && dist < p.rel_extent;
-            float z[GMAX];
+            // this thread's keys: t, t + 128, ... of the tile
+            float z[C::kKB][GH];
+            bool any_past_end = false;
 #pragma unroll
-            for (int g = 0; g < GMAX; ++g) {
-                float zz = -INFINITY;
-                if (valid && g < p.G) {
-                    zz = sc[g] * p.score_log2;
-                    if (has_bias) zz = fmaf(bf16_bits_to_float(__ldg(bias + g * p.rel_extent + dist)),
-                                            kLog2e, zz);
+            for (int kb = 0; kb < C::kKB; ++kb) {
+                const int64_t key = (t0 + i) * C::kKeys + kb * 128 + t;
+                const bool valid = key < len && key >= lo;
+                any_past_end |= key >= len;
+                const int64_t dist = len - 1 - key;
+                const bool has_bias = bias && valid && dist < p.rel_extent;
+#pragma unroll
+                for (int g = 0; g < GH; ++g) {
+                    float zz = -INFINITY;
+                    if (valid && gbase + g < p.G) {
+                        zz = sc[kb][g] * p.score_log2;
+                        if (has_bias)
+                            zz = fmaf(bf16_bits_to_float(__ldg(bias + g * p.rel_extent + dist)),
+                                      kLog2e, zz);
+                    }
+                    z[kb][g] = zz;
                 }
-                z[g] = zz;
             }
-            // block-wide max per head: warp shuffles, then the 4 warps via
-            // shared memory and a (bounded) mbarrier exchange
+            // block-wide max per head: warp shuffles, then the 4 warps of the
+            // warpgroup via shared memory and a (bounded) mbarrier exchange
             float *rb = red + (i & 1) * 64;
 #pragma unroll
-            for (int g = 0; g < GMAX; ++g) {
-                const float mx = warp_max(z[g]);
-                if (lane == 0) rb[warp * 16 + g] = mx;
+            for (int g = 0; g < GH; ++g) {
+                float mx = z[0][g];
+#pragma unroll
+                for (int kb = 1; kb < C::kKB; ++kb) mx = fmaxf(mx, z[kb][g]);
+                mx = warp_max(mx);
+                if (lane == 0) rb[wq * 16 + g] = mx;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&red_bar[i & 1]);
             if (!warp_wait(&red_bar[i & 1], (i >> 1) & 1, fail, p.err)) { ok = false; break; }
-            float alpha[GMAX];
-            uint8_t *phi = smem + C::kOffP + sb * 2 * C::kPBytes;
+            float alpha[GH];
+            uint8_t *phi = smem + C::kOffP + (i % C::kOBuf) * 2 * C::kPBytes;
             uint8_t *plo = phi + C::kPBytes;
 #pragma unroll
-            for (int g = 0; g < GMAX; ++g) {
+            for (int g = 0; g < GH; ++g) {
                 const float tile_max =
                     fmaxf(fmaxf(rb[g], rb[16 + g]), fmaxf(rb[32 + g], rb[48 + g]));
                 const float m_new = fmaxf(m_run[g], tile_max);
                 alpha[g] = (m_new == -INFINITY) ? 1.0f : exp2f(m_run[g] - m_new);
-                const float pv = (z[g] == -INFINITY) ? 0.0f : exp2f(z[g] - m_new + 8.0f);
-                // two-term e4m3 split of P: hi = e4m3(P), lo = e4m3(P - hi)
-                const uint16_t hi2 = f32x2_to_e4m3x2(pv, 0.0f);
-                const float hi_val = __low2float(e4m3x2_to_half2(hi2));
-                const uint16_t lo2 = f32x2_to_e4m3x2(pv - hi_val, 0.0f);
-                l_part[g] = fmaf(l_part[g], alpha[g], pv);
+                float lsum = 0.0f;
+#pragma unroll
+                for (int kb = 0; kb < C::kKB; ++kb) {
+                    const float pv = (z[kb][g] == -INFINITY) ? 0.0f : exp2f(z[kb][g] - m_new + 8.0f);
+                    // two-term e4m3 split of P: hi = e4m3(P), lo = e4m3(P - hi)
+                    const uint16_t hi2 = f32x2_to_e4m3x2(pv, 0.0f);
+                    const float hi_val = __low2float(e4m3x2_to_half2(hi2));
+                    const uint16_t lo2 = f32x2_to_e4m3x2(pv - hi_val, 0.0f);
+                    lsum += pv;
+                    const uint32_t off = kb * (kNPad * 128) + sw128_offset(gbase + g, t);
+                    phi[off] = static_cast<uint8_t>(hi2 & 0xFF);
+                    plo[off] = static_cast<uint8_t>(lo2 & 0xFF);
+                }
+                l_part[g] = fmaf(l_part[g], alpha[g], lsum);
                 m_run[g] = m_new;
-                const uint32_t off = sw128_offset(g, t);
-                phi[off] = static_cast<uint8_t>(hi2 & 0xFF);
-                plo[off] = static_cast<uint8_t>(lo2 & 0xFF);
             }
             // Keys past the sequence end may hold stale bytes (NaN codes
             // included); zero their V rows so that 0 * V stays 0 in the MMA.
-            if (j >= len) {
-                uint8_t *vrow = smem + (i % C::kStages) * C::kStageBytes + C::kTileBytes;
+            // (Warpgroup 0 does it; the PV waits for every consumer warp.)
+            if (hs == 0 && any_past_end) {
+                uint8_t *vtile = smem + (i % C::kStages) * C::kStageBytes + C::kTileBytes;
 #pragma unroll
-                for (int cb = 0; cb < C::kCB; ++cb) {
-                    uint4 *r = reinterpret_cast<uint4 *>(vrow + cb * (kTile * 128) + t * 128);
+                for (int kb = 0; kb < C::kKB; ++kb) {
+                    if ((t0 + i) * C::kKeys + kb * 128 + t < len) continue;
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) r[c] = make_uint4(0, 0, 0, 0);
+                    for (int cb = 0; cb < C::kCB; ++cb) {
+                        uint4 *r = reinterpret_cast<uint4 *>(vtile + cb * C::kCBBytes +
+                                                             (kb * 128 + t) * 128);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) r[c] = make_uint4(0, 0, 0, 0);
+                    }
                 }
             }
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full[sb]);
-            if (i >= 1 && !take_o(i - 1, alpha_prev)) { ok = false; break; }
+            if (lane == 0) mbar_arrive(&p_full[i % C::kOBuf]);
+            if (i >= 2 && !take_o(i - 2, alpha_2)) { ok = false; break; }
 #pragma unroll
-            for (int g = 0; g < GMAX; ++g) alpha_prev[g] = alpha[g];
+            for (int g = 0; g < GH; ++g) {
+                alpha_2[g] = alpha_1[g];
+                alpha_1[g] = alpha[g];
+            }
         }
-        if (ok) ok = take_o(ntiles - 1, alpha_prev);
+        if (ok && ntiles >= 2) ok = take_o(ntiles - 2, alpha_2);
+        if (ok && ntiles >= 1) ok = take_o(ntiles - 1, alpha_1);
 
-        // l per head: sum of the thread partials
+        // l per head: sum of the thread partials of the warpgroup
 #pragma unroll
-        for (int g = 0; g < GMAX; ++g) {
+        for (int g = 0; g < GH; ++g) {
             const float s = warp_sum(l_part[g]);
-            if (lane == 0) lred[warp * 16 + g] = s;
+            if (lane == 0) lred[wq * 16 + g] = s;
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(l_bar);
         if (!warp_wait(l_bar, 0, fail, p.err)) ok = false;
-        const int64_t row0 = (static_cast<int64_t>(b) * p.Hq + h0) * p.num_splits + split;
+        const int64_t row0 = (static_cast<int64_t>(b) * p.Hq + h0 + gbase) * p.num_slots + split;
         if (t == 0) {
 #pragma unroll
-            for (int g = 0; g < GMAX; ++g) {
-                if (g < p.G) {
-                    float *ml = p.part_ml + (row0 + static_cast<int64_t>(g) * p.num_splits) * 2;
+            for (int g = 0; g < GH; ++g) {
+                if (gbase + g < p.G) {
+                    float *ml = p.part_ml + (row0 + static_cast<int64_t>(g) * p.num_slots) * 2;
                     ml[0] = ok ? m_run[g] : -INFINITY;
                     ml[1] = lred[g] + lred[16 + g] + lred[32 + g] + lred[48 + g];
                 }
             }
         }
 #pragma unroll
-        for (int g = 0; g < GMAX; ++g) {
-            if (g < p.G) {
-                float *po = p.part_o + (row0 + static_cast<int64_t>(g) * p.num_splits) * D;
+        for (int g = 0; g < GH; ++g) {
+            if (gbase + g < p.G) {
+                float *po = p.part_o + (row0 + static_cast<int64_t>(g) * p.num_slots) * D;
 #pragma unroll
                 for (int mh = 0; mh < C::kCB; ++mh) po[mh * 128 + t] = o_acc[mh][g];
             }
@@ -447,7 +534,7 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
 
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == C::kMmaWarp) {
         tc_fence_after_sync();
         tmem_dealloc(tmem, C::kTmemCols);
     }
@@ -524,22 +611,23 @@ struct SplitPlan {
     int split_tiles;
 };
 
-// Split plan: enough CTAs for ~8 waves of the resident CTAs, at least 4 tiles
-// (512 keys) per split, all splits of equal length in tiles.
+// Split plan: enough CTAs for ~8 waves of the resident CTAs, at least 4096
+// keys per split, all splits of equal length in tiles.
 bool plan_splits(int32_t num_seqs, int32_t num_kv_heads, int32_t head_dim,
                  int32_t max_blocks_per_seq, int32_t block_size, int32_t window,
                  int32_t split_tokens, int num_sms, SplitPlan *plan) {
+    const int64_t keys = head_dim == 128 ? DecCfg<128>::kKeys : DecCfg<256>::kKeys;
     const int64_t max_len = static_cast<int64_t>(max_blocks_per_seq) * block_size;
-    int64_t tiles = (max_len + kTile - 1) / kTile;
+    int64_t tiles = (max_len + keys - 1) / keys;
     if (window > 0) {
-        const int64_t wt = (static_cast<int64_t>(window) - 1) / kTile + 2;
+        const int64_t wt = (static_cast<int64_t>(window) - 1) / keys + 2;
         if (wt < tiles) tiles = wt;
     }
     if (tiles < 1) tiles = 1;
     int64_t st;
     if (split_tokens > 0) {
-        if (split_tokens % kTile) return false;
-        st = split_tokens / kTile;
+        if (split_tokens % keys) return false;
+        st = split_tokens / keys;
     } else {
         const int64_t ctas_per_sm = head_dim == 128 ? DecCfg<128>::kCtasPerSm : 1;
         const int64_t target = static_cast<int64_t>(num_sms) * ctas_per_sm * 8;
@@ -547,17 +635,26 @@ bool plan_splits(int32_t num_seqs, int32_t num_kv_heads, int32_t head_dim,
         if (pairs < 1) pairs = 1;
         const int64_t want = (target + pairs - 1) / pairs;
         st = (tiles + want - 1) / want;
-        if (st < 4) st = 4;
+        // at least 4096 keys per split: each CTA's start (TMEM, barriers, q
+        // quantization, the first loads) is paid once per split
+        const int64_t min_st = (4096 + keys - 1) / keys;
+        if (st < min_st) st = min_st;
     }
     const int64_t S = (tiles + st - 1) / st;
-    if (S > (1 << 20) || st > (1 << 24)) return false;
+    if (S > 65535 || st > (1 << 24)) return false;
     plan->num_splits = static_cast<int>(S);
     plan->split_tiles = static_cast<int>(st);
     return true;
 }
 
-size_t workspace_bytes_for(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim, int S) {
-    return static_cast<size_t>(num_seqs) * num_q_heads * S * (head_dim + 2) * sizeof(float);
+// Partial-result slots per (sequence, query head): one per split.
+int slots_for(int32_t head_dim, int num_splits) {
+    (void)head_dim;
+    return num_splits;
+}
+
+size_t workspace_bytes_for(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim, int slots) {
+    return static_cast<size_t>(num_seqs) * num_q_heads * slots * (head_dim + 2) * sizeof(float);
 }
 
 template <int D, int GMAX>
@@ -570,8 +667,8 @@ fp8kv_status launch_decode(const CUtensorMap &km, const CUtensorMap &vm, const D
         cudaGetLastError();
         return FP8KV_ERR_LAUNCH;
     }
-    dim3 grid(p.num_splits, num_kv_heads, num_seqs);
-    kern<<<grid, kDecThreads, C::kSmemBytes, stream>>>(km, vm, p);
+    dim3 grid(num_kv_heads, p.num_slots, num_seqs);
+    kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(km, vm, p);
     if (cudaGetLastError() != cudaSuccess) return FP8KV_ERR_LAUNCH;
     return FP8KV_OK;
 }
@@ -594,7 +691,7 @@ extern "C" size_t fp8kv_decode_workspace_size(int32_t num_seqs, int32_t num_q_he
     if (!plan_splits(num_seqs, num_kv_heads, head_dim, max_blocks_per_seq, block_size, window,
                      split_tokens, sms, &plan))
         return 0;
-    return workspace_bytes_for(num_seqs, num_q_heads, head_dim, plan.num_splits);
+    return workspace_bytes_for(num_seqs, num_q_heads, head_dim, slots_for(head_dim, plan.num_splits));
 }
 
 extern "C" fp8kv_status paged_attn_fp8_decode_ex(
@@ -615,7 +712,7 @@ extern "C" fp8kv_status paged_attn_fp8_decode_ex(
         num_seqs > 65535 || Hkv > 65535 || num_q_heads > 65535 || cache->num_blocks >= (1ll << 31))
         return FP8KV_ERR_UNSUPPORTED;
     if (rel_bias && (rel_extent <= 0 || bias_tok_stride < 0)) return FP8KV_ERR_ARG;
-    if (split_tokens % kTile) return FP8KV_ERR_ARG;
+    if (split_tokens % (D == 128 ? DecCfg<128>::kKeys : DecCfg<256>::kKeys)) return FP8KV_ERR_ARG;
     if (num_seqs == 0) return FP8KV_OK;
     if (!q || !block_table || !seq_lens || !out || !cache->k || !cache->v) return FP8KV_ERR_ARG;
     if ((reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(cache->k) & 15) ||
@@ -627,7 +724,8 @@ extern "C" fp8kv_status paged_attn_fp8_decode_ex(
     SplitPlan plan;
     if (!plan_splits(num_seqs, Hkv, D, max_blocks_per_seq, bs, window, split_tokens, sms, &plan))
         return FP8KV_ERR_ARG;
-    const size_t need = workspace_bytes_for(num_seqs, num_q_heads, D, plan.num_splits);
+    const int slots = slots_for(D, plan.num_splits);
+    const size_t need = workspace_bytes_for(num_seqs, num_q_heads, D, slots);
     if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 15))
         return FP8KV_ERR_WORKSPACE;
     CUtensorMap km, vm;
@@ -641,7 +739,7 @@ extern "C" fp8kv_status paged_attn_fp8_decode_ex(
     p.seq_lens = seq_lens;
     p.rel = rel_bias;
     p.part_o = static_cast<float *>(workspace);
-    p.part_ml = p.part_o + static_cast<size_t>(num_seqs) * num_q_heads * plan.num_splits * D;
+    p.part_ml = p.part_o + static_cast<size_t>(num_seqs) * num_q_heads * slots * D;
     p.err = device_error_word();
     p.bias_tok_stride = bias_tok_stride;
     p.num_blocks = cache->num_blocks;
@@ -652,7 +750,7 @@ extern "C" fp8kv_status paged_attn_fp8_decode_ex(
     p.rel_extent = rel_bias ? rel_extent : 0;
     p.window = window;
     p.split_tiles = plan.split_tiles;
-    p.num_splits = plan.num_splits;
+    p.num_slots = slots;
     p.q_scale = q_scale;
     p.score_log2 = static_cast<float>(static_cast<double>(softmax_scale) * q_scale * k_scale *
                                       1.4426950408889634);
@@ -666,10 +764,10 @@ extern "C" fp8kv_status paged_attn_fp8_decode_ex(
     if (st != FP8KV_OK) return st;
     if (D == 128)
         decode_merge_kernel<128><<<dim3(num_q_heads, num_seqs), kMergeWarps * 32, 0, s>>>(
-            p.part_o, p.part_ml, out, num_q_heads, plan.num_splits, v_scale);
+            p.part_o, p.part_ml, out, num_q_heads, slots, v_scale);
     else
         decode_merge_kernel<256><<<dim3(num_q_heads, num_seqs), kMergeWarps * 32, 0, s>>>(
-            p.part_o, p.part_ml, out, num_q_heads, plan.num_splits, v_scale);
+            p.part_o, p.part_ml, out, num_q_heads, slots, v_scale);
     if (cudaGetLastError() != cudaSuccess) return FP8KV_ERR_LAUNCH;
     return FP8KV_OK;
 }

@@ -224,8 +224,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
                 uint8_t *vdst = kdst + C::kTileBytes;
 #pragma unroll
                 for (int cb = 0; cb < C::kCB; ++cb) {
-                    tma_load_4d(kdst + cb * (kTile * 128), &kmap, &full[s], cb * 128, kvh, 0, phys, pol);
-                    tma_load_4d(vdst + cb * (kTile * 128), &vmap, &full[s], cb * 128, kvh, 0, phys, pol);
+                    tma_load_4d(kdst + cb * (kTile * 128), &kmap, &full[s], cb * 128, 0, kvh, phys, pol);
+                    tma_load_4d(vdst + cb * (kTile * 128), &vmap, &full[s], cb * 128, 0, kvh, phys, pol);
                 }
             }
             last_issued[s] = i;

@@ -321,9 +321,10 @@ uint32_t *device_error_word();
 // count.  Cached per device.
 fp8kv_status check_device(int *num_sms);
 bool scale_ok(float s);
-// Tensor map over one cache array, viewed as a 4-D tensor
-// (head_dim bytes, kv heads, block rows, blocks), box (128, 1, block_size, 1),
-// 128-byte swizzle.  Returns false when the driver rejects it.
+// Tensor map over one cache array [block][head][row][d], viewed as a 4-D
+// tensor (head_dim bytes, block rows, kv heads, blocks), box
+// (128, block_size, 1, 1), 128-byte swizzle.  Returns false when the driver
+// rejects it.
 bool make_cache_map(CUtensorMap *map, const uint8_t *base, int64_t num_blocks, int block_size,
                     int num_kv_heads, int head_dim);
 

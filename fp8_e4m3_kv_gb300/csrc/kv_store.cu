@@ -28,8 +28,9 @@ __device__ __forceinline__ uint4 quantize16(const uint4 lo, const uint4 hi, floa
 __global__ void __launch_bounds__(kStoreThreads)
 kv_store_kernel(const uint16_t *__restrict__ k, const uint16_t *__restrict__ v, int64_t k_stride,
                 int64_t v_stride, const int64_t *__restrict__ slots, int64_t num_tokens,
-                int32_t row_elems, int64_t capacity, uint8_t *__restrict__ ck,
-                uint8_t *__restrict__ cv, float k_scale, float v_scale, uint32_t *err) {
+                int32_t row_elems, int32_t head_dim, int32_t num_kv_heads, int32_t block_size,
+                int64_t capacity, uint8_t *__restrict__ ck, uint8_t *__restrict__ cv,
+                float k_scale, float v_scale, uint32_t *err) {
     const int32_t chunks = row_elems / kChunk;
     const int64_t total = num_tokens * chunks;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
@@ -46,7 +47,10 @@ kv_store_kernel(const uint16_t *__restrict__ k, const uint16_t *__restrict__ v, 
         const uint4 *vs = reinterpret_cast<const uint4 *>(v + t * v_stride + c * kChunk);
         const uint4 k0 = __ldcs(ks), k1 = __ldcs(ks + 1);
         const uint4 v0 = __ldcs(vs), v1 = __ldcs(vs + 1);
-        const int64_t dst = slot * row_elems + c * kChunk;
+        // cache[block][head][row][d]: head h's row of the block
+        const int32_t e = c * kChunk, h = e / head_dim, d = e - h * head_dim;
+        const int64_t blk = slot / block_size, row = slot - blk * block_size;
+        const int64_t dst = ((blk * num_kv_heads + h) * block_size + row) * head_dim + d;
         *reinterpret_cast<uint4 *>(ck + dst) = quantize16(k0, k1, k_scale);
         *reinterpret_cast<uint4 *>(cv + dst) = quantize16(v0, v1, v_scale);
     }
@@ -132,7 +136,8 @@ extern "C" fp8kv_status kv_store_e4m3(const fp8kv_cache *cache, const fp8kv_bf16
         cache->head_dim <= 0)
         return FP8KV_ERR_ARG;
     const int64_t row = static_cast<int64_t>(cache->num_kv_heads) * cache->head_dim;
-    if (row % kChunk != 0 || row > (1 << 30)) return FP8KV_ERR_UNSUPPORTED;
+    if (row % kChunk != 0 || cache->head_dim % kChunk != 0 || row > (1 << 30))
+        return FP8KV_ERR_UNSUPPORTED;
     if (num_tokens == 0) return FP8KV_OK;
     if (!cache->k || !cache->v || !k || !v || !slot_mapping) return FP8KV_ERR_ARG;
     if (k_tok_stride < row || v_tok_stride < row || (k_tok_stride % 8) || (v_tok_stride % 8))
@@ -147,7 +152,8 @@ extern "C" fp8kv_status kv_store_e4m3(const fp8kv_cache *cache, const fp8kv_bf16
     const int grid = grid_for(num_tokens * (row / kChunk), sms);
     kv_store_kernel<<<grid, kStoreThreads, 0, static_cast<cudaStream_t>(stream)>>>(
         k, v, k_tok_stride, v_tok_stride, slot_mapping, num_tokens, static_cast<int32_t>(row),
-        capacity, cache->k, cache->v, k_scale, v_scale, err);
+        cache->head_dim, cache->num_kv_heads, cache->block_size, capacity, cache->k, cache->v,
+        k_scale, v_scale, err);
     if (cudaGetLastError() != cudaSuccess) return FP8KV_ERR_LAUNCH;
     return FP8KV_OK;
 }

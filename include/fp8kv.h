@@ -37,9 +37,10 @@
  *     device is not compute capability 10.3).
  *
  * Cache layout (fp8kv_cache): two byte arrays, K and V, each
- *   uint8[num_blocks][block_size][num_kv_heads][head_dim]  (row-major),
- * every byte an e4m3 code.  Token slot s lives in block s / block_size, row
- * s % block_size.  A sequence's keys are listed by its block-table row:
+ *   uint8[num_blocks][num_kv_heads][block_size][head_dim]  (row-major),
+ * every byte an e4m3 code: one head's rows of a block are contiguous
+ * (block_size * head_dim bytes).  Token slot s lives in block s / block_size,
+ * row s % block_size, of every head.  A sequence's keys are listed by its block-table row:
  * logical block i of sequence b is physical block block_table[b][i].
  * Supported: block_size in {16, 32, 64, 128}, head_dim in {128, 256}.
  */
@@ -71,7 +72,7 @@ typedef uint16_t fp8kv_bf16;    /* raw bfloat16 bit pattern */
 #define FP8KV_DEVERR_BAD_SLOT     0x4u   /* a slot outside the pool                */
 
 typedef struct {
-    uint8_t *k;            /* device, num_blocks*block_size*num_kv_heads*head_dim bytes */
+    uint8_t *k;            /* device, num_blocks*num_kv_heads*block_size*head_dim bytes */
     uint8_t *v;            /* device, same size as k                                    */
     int64_t num_blocks;
     int32_t block_size;
@@ -133,8 +134,9 @@ fp8kv_status paged_attn_fp8_decode(const fp8kv_cache *cache, const fp8kv_bf16 *q
 
 /*
  * paged_attn_fp8_decode_ex -- paged_attn_fp8_decode with an explicit split
- * length: split_tokens > 0 (a multiple of 128) makes every split cover that
- * many keys; 0 chooses it from the device's SM count (the plain call).
+ * length: split_tokens > 0 makes every split cover that many keys and must be
+ * a multiple of the kernel's key tile (256 keys at head_dim 128, 128 at 256);
+ * 0 chooses it from the device's SM count (the plain call).
  */
 fp8kv_status paged_attn_fp8_decode_ex(const fp8kv_cache *cache, const fp8kv_bf16 *q,
                                       int32_t num_q_heads, const int32_t *block_table,

@@ -136,11 +136,12 @@ def encode_f32(x: np.ndarray) -> np.ndarray:
 def kv_store(cache_k, cache_v, k_bf16, v_bf16, slot_mapping, k_scale, v_scale,
              block_size):
     """Quantize and scatter k/v ([T][Hkv][D] uint16 bits) into the caches
-    ([num_blocks][block_size][Hkv][D] uint8), in place."""
+    ([num_blocks][Hkv][block_size][D] uint8), in place."""
     k = _u16(k_bf16)
     v = _u16(v_bf16)
     T, H, D = k.shape
     nb = cache_k.shape[0]
+    assert cache_k.shape == (nb, H, block_size, D)
     sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
     assert cache_k.flags.c_contiguous and cache_v.flags.c_contiguous
     rc = _load().or_kv_store(_ptr(cache_k), _ptr(cache_v), nb, block_size, H, D,

@@ -133,9 +133,10 @@ void or_decode_array(const uint8_t *x, int64_t n, double *out)
 
 /* Store into the paged cache [PR "Purpose", quant-on-store and cache
  * plumbing: caches are byte arrays, written at each token's slot].
- * READING: each cache is uint8[num_blocks][block_size][num_kv_heads][head_dim];
- * token t goes to block slot/block_size, row slot%block_size; a negative
- * slot means the token is not stored.
+ * READING: each cache is uint8[num_blocks][num_kv_heads][block_size][head_dim]
+ * (the pages fix no layout; head-major blocks keep one head's block rows
+ * contiguous); token t goes to block slot/block_size, row slot%block_size of
+ * every head; a negative slot means the token is not stored.
  * k, v: bf16 [num_tokens] rows of num_kv_heads*head_dim, rows k_stride /
  * v_stride elements apart.  Returns 0, or -1 when a slot is out of range. */
 int or_kv_store(uint8_t *cache_k, uint8_t *cache_v, int64_t num_blocks,
@@ -144,19 +145,23 @@ int or_kv_store(uint8_t *cache_k, uint8_t *cache_v, int64_t num_blocks,
                 int64_t v_stride, const int64_t *slot_mapping,
                 int64_t num_tokens, float k_scale, float v_scale)
 {
-    int64_t t, row = (int64_t)num_kv_heads * head_dim;
+    int64_t t;
+    int32_t h, d;
     for (t = 0; t < num_tokens; ++t) {
-        int64_t slot = slot_mapping[t], blk, off, base, i;
+        int64_t slot = slot_mapping[t], blk, off;
         if (slot < 0)
             continue;
         blk = slot / block_size;
         off = slot % block_size;
         if (blk >= num_blocks)
             return -1;
-        base = (blk * block_size + off) * row;
-        for (i = 0; i < row; ++i) {
-            cache_k[base + i] = or_quantize(k[t * k_stride + i], k_scale);
-            cache_v[base + i] = or_quantize(v[t * v_stride + i], v_scale);
+        for (h = 0; h < num_kv_heads; ++h) {
+            int64_t dst = ((blk * num_kv_heads + h) * block_size + off) * head_dim;
+            int64_t src = (int64_t)h * head_dim;
+            for (d = 0; d < head_dim; ++d) {
+                cache_k[dst + d] = or_quantize(k[t * k_stride + src + d], k_scale);
+                cache_v[dst + d] = or_quantize(v[t * v_stride + src + d], v_scale);
+            }
         }
     }
     return 0;

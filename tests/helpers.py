@@ -73,7 +73,7 @@ def oracle_decode_rows(inp, rows, q_scale, k_scale, v_scale, softmax_scale=None,
 
 def oracle_store(kv, k_scale, v_scale, fill=0xA5):
     """Oracle's paged cache for the whole PagedKV (small cases only)."""
-    shape = (kv.num_blocks, kv.block_size, kv.k.shape[1], kv.k.shape[2])
+    shape = (kv.num_blocks, kv.k.shape[1], kv.block_size, kv.k.shape[2])
     ck = np.full(shape, fill, dtype=np.uint8)
     cv = np.full(shape, fill, dtype=np.uint8)
     oracle.kv_store(ck, cv, bits(kv.k.cpu()), bits(kv.v.cpu()), kv.slot_mapping.cpu().numpy(),

@@ -121,6 +121,7 @@ def test_decode_rejects_bad_arguments_on_host(lib):
     assert _decode(lib, lib.CacheStruct(16, 16, 4, 24, 2, 128)) == lib.ERR_UNSUPPORTED
     assert _decode(lib, cache, rel=16, E=0) == lib.ERR_ARG
     assert _decode(lib, cache, split=100) == lib.ERR_ARG
+    assert _decode(lib, cache, split=64) == lib.ERR_ARG              # not a whole key tile
     assert _decode(lib, cache, window=-1) == lib.ERR_ARG
     assert _decode(lib, cache, B=0) == lib.OK                        # nothing to do
     assert _decode(lib, cache, q=None) == lib.ERR_ARG
@@ -128,9 +129,14 @@ def test_decode_rejects_bad_arguments_on_host(lib):
 
 
 def test_workspace_size_is_host_only_with_explicit_splits(lib):
-    # 2 seqs x 8 q heads, max 4 blocks of 16 = 64 keys -> 1 split of 128 keys
-    n = lib.decode_workspace_size(2, 8, 2, 128, 4, 16, 0, 128)
-    assert n == 2 * 8 * 1 * (128 + 2) * 4
-    n = lib.decode_workspace_size(1, 4, 1, 256, 64, 16, 0, 256)        # 1024 keys, 4 splits
-    assert n == 1 * 4 * 4 * (256 + 2) * 4
+    def per_slot(B, Hq, D):
+        return B * Hq * (D + 2) * 4          # fp32 partial o plus (m, l) per query head
+    # 2 seqs x 8 q heads, max 4 blocks of 16 = 64 keys -> one split of 256 keys
+    n1 = lib.decode_workspace_size(2, 8, 2, 128, 4, 16, 0, 256)
+    assert n1 % per_slot(2, 8, 128) == 0
+    slots_per_split = n1 // per_slot(2, 8, 128)
+    assert 1 <= slots_per_split <= 4
+    # 1024 keys in splits of 256 keys: 4 splits
+    n2 = lib.decode_workspace_size(1, 4, 1, 256, 64, 16, 0, 256)
+    assert n2 % per_slot(1, 4, 256) == 0 and (n2 // per_slot(1, 4, 256)) % 4 == 0
     assert lib.decode_workspace_size(1, 4, 1, 64, 4, 16, 0, 128) == 0

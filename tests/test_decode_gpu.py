@@ -91,7 +91,7 @@ def test_heavy_tailed_values(fk, v_scale):
              v_dist="v_t3", plant=True, seed=9)
 
 
-@pytest.mark.parametrize("split", [128, 256, 896])
+@pytest.mark.parametrize("split", [256, 512, 1792])
 def test_explicit_splits_agree(fk, split):
     lens = [1, 130, 1000, 2500]
     _, auto = run_case(fk, lens, 8, 1, 128, 16, seed=11)

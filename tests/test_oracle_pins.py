@@ -169,8 +169,8 @@ def test_paged_store_round_trips_through_block_table(oracle_lib):
     lens = [37, 16, 1, 70]
     kv = workloads.make_paged_kv(lens, 2, 128, 16, g=g, device="cpu", v_dist="v_t3")
     nb = kv.num_blocks
-    ck = np.full((nb, 16, 2, 128), 0xA5, dtype=np.uint8)      # canary
-    cv = np.full((nb, 16, 2, 128), 0xA5, dtype=np.uint8)
+    ck = np.full((nb, 2, 16, 128), 0xA5, dtype=np.uint8)      # canary, [block][head][row][d]
+    cv = np.full((nb, 2, 16, 128), 0xA5, dtype=np.uint8)
     sm = kv.slot_mapping.numpy().copy()
     sm[5] = -1                                                # one skipped token
     oracle_lib.kv_store(ck, cv, workloads.bf16_bits(kv.k), workloads.bf16_bits(kv.v), sm,
@@ -178,16 +178,16 @@ def test_paged_store_round_trips_through_block_table(oracle_lib):
     bt = kv.block_table.numpy()
     kq = oracle_lib.quantize(workloads.bf16_bits(kv.k), 1.0)
     vq = oracle_lib.quantize(workloads.bf16_bits(kv.v), 3.0)
-    touched = np.zeros((nb, 16), dtype=bool)
+    touched = np.zeros((nb, 2, 16), dtype=bool)
     t = 0
     for b, L in enumerate(lens):
         for p in range(L):
             blk, off = bt[b, p // 16], p % 16
             if t == 5:
-                assert (ck[blk, off] == 0xA5).all()
+                assert (ck[blk, :, off] == 0xA5).all()
             else:
-                assert np.array_equal(ck[blk, off], kq[t]) and np.array_equal(cv[blk, off], vq[t])
-                touched[blk, off] = True
+                assert np.array_equal(ck[blk, :, off], kq[t]) and np.array_equal(cv[blk, :, off], vq[t])
+                touched[blk, :, off] = True
             t += 1
     assert (ck[~touched] == 0xA5).all() and (cv[~touched] == 0xA5).all()
 

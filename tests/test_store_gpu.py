@@ -56,7 +56,7 @@ def test_store_every_bf16_pattern(fk, scale):
     cache = fk.KVCache.empty(32, 16, 1, 128, device=DEV, fill=0xA5)
     fk.kv_store_e4m3(cache, k.to(DEV), v.to(DEV), slots.to(DEV), scale, scale)
     torch.cuda.synchronize()
-    ck = np.full((32, 16, 1, 128), 0xA5, dtype=np.uint8)
+    ck = np.full((32, 1, 16, 128), 0xA5, dtype=np.uint8)
     cv = ck.copy()
     oracle.kv_store(ck, cv, bits(k), bits(v), slots.numpy(), scale, scale, 16)
     assert np.array_equal(cache.k.cpu().numpy(), ck)
@@ -73,7 +73,7 @@ def test_store_skips_negative_and_flags_out_of_range_slots(fk):
     fk.kv_store_e4m3(cache, k.to(DEV), v.to(DEV), slots.to(DEV), 1.0, 1.0)
     err = fk.device_error()
     assert err == fk.DEVERR_BAD_SLOT
-    ck = np.full((4, 16, 2, 128), 0xA5, dtype=np.uint8)
+    ck = np.full((4, 2, 16, 128), 0xA5, dtype=np.uint8)
     cv = ck.copy()
     keep = slots.clone()
     keep[3] = -1
@@ -92,7 +92,7 @@ def test_store_strided_rows(fk):
     qkv_d = qkv.to(DEV)
     fk.kv_store_e4m3(cache, qkv_d[:, 1], qkv_d[:, 2], slots.to(DEV), 1.0, 0.5)
     torch.cuda.synchronize()
-    ck = np.zeros((3, 16, 2, 128), dtype=np.uint8)
+    ck = np.zeros((3, 2, 16, 128), dtype=np.uint8)
     cv = ck.copy()
     oracle.kv_store(ck, cv, bits(k.reshape(40, 2, 128)), bits(v.reshape(40, 2, 128)),
                     slots.numpy(), 1.0, 0.5, 16)
@@ -132,8 +132,9 @@ def test_store_at_decode_pool_size(fk):
     T = kv.k.shape[0]
     idx = torch.randint(0, T, (3000,), generator=torch.Generator().manual_seed(0))
     slots = kv.slot_mapping[idx.to(DEV)]
-    gk = cache.k.view(-1, spec.Hkv, spec.D)[slots].cpu().numpy()
-    gv = cache.v.view(-1, spec.Hkv, spec.D)[slots].cpu().numpy()
+    blk, row = slots // kv.block_size, slots % kv.block_size
+    gk = cache.k[blk, :, row].cpu().numpy()      # [block][head][row][d] -> [n][head][d]
+    gv = cache.v[blk, :, row].cpu().numpy()
     hk = kv.k[idx.to(DEV)].cpu()
     hv = kv.v[idx.to(DEV)].cpu()
     assert np.array_equal(gk, oracle.quantize(bits(hk), 1.0))
