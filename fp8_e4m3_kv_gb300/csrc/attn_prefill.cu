@@ -431,6 +431,469 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     }
 }
 
+// ---------------------------------------------------------------------------
+// head_dim 128: two query tiles per CTA
+//
+// One CTA computes query tiles 2c and 2c + 1 (256 rows) of one head of one
+// sequence.  Both tiles share every K/V tile the producer loads; TMEM holds
+// S0, S1 (128 columns each) and O0, O1 (128 columns each).  Warpgroup k (warps
+// 4k .. 4k + 3) runs the softmax of query tile k; the MMA warp interleaves the
+// two tiles' QK and PV products.  Per element the softmax is one FMA (the
+// folded score scale and the running max), one ex2, the row sum, and the
+// two-term e4m3 split done on packed f16 pairs.
+// ---------------------------------------------------------------------------
+// Three warpgroups: two softmax warpgroups, then the producer warp, the MMA
+// warp and two idle warps.  The kernel is built for 384 threads at 168
+// registers; at run time the third warpgroup gives registers back
+// (setmaxnreg.dec to kRegsIo) and the softmax warpgroups take them
+// (setmaxnreg.inc to kRegsSoftmax): 2*128*224 + 128*56 = 384*168.
+constexpr int kPre2Threads = 384;
+constexpr int kRegsLaunch = 168;
+constexpr int kRegsSoftmax = 224;
+constexpr int kRegsIo = 56;
+static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsIo <= kPre2Threads * kRegsLaunch,
+              "register split exceeds the launch's registers");
+
+struct Pre2Cfg {
+    static constexpr int kStages = 3;
+    static constexpr int kTileBytes = kTile * 128;          // K or V tile, 16 KB
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kQBytes = kTile * 128;             // one Q8 tile, 16 KB
+    static constexpr int kPBytes = kTile * kTile;           // one P term, 16 KB
+    static constexpr int kOffQ = 0;                         // [2] Q8 tiles
+    static constexpr int kOffStages = 2 * kQBytes;
+    static constexpr int kOffP = kOffStages + kStages * kStageBytes;   // [2 tiles][hi, lo]
+    static constexpr int kOffMisc = kOffP + 4 * kPBytes;
+    static constexpr int kSmemBytes = kOffMisc + 512 + 1024;
+    static constexpr uint32_t kTmemCols = 512;              // S0 S1 O0 O1
+};
+
+__device__ __forceinline__ float ex2_fast(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// P for 16 consecutive keys: p = 2^(x*mult - m8); adds them to l and writes
+// the P_hi and P_lo bytes (16 each) for this row.
+__device__ __forceinline__ void p_chunk16(const float *x, float mult, float neg_m8, float &l0,
+                                          float &l1, uint4 &hi, uint4 &lo) {
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        uint32_t h2w[2], l2w[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const float p0 = ex2_fast(fmaf(x[4 * w + 2 * k], mult, neg_m8));
+            const float p1 = ex2_fast(fmaf(x[4 * w + 2 * k + 1], mult, neg_m8));
+            l0 += p0;
+            l1 += p1;
+            const __half2 ph = __floats2half2_rn(p0, p1);
+            const uint32_t h8 = __nv_cvt_halfraw2_to_fp8x2(ph, __NV_SATFINITE, __NV_E4M3);
+            const __half2 hh = e4m3x2_to_half2(static_cast<uint16_t>(h8));
+            const uint32_t l8 = __nv_cvt_halfraw2_to_fp8x2(__hsub2(ph, hh), __NV_SATFINITE, __NV_E4M3);
+            h2w[k] = h8 & 0xFFFFu;
+            l2w[k] = l8 & 0xFFFFu;
+        }
+        hw[w] = h2w[0] | (h2w[1] << 16);
+        lw[w] = l2w[0] | (l2w[1] << 16);
+    }
+    hi = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    lo = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+}
+
+__global__ void __launch_bounds__(kPre2Threads, 1)
+prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                const PrefillParams p) {
+    using C = Pre2Cfg;
+    constexpr int D = 128;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_pairs = (p.n_qtiles + 1) / 2;
+    const int pair = n_pairs - 1 - static_cast<int>(blockIdx.x);   // longest tiles first
+    const int h = blockIdx.y, b = blockIdx.z;
+    const int kvh = h / p.G;
+    const int q_first = p.cu_q[b];
+    const int len_q = p.cu_q[b + 1] - q_first;
+    const int64_t len_k = p.lens_k[b];
+    if (pair * 2 * kTile >= len_q || len_k < len_q) return;
+
+    // per query tile k of the pair: rows, positions and key tiles
+    int n_rows[2];
+    int64_t P0[2], kt_lo[2], kt_hi[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int qt = 2 * pair + k;
+        n_rows[k] = max(0, min(kTile, len_q - qt * kTile));
+        P0[k] = len_k - len_q + static_cast<int64_t>(qt) * kTile;
+        const int64_t pos_last = P0[k] + max(n_rows[k], 1) - 1;
+        int64_t key_lo = 0;
+        if (p.window > 0 && P0[k] - p.window + 1 > 0) key_lo = P0[k] - p.window + 1;
+        kt_lo[k] = key_lo / kTile;
+        kt_hi[k] = pos_last / kTile;
+    }
+    const bool act1 = n_rows[1] > 0;
+    const int64_t kt0 = kt_lo[0];
+    const int64_t kt1 = act1 ? kt_hi[1] : kt_hi[0];
+    const int ntiles = static_cast<int>(kt1 - kt0 + 1);
+    // does query tile k use CTA-local key tile j?
+    auto need = [&](int k, int j) -> bool {
+        const int64_t t = kt0 + j;
+        return (k == 0 || act1) && t >= kt_lo[k] && t <= kt_hi[k];
+    };
+
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffMisc);
+    uint64_t *full = bars;              // [3]
+    uint64_t *empty = bars + 3;         // [3]
+    uint64_t *s_full = bars + 6;        // [2] per query tile
+    uint64_t *s_free = bars + 8;        // [2]
+    uint64_t *p_full = bars + 10;       // [2]
+    uint64_t *o_done = bars + 12;       // [2]
+    uint64_t *mma_done = bars + 14;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc + 128);
+    CtaFail *fail = reinterpret_cast<CtaFail *>(smem + C::kOffMisc + 132);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(&s_full[k], 1);
+            mbar_init(&s_free[k], 4);
+            mbar_init(&p_full[k], 4);
+            mbar_init(&o_done[k], 1);
+        }
+        mbar_init(mma_done, 1);
+        fail->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 9) tmem_alloc(tmem_slot, C::kTmemCols);
+    if (warp < 8) {
+        // Q8 row r of query tile k = e4m3(q / q_scale); rows past the
+        // sequence's queries are zero.
+        const int k = warp >> 2, r = threadIdx.x & 127;
+        const int qt = 2 * pair + k;
+        const uint16_t *qrow = p.q + (static_cast<int64_t>(q_first) + qt * kTile + r) * p.Hq * D +
+                               static_cast<int64_t>(h) * D;
+        uint8_t *q8 = smem + C::kOffQ + k * C::kQBytes;
+#pragma unroll 4
+        for (int c = 0; c < D / 16; ++c) {
+            uint4 packed = make_uint4(0, 0, 0, 0);
+            if (r < n_rows[k]) {
+                const uint4 w0 = *reinterpret_cast<const uint4 *>(qrow + c * 16);
+                const uint4 w1 = *reinterpret_cast<const uint4 *>(qrow + c * 16 + 8);
+                packed.x = quantize_bf16x2(w0.x, p.q_scale) | (quantize_bf16x2(w0.y, p.q_scale) << 16);
+                packed.y = quantize_bf16x2(w0.z, p.q_scale) | (quantize_bf16x2(w0.w, p.q_scale) << 16);
+                packed.z = quantize_bf16x2(w1.x, p.q_scale) | (quantize_bf16x2(w1.y, p.q_scale) << 16);
+                packed.w = quantize_bf16x2(w1.z, p.q_scale) | (quantize_bf16x2(w1.w, p.q_scale) << 16);
+            }
+            *reinterpret_cast<uint4 *>(q8 + r * 128 + ((c ^ (r & 7)) << 4)) = packed;
+        }
+        fence_proxy_async_smem();
+    }
+    if (warp == 8 && lane == 0) {
+        tma_prefetch_map(&kmap);
+        tma_prefetch_map(&vmap);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp >= 8) {
+      // the third warpgroup (producer, MMA, two idle warps) gives registers back
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsIo));
+      if (warp == 8) {
+        // ------------------------------------------------------------ producer
+        const uint64_t pol = l2_policy_evict_first();
+        const int nb = kTile / p.block_size;
+        int last_issued[C::kStages];
+#pragma unroll
+        for (int s = 0; s < C::kStages; ++s) last_issued[s] = -1;
+        for (int i = 0; i < ntiles; ++i) {
+            const int s = i % C::kStages;
+            int32_t phys = static_cast<int32_t>(p.num_blocks);   // out of range: zero fill
+            if (lane < nb) {
+                const int64_t lb = (kt0 + i) * nb + lane;
+                if (lb * p.block_size < len_k && lb < p.max_blocks) {
+                    const int32_t id =
+                        __ldg(p.block_table + static_cast<int64_t>(b) * p.max_blocks + lb);
+                    if (id >= 0 && id < p.num_blocks)
+                        phys = id;
+                    else
+                        atomicOr(p.err, FP8KV_DEVERR_BAD_BLOCK);
+                }
+            }
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait(&empty[s], ((i / C::kStages) & 1) ^ 1, fail, p.err);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            if (lane == 0) mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+            __syncwarp();
+            if (lane < nb) {
+                uint8_t *kdst = smem + C::kOffStages + s * C::kStageBytes + lane * p.block_size * 128;
+                tma_load_4d(kdst, &kmap, &full[s], 0, 0, kvh, phys, pol);
+                tma_load_4d(kdst + C::kTileBytes, &vmap, &full[s], 0, 0, kvh, phys, pol);
+            }
+            last_issued[s] = i;
+        }
+        if (lane == 0 && fail->abort) {
+            for (int s = 0; s < C::kStages; ++s)
+                if (last_issued[s] >= 0)
+                    mbar_drain_p(&full[s], (last_issued[s] / C::kStages) & 1, p.err);
+        }
+    } else if (warp == 9) {
+        // ------------------------------------------------------------ MMA issuer
+        // Step j: S_k = Q8_k . K_j^T for the query tiles that use key tile j,
+        // then O_k += P_k . V_{j-1} for those that used key tile j - 1.
+        if (lane == 0) {
+            const uint32_t idesc_qk = idesc_e4m3_f32(128, 128, false, false);
+            const uint32_t idesc_pv = idesc_e4m3_f32(128, 128, false, true);
+            int n_qk[2] = {0, 0}, n_pv[2] = {0, 0};
+            bool ok = true;
+            for (int j = 0; j <= ntiles && ok; ++j) {
+                if (j < ntiles) {
+                    const int s = j % C::kStages;
+                    if (!mbar_wait(&full[s], (j / C::kStages) & 1, fail, p.err)) break;
+                    const uint32_t k_addr = smem_u32(smem + C::kOffStages + s * C::kStageBytes);
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        if (!need(k, j)) continue;
+                        if (!mbar_wait(&s_free[k], (n_qk[k] & 1) ^ 1, fail, p.err)) { ok = false; break; }
+                        tc_fence_after_sync();
+                        const uint32_t q_addr = smem_u32(smem + C::kOffQ + k * C::kQBytes);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t a = sdesc_sw128(q_addr + kk * 32, 16, 1024);
+                            const uint64_t bd = sdesc_sw128(k_addr + kk * 32, 16, 1024);
+                            mma_e4m3(tmem + k * 128, a, bd, idesc_qk, kk > 0);
+                        }
+                        tc_commit(&s_full[k]);
+                        ++n_qk[k];
+                    }
+                    if (!ok) break;
+                }
+                if (j >= 1) {
+                    const int jj = j - 1, s = jj % C::kStages;
+                    const uint32_t v_addr =
+                        smem_u32(smem + C::kOffStages + s * C::kStageBytes + C::kTileBytes);
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        if (!need(k, jj)) continue;
+                        if (!mbar_wait(&p_full[k], n_pv[k] & 1, fail, p.err)) { ok = false; break; }
+                        tc_fence_after_sync();
+                        const uint32_t p_addr = smem_u32(smem + C::kOffP + k * 2 * C::kPBytes);
+#pragma unroll
+                        for (int part = 0; part < 2; ++part) {
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk) {
+                                const uint64_t a =
+                                    sdesc_sw128(p_addr + part * C::kPBytes + kk * 32, 16, 1024);
+                                const uint64_t bd =
+                                    sdesc_sw128(v_addr + kk * 32 * 128, kTile * 128, 1024);
+                                mma_e4m3(tmem + 256 + k * 128, a, bd, idesc_pv,
+                                         (n_pv[k] > 0 || part > 0 || kk > 0) ? 1u : 0u);
+                            }
+                        }
+                        tc_commit(&o_done[k]);
+                        ++n_pv[k];
+                    }
+                    if (!ok) break;
+                    tc_commit(&empty[s]);
+                }
+            }
+            tc_commit(mma_done);
+            mbar_drain_p(mma_done, 0, p.err);
+        }
+        __syncwarp();
+      }
+    } else {
+        // ------------------------------------------------------------ softmax
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+        const int k = warp >> 2, wq = warp & 3;
+        const int r = threadIdx.x & 127;
+        const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+        const uint32_t col_s = k * 128, col_o = 256 + k * 128;
+        const int qt = 2 * pair + k;
+        const int my_rows = k == 0 ? n_rows[0] : n_rows[1];
+        const int64_t my_P0 = k == 0 ? P0[0] : P0[1];
+        const int64_t my_lo = k == 0 ? kt_lo[0] : kt_lo[1];
+        const int64_t my_hi = k == 0 ? kt_hi[0] : kt_hi[1];
+        const int64_t pos = my_P0 + r;
+        const bool row_ok = r < my_rows;
+        const int64_t pos_first = my_P0, pos_last = my_P0 + max(my_rows, 1) - 1;
+        const uint16_t *bias_row =
+            (p.rel && row_ok) ? p.rel + (static_cast<int64_t>(q_first) + qt * kTile + r) *
+                                            p.bias_tok_stride + static_cast<int64_t>(h) * p.rel_extent
+                              : nullptr;
+        uint8_t *p_hi = smem + C::kOffP + k * 2 * C::kPBytes;
+        uint8_t *p_lo = p_hi + C::kPBytes;
+        const int sw = r & 7;
+        float m_used = -INFINITY, l0 = 0.0f, l1 = 0.0f;
+        bool ok = true;
+        int c = 0;   // key tiles processed by this query tile
+        for (int j = static_cast<int>(my_lo - kt0); j <= static_cast<int>(my_hi - kt0) &&
+                                                    (k == 0 || act1);
+             ++j) {
+            if (!warp_wait_p(&s_full[k], c & 1, fail, p.err)) { ok = false; break; }
+            tc_fence_after_sync();
+
+            const int64_t k0 = (kt0 + j) * kTile;
+            const bool full_tile = (k0 + kTile - 1 <= pos_first) &&
+                                   (p.window == 0 || pos_last - k0 < p.window);
+            const bool bias_tile = bias_row != nullptr && pos - k0 >= 0 &&
+                                   pos - k0 - (kTile - 1) < p.rel_extent;
+            float x[128];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tmem_ld_x32(tmem + lane_base + col_s + q * 32, x + q * 32);
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_free[k]);
+
+            float mult, mx = -INFINITY;
+            if (full_tile && !__any_sync(0xffffffffu, bias_tile)) {
+                // every key visible, no bias in this warp: max over the raw
+                // scores (the scale is positive), scale folded into the FMA
+#pragma unroll
+                for (int e = 0; e < 128; ++e) mx = fmaxf(mx, x[e]);
+                mx *= p.score_log2;
+                mult = p.score_log2;
+            } else {
+                // key e of the tile sits at distance d0 - e from this row:
+                // visible for e in [e_lo, e_hi] (causal, window, sequence end);
+                // biased for e in [b_lo, d0] (distance below the extent)
+                const int32_t d0 = static_cast<int32_t>(pos - k0);   // < 2^31: positions are int32
+                const int32_t keys_left =
+                    static_cast<int32_t>(len_k - k0 < kTile ? len_k - k0 : kTile);
+                const int32_t e_hi = min(d0, keys_left - 1);
+                const int32_t e_lo = p.window > 0 ? max(0, d0 - p.window + 1) : 0;
+                const int32_t b_lo = bias_tile ? max(0, d0 - p.rel_extent + 1) : 1 << 30;
+                const uint16_t *brow = bias_tile ? bias_row + d0 : nullptr;   // brow[-e] = bias(e)
+#pragma unroll
+                for (int e = 0; e < 128; ++e) {
+                    float zz = x[e] * p.score_log2;
+                    if (e >= b_lo && e <= d0) zz = fmaf(bf16_bits_to_float(__ldg(brow - e)), kLog2eP, zz);
+                    zz = (e >= e_lo && e <= e_hi) ? zz : -INFINITY;
+                    x[e] = zz;
+                    mx = fmaxf(mx, zz);
+                }
+                mult = 1.0f;
+            }
+            // lazy rescale: move the reference max only when the row max grew
+            // by more than tau, so P <= 2^(8 + tau) stays below 448
+            const bool resc = mx > m_used + kRescaleTau;
+            const float m_new = resc ? mx : m_used;
+            const float alpha = (resc && m_used != -INFINITY) ? ex2_fast(m_used - m_new) : 1.0f;
+            if (c >= 1) {
+                if (!warp_wait_p(&o_done[k], (c - 1) & 1, fail, p.err)) { ok = false; break; }
+                tc_fence_after_sync();
+                if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+#pragma unroll 1
+                    for (int q = 0; q < D / 32; ++q) {
+                        float o[32];
+                        const uint32_t ta = tmem + lane_base + col_o + q * 32;
+                        tmem_ld_x32(ta, o);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] *= alpha;
+                        tmem_st_x32(ta, o);
+                    }
+                }
+            }
+            l0 *= alpha;
+            l1 *= alpha;
+            m_used = m_new;
+            const float neg_m8 = (m_used == -INFINITY) ? 0.0f : kPOffset - m_used;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                uint4 hi, lo;
+                p_chunk16(x + q * 16, mult, neg_m8, l0, l1, hi, lo);
+                const uint32_t off = r * 128 + ((q ^ sw) << 4);
+                *reinterpret_cast<uint4 *>(p_hi + off) = hi;
+                *reinterpret_cast<uint4 *>(p_lo + off) = lo;
+            }
+            // keys past the end of the sequence may hold stale bytes (NaN codes
+            // included): zero their V rows so that 0 * V stays 0 in the MMA
+            if (k0 + r >= len_k) {
+                uint4 *q4 = reinterpret_cast<uint4 *>(smem + C::kOffStages +
+                                                      (j % C::kStages) * C::kStageBytes +
+                                                      C::kTileBytes + r * 128);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) q4[e] = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_full[k]);
+            ++c;
+        }
+        if (ok && c > 0 && warp_wait_p(&o_done[k], (c - 1) & 1, fail, p.err)) {
+            tc_fence_after_sync();
+            const float l = l0 + l1;
+            const float f = (l > 0.0f) ? p.v_scale / l : 0.0f;
+            uint16_t *orow = p.out + (static_cast<int64_t>(q_first) + qt * kTile + r) * p.Hq * D +
+                             static_cast<int64_t>(h) * D;
+#pragma unroll 1
+            for (int q = 0; q < D / 32; ++q) {
+                float o[32];
+                tmem_ld_x32(tmem + lane_base + col_o + q * 32, o);
+                if (row_ok) {
+                    uint32_t w[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const __nv_bfloat162 v2 = __floats2bfloat162_rn(o[2 * e] * f, o[2 * e + 1] * f);
+                        w[e] = *reinterpret_cast<const uint32_t *>(&v2);
+                    }
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + q * 32);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+                }
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 9) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+// The register split relies on the kernel being launched with kRegsLaunch
+// registers per thread: with fewer, setmaxnreg.inc would wait for registers
+// that do not exist.  Checked once per process against the built kernel.
+bool prefill2_registers_ok() {
+    static int ok = -1;
+    if (ok < 0) {
+        cudaFuncAttributes attr;
+        ok = (cudaFuncGetAttributes(&attr, prefill2_kernel) == cudaSuccess &&
+              attr.numRegs >= kRegsLaunch && attr.maxThreadsPerBlock >= kPre2Threads)
+                 ? 1
+                 : 0;
+        if (!ok) cudaGetLastError();
+    }
+    return ok == 1;
+}
+
+fp8kv_status launch_prefill2(const CUtensorMap &km, const CUtensorMap &vm, const PrefillParams &p,
+                             int num_seqs, cudaStream_t stream) {
+    if (!prefill2_registers_ok()) return FP8KV_ERR_UNSUPPORTED;
+    if (cudaFuncSetAttribute(prefill2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Pre2Cfg::kSmemBytes) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8KV_ERR_LAUNCH;
+    }
+    dim3 grid((p.n_qtiles + 1) / 2, p.Hq, num_seqs);
+    prefill2_kernel<<<grid, kPre2Threads, Pre2Cfg::kSmemBytes, stream>>>(km, vm, p);
+    if (cudaGetLastError() != cudaSuccess) return FP8KV_ERR_LAUNCH;
+    return FP8KV_OK;
+}
+
 template <int D>
 fp8kv_status launch_prefill(const CUtensorMap &km, const CUtensorMap &vm, const PrefillParams &p,
                             int num_seqs, cudaStream_t stream) {
@@ -507,6 +970,6 @@ extern "C" fp8kv_status attn_fp8_varlen_prefill(
                                       1.4426950408889634);
     p.v_scale = v_scale;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return D == 128 ? launch_prefill<128>(km, vm, p, num_seqs, s)
+    return D == 128 ? launch_prefill2(km, vm, p, num_seqs, s)
                     : launch_prefill<256>(km, vm, p, num_seqs, s);
 }
