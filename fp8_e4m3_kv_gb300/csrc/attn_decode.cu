@@ -159,9 +159,12 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // KV heads fastest: the CTAs of one split read neighbouring cache blocks
-    // at about the same time
-    const int kvh = blockIdx.x, split = blockIdx.y, b = blockIdx.z;
+    // KV heads fastest (the CTAs of one split stream neighbouring cache
+    // blocks together), then sequences; splits slowest and in descending
+    // order, so the last CTAs to run are the first splits, which are the
+    // short ones of short sequences
+    const int kvh = blockIdx.x, b = blockIdx.y;
+    const int split = static_cast<int>(gridDim.z) - 1 - static_cast<int>(blockIdx.z);
     const int h0 = kvh * p.G;
     const int64_t len = p.seq_lens[b];
     const int64_t lo = (p.window > 0 && len > p.window) ? len - p.window : 0;
@@ -667,7 +670,7 @@ fp8kv_status launch_decode(const CUtensorMap &km, const CUtensorMap &vm, const D
         cudaGetLastError();
         return FP8KV_ERR_LAUNCH;
     }
-    dim3 grid(num_kv_heads, p.num_slots, num_seqs);
+    dim3 grid(num_kv_heads, num_seqs, p.num_slots);
     kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(km, vm, p);
     if (cudaGetLastError() != cudaSuccess) return FP8KV_ERR_LAUNCH;
     return FP8KV_OK;
