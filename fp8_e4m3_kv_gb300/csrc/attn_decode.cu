@@ -114,7 +114,7 @@ struct DecodeParams {
     int32_t window;
     int32_t split_tiles;
     int32_t num_slots;      // partial slots per (sequence, head) = splits
-    float q_scale;
+    QScale q_scale;
     float score_log2;       // softmax_scale * q_scale * k_scale * log2(e)
 };
 
@@ -754,7 +754,7 @@ extern "C" fp8kv_status paged_attn_fp8_decode_ex(
     p.window = window;
     p.split_tiles = plan.split_tiles;
     p.num_slots = slots;
-    p.q_scale = q_scale;
+    p.q_scale = make_qscale(q_scale);
     p.score_log2 = static_cast<float>(static_cast<double>(softmax_scale) * q_scale * k_scale *
                                       1.4426950408889634);
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -66,7 +66,7 @@ struct PrefillParams {
     int32_t rel_extent;
     int32_t window;
     int32_t n_qtiles;
-    float q_scale;
+    QScale q_scale;
     float score_log2;   // softmax_scale * q_scale * k_scale * log2(e)
     float v_scale;
 };
@@ -454,16 +454,24 @@ constexpr int kRegsIo = 56;
 static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsIo <= kPre2Threads * kRegsLaunch,
               "register split exceeds the launch's registers");
 
+#ifndef FP8KV_PREFILL_PBUF
+#define FP8KV_PREFILL_PBUF 1
+#endif
+
 struct Pre2Cfg {
-    static constexpr int kStages = 3;
+    // P buffers per query tile: 2 lets a tile's softmax write while the
+    // previous tile's PV runs, at the cost of a K/V stage
+    static constexpr int kPBuf = FP8KV_PREFILL_PBUF;
+    static constexpr int kStages = kPBuf == 2 ? 2 : 3;
     static constexpr int kTileBytes = kTile * 128;          // K or V tile, 16 KB
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kQBytes = kTile * 128;             // one Q8 tile, 16 KB
     static constexpr int kPBytes = kTile * kTile;           // one P term, 16 KB
     static constexpr int kOffQ = 0;                         // [2] Q8 tiles
     static constexpr int kOffStages = 2 * kQBytes;
-    static constexpr int kOffP = kOffStages + kStages * kStageBytes;   // [2 tiles][hi, lo]
-    static constexpr int kOffMisc = kOffP + 4 * kPBytes;
+    // P: [query tile][kPBuf buffers][hi, lo] (16 KB each term)
+    static constexpr int kOffP = kOffStages + kStages * kStageBytes;
+    static constexpr int kOffMisc = kOffP + 2 * kPBuf * 2 * kPBytes;
     static constexpr int kSmemBytes = kOffMisc + 512 + 1024;
     static constexpr uint32_t kTmemCols = 512;              // S0 S1 O0 O1
 };
@@ -546,28 +554,30 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     };
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffMisc);
-    uint64_t *full = bars;              // [3]
-    uint64_t *empty = bars + 3;         // [3]
-    uint64_t *s_full = bars + 6;        // [2] per query tile
-    uint64_t *s_free = bars + 8;        // [2]
-    uint64_t *p_full = bars + 10;       // [2]
-    uint64_t *o_done = bars + 12;       // [2]
-    uint64_t *mma_done = bars + 14;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc + 128);
-    CtaFail *fail = reinterpret_cast<CtaFail *>(smem + C::kOffMisc + 132);
+    uint64_t *full = bars;              // [kStages]
+    uint64_t *empty = bars + 4;         // [kStages]
+    uint64_t *s_full = bars + 8;        // [query tile]
+    uint64_t *s_free = bars + 10;       // [query tile]
+    uint64_t *p_full = bars + 12;       // [query tile][P buffer]
+    uint64_t *o_done = bars + 16;       // [query tile][P buffer]: PV that read the buffer is done
+    uint64_t *mma_done = bars + 20;     // [query tile]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc + 256);
+    CtaFail *fail = reinterpret_cast<CtaFail *>(smem + C::kOffMisc + 260);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], 2);   // one arrival per MMA issuer
         }
         for (int k = 0; k < 2; ++k) {
             mbar_init(&s_full[k], 1);
             mbar_init(&s_free[k], 4);
-            mbar_init(&p_full[k], 4);
-            mbar_init(&o_done[k], 1);
+            for (int b2 = 0; b2 < 2; ++b2) {
+                mbar_init(&p_full[2 * k + b2], 4);
+                mbar_init(&o_done[2 * k + b2], 1);
+            }
+            mbar_init(&mma_done[k], 1);
         }
-        mbar_init(mma_done, 1);
         fail->abort = 0;
         fence_mbar_init();
     }
@@ -646,68 +656,72 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
                 if (last_issued[s] >= 0)
                     mbar_drain_p(&full[s], (last_issued[s] / C::kStages) & 1, p.err);
         }
-    } else if (warp == 9) {
-        // ------------------------------------------------------------ MMA issuer
-        // Step j: S_k = Q8_k . K_j^T for the query tiles that use key tile j,
-        // then O_k += P_k . V_{j-1} for those that used key tile j - 1.
+      } else if (warp == 9 || warp == 10) {
+        // ------------------------------------------------------------ MMA issuers
+        // One thread per query tile k (warp 9: tile 0, warp 10: tile 1), so
+        // neither tile's chain waits on the other's.  For each key tile j the
+        // tile uses: S_k = Q8_k . K_j^T, then O_k += P_k . V of the tile it
+        // used before.  A stage is released once both threads are done with
+        // it (empty[] counts two arrivals).
+        const int k = warp - 9;
         if (lane == 0) {
             const uint32_t idesc_qk = idesc_e4m3_f32(128, 128, false, false);
             const uint32_t idesc_pv = idesc_e4m3_f32(128, 128, false, true);
-            int n_qk[2] = {0, 0}, n_pv[2] = {0, 0};
+            const uint32_t q_addr = smem_u32(smem + C::kOffQ + k * C::kQBytes);
+            int n_qk = 0, n_pv = 0, prev = -1;
             bool ok = true;
-            for (int j = 0; j <= ntiles && ok; ++j) {
-                if (j < ntiles) {
-                    const int s = j % C::kStages;
-                    if (!mbar_wait(&full[s], (j / C::kStages) & 1, fail, p.err)) break;
-                    const uint32_t k_addr = smem_u32(smem + C::kOffStages + s * C::kStageBytes);
+            // PV of key tile jj (the tile this query tile used before), then
+            // release its stage
+            auto issue_pv = [&](int jj) -> bool {
+                const int s = jj % C::kStages;
+                const int pb = n_pv % C::kPBuf;
+                const uint32_t ph = (n_pv / C::kPBuf) & 1;
+                if (!mbar_wait(&p_full[2 * k + pb], ph, fail, p.err)) return false;
+                tc_fence_after_sync();
+                const uint32_t v_addr =
+                    smem_u32(smem + C::kOffStages + s * C::kStageBytes + C::kTileBytes);
+                const uint32_t p_addr =
+                    smem_u32(smem + C::kOffP + (k * C::kPBuf + pb) * 2 * C::kPBytes);
 #pragma unroll
-                    for (int k = 0; k < 2; ++k) {
-                        if (!need(k, j)) continue;
-                        if (!mbar_wait(&s_free[k], (n_qk[k] & 1) ^ 1, fail, p.err)) { ok = false; break; }
-                        tc_fence_after_sync();
-                        const uint32_t q_addr = smem_u32(smem + C::kOffQ + k * C::kQBytes);
+                for (int part = 0; part < 2; ++part) {
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t a = sdesc_sw128(q_addr + kk * 32, 16, 1024);
-                            const uint64_t bd = sdesc_sw128(k_addr + kk * 32, 16, 1024);
-                            mma_e4m3(tmem + k * 128, a, bd, idesc_qk, kk > 0);
-                        }
-                        tc_commit(&s_full[k]);
-                        ++n_qk[k];
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t a = sdesc_sw128(p_addr + part * C::kPBytes + kk * 32, 16, 1024);
+                        const uint64_t bd = sdesc_sw128(v_addr + kk * 32 * 128, kTile * 128, 1024);
+                        mma_e4m3(tmem + 256 + k * 128, a, bd, idesc_pv,
+                                 (n_pv > 0 || part > 0 || kk > 0) ? 1u : 0u);
                     }
-                    if (!ok) break;
                 }
-                if (j >= 1) {
-                    const int jj = j - 1, s = jj % C::kStages;
-                    const uint32_t v_addr =
-                        smem_u32(smem + C::kOffStages + s * C::kStageBytes + C::kTileBytes);
-#pragma unroll
-                    for (int k = 0; k < 2; ++k) {
-                        if (!need(k, jj)) continue;
-                        if (!mbar_wait(&p_full[k], n_pv[k] & 1, fail, p.err)) { ok = false; break; }
-                        tc_fence_after_sync();
-                        const uint32_t p_addr = smem_u32(smem + C::kOffP + k * 2 * C::kPBytes);
-#pragma unroll
-                        for (int part = 0; part < 2; ++part) {
-#pragma unroll
-                            for (int kk = 0; kk < 4; ++kk) {
-                                const uint64_t a =
-                                    sdesc_sw128(p_addr + part * C::kPBytes + kk * 32, 16, 1024);
-                                const uint64_t bd =
-                                    sdesc_sw128(v_addr + kk * 32 * 128, kTile * 128, 1024);
-                                mma_e4m3(tmem + 256 + k * 128, a, bd, idesc_pv,
-                                         (n_pv[k] > 0 || part > 0 || kk > 0) ? 1u : 0u);
-                            }
-                        }
-                        tc_commit(&o_done[k]);
-                        ++n_pv[k];
-                    }
-                    if (!ok) break;
-                    tc_commit(&empty[s]);
+                tc_commit(&o_done[2 * k + pb]);
+                tc_commit(&empty[s]);
+                ++n_pv;
+                return true;
+            };
+            for (int j = 0; j < ntiles && ok; ++j) {
+                const int s = j % C::kStages;
+                if (!mbar_wait(&full[s], (j / C::kStages) & 1, fail, p.err)) { ok = false; break; }
+                if (!need(k, j)) {
+                    // not this query tile's key tile: release the stage now
+                    mbar_arrive(&empty[s]);
+                    continue;
                 }
+                if (!mbar_wait(&s_free[k], (n_qk & 1) ^ 1, fail, p.err)) { ok = false; break; }
+                tc_fence_after_sync();
+                const uint32_t k_addr = smem_u32(smem + C::kOffStages + s * C::kStageBytes);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint64_t a = sdesc_sw128(q_addr + kk * 32, 16, 1024);
+                    const uint64_t bd = sdesc_sw128(k_addr + kk * 32, 16, 1024);
+                    mma_e4m3(tmem + k * 128, a, bd, idesc_qk, kk > 0);
+                }
+                tc_commit(&s_full[k]);
+                ++n_qk;
+                if (prev >= 0 && !issue_pv(prev)) { ok = false; break; }
+                prev = j;
             }
-            tc_commit(mma_done);
-            mbar_drain_p(mma_done, 0, p.err);
+            if (ok && prev >= 0) issue_pv(prev);
+            tc_commit(&mma_done[k]);
+            mbar_drain_p(&mma_done[k], 0, p.err);
         }
         __syncwarp();
       }
@@ -730,8 +744,6 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
             (p.rel && row_ok) ? p.rel + (static_cast<int64_t>(q_first) + qt * kTile + r) *
                                             p.bias_tok_stride + static_cast<int64_t>(h) * p.rel_extent
                               : nullptr;
-        uint8_t *p_hi = smem + C::kOffP + k * 2 * C::kPBytes;
-        uint8_t *p_lo = p_hi + C::kPBytes;
         const int sw = r & 7;
         float m_used = -INFINITY, l0 = 0.0f, l1 = 0.0f;
         bool ok = true;
@@ -758,9 +770,13 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
             if (full_tile && !__any_sync(0xffffffffu, bias_tile)) {
                 // every key visible, no bias in this warp: max over the raw
                 // scores (the scale is positive), scale folded into the FMA
+                float m2 = -INFINITY;
 #pragma unroll
-                for (int e = 0; e < 128; ++e) mx = fmaxf(mx, x[e]);
-                mx *= p.score_log2;
+                for (int e = 0; e < 128; e += 4) {
+                    mx = fmax3(mx, x[e], x[e + 1]);
+                    m2 = fmax3(m2, x[e + 2], x[e + 3]);
+                }
+                mx = fmaxf(mx, m2) * p.score_log2;
                 mult = p.score_log2;
             } else {
                 // key e of the tile sits at distance d0 - e from this row:
@@ -788,10 +804,26 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
             const bool resc = mx > m_used + kRescaleTau;
             const float m_new = resc ? mx : m_used;
             const float alpha = (resc && m_used != -INFINITY) ? ex2_fast(m_used - m_new) : 1.0f;
+            // P buffer c % kPBuf was read by the PV of tile c - kPBuf; rescaling
+            // O needs the PV of tile c - 1 to be done as well
+            const bool rescale_o = __any_sync(0xffffffffu, alpha != 1.0f);
+            if (c >= C::kPBuf) {
+                const int pc = c - C::kPBuf;
+                if (!warp_wait_p(&o_done[2 * k + pc % C::kPBuf], (pc / C::kPBuf) & 1, fail, p.err)) {
+                    ok = false;
+                    break;
+                }
+            }
+            if (c >= 1 && rescale_o && C::kPBuf > 1) {
+                const int pc = c - 1;
+                if (!warp_wait_p(&o_done[2 * k + pc % C::kPBuf], (pc / C::kPBuf) & 1, fail, p.err)) {
+                    ok = false;
+                    break;
+                }
+            }
             if (c >= 1) {
-                if (!warp_wait_p(&o_done[k], (c - 1) & 1, fail, p.err)) { ok = false; break; }
                 tc_fence_after_sync();
-                if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+                if (rescale_o) {
 #pragma unroll 1
                     for (int q = 0; q < D / 32; ++q) {
                         float o[32];
@@ -807,6 +839,8 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
             l1 *= alpha;
             m_used = m_new;
             const float neg_m8 = (m_used == -INFINITY) ? 0.0f : kPOffset - m_used;
+            uint8_t *p_hi = smem + C::kOffP + (k * C::kPBuf + c % C::kPBuf) * 2 * C::kPBytes;
+            uint8_t *p_lo = p_hi + C::kPBytes;
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
                 uint4 hi, lo;
@@ -827,10 +861,11 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
             fence_proxy_async_smem();
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full[k]);
+            if (lane == 0) mbar_arrive(&p_full[2 * k + c % C::kPBuf]);
             ++c;
         }
-        if (ok && c > 0 && warp_wait_p(&o_done[k], (c - 1) & 1, fail, p.err)) {
+        if (ok && c > 0 &&
+            warp_wait_p(&o_done[2 * k + (c - 1) % C::kPBuf], ((c - 1) / C::kPBuf) & 1, fail, p.err)) {
             tc_fence_after_sync();
             const float l = l0 + l1;
             const float f = (l > 0.0f) ? p.v_scale / l : 0.0f;
@@ -965,7 +1000,7 @@ extern "C" fp8kv_status attn_fp8_varlen_prefill(
     p.rel_extent = rel_bias ? rel_extent : 0;
     p.window = window;
     p.n_qtiles = (max_seqlen_q + kTile - 1) / kTile;
-    p.q_scale = q_scale;
+    p.q_scale = make_qscale(q_scale);
     p.score_log2 = static_cast<float>(static_cast<double>(softmax_scale) * q_scale * k_scale *
                                       1.4426950408889634);
     p.v_scale = v_scale;

@@ -9,6 +9,7 @@
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
+#include <math.h>
 #include <stdint.h>
 
 #include "../../include/fp8kv.h"
@@ -46,24 +47,57 @@ __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float a, float b) {
     return static_cast<uint16_t>(__nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3));
 }
 
+// A per-tensor scale as the kernels use it.  x / s is the IEEE fp32 quotient;
+// when s is a power of two (1.0 included) x * (1 / s) is the same real
+// number rounded the same way (1 / s is exact and both operations round
+// once to nearest), so the kernels multiply instead of dividing.
+struct QScale {
+    float scale;
+    float inv;       // 1 / scale, used when pow2 != 0
+    uint32_t pow2;
+};
+
+inline QScale make_qscale(float s) {
+    int e = 0;
+    const float m = frexpf(s, &e);
+    const float inv = 1.0f / s;
+    QScale q;
+    q.scale = s;
+    q.inv = inv;
+    q.pow2 = (m == 0.5f && isnormal(inv) && isnormal(s)) ? 1u : 0u;
+    return q;
+}
+
+__device__ __forceinline__ float scale_div(float x, const QScale &q) {
+    return q.pow2 ? x * q.inv : __fdiv_rn(x, q.scale);
+}
+
 // Quantize two fp32 values (already in the value domain) by a per-tensor
 // scale: IEEE fp32 division, clamp to +-448 keeping NaN, nearest-even e4m3
 // with saturation.  `sign_a` / `sign_b` are the sign bits of the inputs,
 // copied into the bytes so that -NaN and -0 keep their sign (the division
 // returns the canonical positive NaN).  Returns lo byte = a, hi byte = b.
-__device__ __forceinline__ uint32_t quantize_pair(float a, float b, float scale,
+__device__ __forceinline__ uint32_t quantize_pair(float a, float b, const QScale &scale,
                                                   uint32_t sign_a, uint32_t sign_b) {
-    a = __fdiv_rn(a, scale);
-    b = __fdiv_rn(b, scale);
+    a = scale_div(a, scale);
+    b = scale_div(b, scale);
     a = a > kE4M3Max ? kE4M3Max : (a < -kE4M3Max ? -kE4M3Max : a);
     b = b > kE4M3Max ? kE4M3Max : (b < -kE4M3Max ? -kE4M3Max : b);
     return static_cast<uint32_t>(f32x2_to_e4m3x2(a, b)) | (sign_a << 7) | (sign_b << 15);
 }
 
 // Quantize the two bf16 elements packed in `word` (element 0 in the low half).
-__device__ __forceinline__ uint32_t quantize_bf16x2(uint32_t word, float scale) {
+__device__ __forceinline__ uint32_t quantize_bf16x2(uint32_t word, const QScale &scale) {
     return quantize_pair(__uint_as_float(word << 16), __uint_as_float(word & 0xFFFF0000u), scale,
                          (word >> 15) & 1u, word >> 31);
+}
+
+// max(a, b, c) in one instruction (sm_100 and later); a NaN operand is
+// ignored like fmaxf does.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
 }
 
 // packed e4m3x2 -> two halves (exact: every e4m3 value is an fp16 value).

@@ -16,7 +16,7 @@ constexpr int kChunk = 16;   // elements per thread-step
 
 // 16 bf16 elements -> 16 e4m3 bytes (quantize_bf16x2: IEEE fp32 x / s,
 // clamp to +-448 keeping NaN, nearest-even saturating conversion, sign kept).
-__device__ __forceinline__ uint4 quantize16(const uint4 lo, const uint4 hi, float s) {
+__device__ __forceinline__ uint4 quantize16(const uint4 lo, const uint4 hi, const QScale &s) {
     const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
     uint32_t out[4];
 #pragma unroll
@@ -30,7 +30,7 @@ kv_store_kernel(const uint16_t *__restrict__ k, const uint16_t *__restrict__ v, 
                 int64_t v_stride, const int64_t *__restrict__ slots, int64_t num_tokens,
                 int32_t row_elems, int32_t head_dim, int32_t num_kv_heads, int32_t block_size,
                 int64_t capacity, uint8_t *__restrict__ ck, uint8_t *__restrict__ cv,
-                float k_scale, float v_scale, uint32_t *err) {
+                const QScale k_scale, const QScale v_scale, uint32_t *err) {
     const int32_t chunks = row_elems / kChunk;
     const int64_t total = num_tokens * chunks;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
@@ -153,7 +153,7 @@ extern "C" fp8kv_status kv_store_e4m3(const fp8kv_cache *cache, const fp8kv_bf16
     kv_store_kernel<<<grid, kStoreThreads, 0, static_cast<cudaStream_t>(stream)>>>(
         k, v, k_tok_stride, v_tok_stride, slot_mapping, num_tokens, static_cast<int32_t>(row),
         cache->head_dim, cache->num_kv_heads, cache->block_size, capacity, cache->k, cache->v,
-        k_scale, v_scale, err);
+        make_qscale(k_scale), make_qscale(v_scale), err);
     if (cudaGetLastError() != cudaSuccess) return FP8KV_ERR_LAUNCH;
     return FP8KV_OK;
 }
