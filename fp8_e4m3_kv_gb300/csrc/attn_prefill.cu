@@ -437,8 +437,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
 // One CTA computes query tiles 2c and 2c + 1 (256 rows) of one head of one
 // sequence.  Both tiles share every K/V tile the producer loads; TMEM holds
 // S0, S1 (128 columns each) and O0, O1 (128 columns each).  Warpgroup k (warps
-// 4k .. 4k + 3) runs the softmax of query tile k; the MMA warp interleaves the
-// two tiles' QK and PV products.  Per element the softmax is one FMA (the
+// 4k .. 4k + 3) runs the softmax of query tile k; one MMA thread per query
+// tile issues its QK and PV products.  Each key tile is worked in two halves
+// of 64 keys, each with its own half of S and of P, so that S and P are
+// double-buffered within the same TMEM and shared memory and the lazy rescale
+// is decided per half.  Per element the softmax is one FMA (the
 // folded score scale and the running max), one ex2, the row sum, and the
 // two-term e4m3 split done on packed f16 pairs.
 // ---------------------------------------------------------------------------
@@ -454,26 +457,19 @@ constexpr int kRegsIo = 56;
 static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsIo <= kPre2Threads * kRegsLaunch,
               "register split exceeds the launch's registers");
 
-#ifndef FP8KV_PREFILL_PBUF
-#define FP8KV_PREFILL_PBUF 1
-#endif
-
 struct Pre2Cfg {
-    // P buffers per query tile: 2 lets a tile's softmax write while the
-    // previous tile's PV runs, at the cost of a K/V stage
-    static constexpr int kPBuf = FP8KV_PREFILL_PBUF;
-    static constexpr int kStages = kPBuf == 2 ? 2 : 3;
+    static constexpr int kStages = 3;
     static constexpr int kTileBytes = kTile * 128;          // K or V tile, 16 KB
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kQBytes = kTile * 128;             // one Q8 tile, 16 KB
     static constexpr int kPBytes = kTile * kTile;           // one P term, 16 KB
     static constexpr int kOffQ = 0;                         // [2] Q8 tiles
     static constexpr int kOffStages = 2 * kQBytes;
-    // P: [query tile][kPBuf buffers][hi, lo] (16 KB each term)
-    static constexpr int kOffP = kOffStages + kStages * kStageBytes;
-    static constexpr int kOffMisc = kOffP + 2 * kPBuf * 2 * kPBytes;
+    static constexpr int kOffP = kOffStages + kStages * kStageBytes;   // [query tile][hi, lo]
+    static constexpr int kOffMisc = kOffP + 2 * 2 * kPBytes;
     static constexpr int kSmemBytes = kOffMisc + 512 + 1024;
     static constexpr uint32_t kTmemCols = 512;              // S0 S1 O0 O1
+    static constexpr int kHalf = kTile / 2;                 // keys per unit
 };
 
 __device__ __forceinline__ float ex2_fast(float x) {
@@ -556,11 +552,12 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffMisc);
     uint64_t *full = bars;              // [kStages]
     uint64_t *empty = bars + 4;         // [kStages]
-    uint64_t *s_full = bars + 8;        // [query tile]
-    uint64_t *s_free = bars + 10;       // [query tile]
-    uint64_t *p_full = bars + 12;       // [query tile][P buffer]
-    uint64_t *o_done = bars + 16;       // [query tile][P buffer]: PV that read the buffer is done
-    uint64_t *mma_done = bars + 20;     // [query tile]
+    // per query tile k and key half hh, index 2k + hh
+    uint64_t *s_full = bars + 8;        // S half written by QK
+    uint64_t *s_free = bars + 12;       // S half read into registers
+    uint64_t *p_full = bars + 16;       // P half written
+    uint64_t *o_done = bars + 20;       // PV of the P half complete
+    uint64_t *mma_done = bars + 24;     // [query tile]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc + 256);
     CtaFail *fail = reinterpret_cast<CtaFail *>(smem + C::kOffMisc + 260);
 
@@ -569,15 +566,13 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 2);   // one arrival per MMA issuer
         }
-        for (int k = 0; k < 2; ++k) {
-            mbar_init(&s_full[k], 1);
-            mbar_init(&s_free[k], 4);
-            for (int b2 = 0; b2 < 2; ++b2) {
-                mbar_init(&p_full[2 * k + b2], 4);
-                mbar_init(&o_done[2 * k + b2], 1);
-            }
-            mbar_init(&mma_done[k], 1);
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_free[i], 4);
+            mbar_init(&p_full[i], 4);
+            mbar_init(&o_done[i], 1);
         }
+        for (int k = 0; k < 2; ++k) mbar_init(&mma_done[k], 1);
         fail->abort = 0;
         fence_mbar_init();
     }
@@ -659,42 +654,43 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
       } else if (warp == 9 || warp == 10) {
         // ------------------------------------------------------------ MMA issuers
         // One thread per query tile k (warp 9: tile 0, warp 10: tile 1), so
-        // neither tile's chain waits on the other's.  For each key tile j the
-        // tile uses: S_k = Q8_k . K_j^T, then O_k += P_k . V of the tile it
-        // used before.  A stage is released once both threads are done with
-        // it (empty[] counts two arrivals).
+        // neither tile's chain waits on the other's.  Work goes in units of
+        // 64 keys: unit u is half u & 1 of a key tile, with its own S half
+        // (TMEM columns k*128 + 64*(u & 1)) and P half (key bytes 64*(u & 1)
+        // of each P row).  After S of unit u the thread issues the PV of
+        // unit u - 1, so the softmax of one half overlaps the QK of the next
+        // and the PV of the last.  A stage is released once both threads
+        // are done with it (empty[] counts two arrivals).
         const int k = warp - 9;
         if (lane == 0) {
-            const uint32_t idesc_qk = idesc_e4m3_f32(128, 128, false, false);
+            const uint32_t idesc_qk = idesc_e4m3_f32(128, C::kHalf, false, false);
             const uint32_t idesc_pv = idesc_e4m3_f32(128, 128, false, true);
             const uint32_t q_addr = smem_u32(smem + C::kOffQ + k * C::kQBytes);
-            int n_qk = 0, n_pv = 0, prev = -1;
+            const uint32_t p_addr = smem_u32(smem + C::kOffP + k * 2 * C::kPBytes);
+            int u = 0, last_j = -1;   // units whose QK was issued; last key tile used
             bool ok = true;
-            // PV of key tile jj (the tile this query tile used before), then
-            // release its stage
-            auto issue_pv = [&](int jj) -> bool {
-                const int s = jj % C::kStages;
-                const int pb = n_pv % C::kPBuf;
-                const uint32_t ph = (n_pv / C::kPBuf) & 1;
-                if (!mbar_wait(&p_full[2 * k + pb], ph, fail, p.err)) return false;
+            // O_k += P_k[:, half] . V_jj[half, :] for unit v (half v & 1 of
+            // key tile jj); the second half releases the stage
+            auto issue_pv = [&](int v, int jj) -> bool {
+                const int hv = v & 1;
+                if (!mbar_wait(&p_full[2 * k + hv], (v >> 1) & 1, fail, p.err)) return false;
                 tc_fence_after_sync();
+                const int s = jj % C::kStages;
                 const uint32_t v_addr =
                     smem_u32(smem + C::kOffStages + s * C::kStageBytes + C::kTileBytes);
-                const uint32_t p_addr =
-                    smem_u32(smem + C::kOffP + (k * C::kPBuf + pb) * 2 * C::kPBytes);
 #pragma unroll
                 for (int part = 0; part < 2; ++part) {
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t a = sdesc_sw128(p_addr + part * C::kPBytes + kk * 32, 16, 1024);
-                        const uint64_t bd = sdesc_sw128(v_addr + kk * 32 * 128, kTile * 128, 1024);
+                    for (int kk = 0; kk < 2; ++kk) {
+                        const int ks = 2 * hv + kk;   // 32-key step within the tile
+                        const uint64_t a = sdesc_sw128(p_addr + part * C::kPBytes + ks * 32, 16, 1024);
+                        const uint64_t bd = sdesc_sw128(v_addr + ks * 32 * 128, kTile * 128, 1024);
                         mma_e4m3(tmem + 256 + k * 128, a, bd, idesc_pv,
-                                 (n_pv > 0 || part > 0 || kk > 0) ? 1u : 0u);
+                                 (v > 0 || part > 0 || kk > 0) ? 1u : 0u);
                     }
                 }
-                tc_commit(&o_done[2 * k + pb]);
-                tc_commit(&empty[s]);
-                ++n_pv;
+                tc_commit(&o_done[2 * k + hv]);
+                if (hv == 1) tc_commit(&empty[s]);
                 return true;
             };
             for (int j = 0; j < ntiles && ok; ++j) {
@@ -705,21 +701,30 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
                     mbar_arrive(&empty[s]);
                     continue;
                 }
-                if (!mbar_wait(&s_free[k], (n_qk & 1) ^ 1, fail, p.err)) { ok = false; break; }
-                tc_fence_after_sync();
                 const uint32_t k_addr = smem_u32(smem + C::kOffStages + s * C::kStageBytes);
+                for (int hh = 0; hh < 2; ++hh) {
+                    if (!mbar_wait(&s_free[2 * k + hh], ((u >> 1) & 1) ^ 1, fail, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t a = sdesc_sw128(q_addr + kk * 32, 16, 1024);
-                    const uint64_t bd = sdesc_sw128(k_addr + kk * 32, 16, 1024);
-                    mma_e4m3(tmem + k * 128, a, bd, idesc_qk, kk > 0);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t a = sdesc_sw128(q_addr + kk * 32, 16, 1024);
+                        const uint64_t bd =
+                            sdesc_sw128(k_addr + hh * C::kHalf * 128 + kk * 32, 16, 1024);
+                        mma_e4m3(tmem + k * 128 + hh * C::kHalf, a, bd, idesc_qk, kk > 0);
+                    }
+                    tc_commit(&s_full[2 * k + hh]);
+                    ++u;
+                    if (u >= 2 && !issue_pv(u - 2, hh == 1 ? j : last_j)) {
+                        ok = false;
+                        break;
+                    }
                 }
-                tc_commit(&s_full[k]);
-                ++n_qk;
-                if (prev >= 0 && !issue_pv(prev)) { ok = false; break; }
-                prev = j;
+                last_j = j;
             }
-            if (ok && prev >= 0) issue_pv(prev);
+            if (ok && u > 0) issue_pv(u - 1, last_j);
             tc_commit(&mma_done[k]);
             mbar_drain_p(&mma_done[k], 0, p.err);
         }
@@ -749,123 +754,127 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
         bool ok = true;
         int c = 0;   // key tiles processed by this query tile
         for (int j = static_cast<int>(my_lo - kt0); j <= static_cast<int>(my_hi - kt0) &&
-                                                    (k == 0 || act1);
+                                                    (k == 0 || act1) && ok;
              ++j) {
-            if (!warp_wait_p(&s_full[k], c & 1, fail, p.err)) { ok = false; break; }
-            tc_fence_after_sync();
-
             const int64_t k0 = (kt0 + j) * kTile;
-            const bool full_tile = (k0 + kTile - 1 <= pos_first) &&
-                                   (p.window == 0 || pos_last - k0 < p.window);
-            const bool bias_tile = bias_row != nullptr && pos - k0 >= 0 &&
-                                   pos - k0 - (kTile - 1) < p.rel_extent;
-            float x[128];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) tmem_ld_x32(tmem + lane_base + col_s + q * 32, x + q * 32);
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s_free[k]);
-
-            float mult, mx = -INFINITY;
-            if (full_tile && !__any_sync(0xffffffffu, bias_tile)) {
-                // every key visible, no bias in this warp: max over the raw
-                // scores (the scale is positive), scale folded into the FMA
-                float m2 = -INFINITY;
-#pragma unroll
-                for (int e = 0; e < 128; e += 4) {
-                    mx = fmax3(mx, x[e], x[e + 1]);
-                    m2 = fmax3(m2, x[e + 2], x[e + 3]);
-                }
-                mx = fmaxf(mx, m2) * p.score_log2;
-                mult = p.score_log2;
-            } else {
-                // key e of the tile sits at distance d0 - e from this row:
-                // visible for e in [e_lo, e_hi] (causal, window, sequence end);
-                // biased for e in [b_lo, d0] (distance below the extent)
-                const int32_t d0 = static_cast<int32_t>(pos - k0);   // < 2^31: positions are int32
-                const int32_t keys_left =
-                    static_cast<int32_t>(len_k - k0 < kTile ? len_k - k0 : kTile);
-                const int32_t e_hi = min(d0, keys_left - 1);
-                const int32_t e_lo = p.window > 0 ? max(0, d0 - p.window + 1) : 0;
-                const int32_t b_lo = bias_tile ? max(0, d0 - p.rel_extent + 1) : 1 << 30;
-                const uint16_t *brow = bias_tile ? bias_row + d0 : nullptr;   // brow[-e] = bias(e)
-#pragma unroll
-                for (int e = 0; e < 128; ++e) {
-                    float zz = x[e] * p.score_log2;
-                    if (e >= b_lo && e <= d0) zz = fmaf(bf16_bits_to_float(__ldg(brow - e)), kLog2eP, zz);
-                    zz = (e >= e_lo && e <= e_hi) ? zz : -INFINITY;
-                    x[e] = zz;
-                    mx = fmaxf(mx, zz);
-                }
-                mult = 1.0f;
-            }
-            // lazy rescale: move the reference max only when the row max grew
-            // by more than tau, so P <= 2^(8 + tau) stays below 448
-            const bool resc = mx > m_used + kRescaleTau;
-            const float m_new = resc ? mx : m_used;
-            const float alpha = (resc && m_used != -INFINITY) ? ex2_fast(m_used - m_new) : 1.0f;
-            // P buffer c % kPBuf was read by the PV of tile c - kPBuf; rescaling
-            // O needs the PV of tile c - 1 to be done as well
-            const bool rescale_o = __any_sync(0xffffffffu, alpha != 1.0f);
-            if (c >= C::kPBuf) {
-                const int pc = c - C::kPBuf;
-                if (!warp_wait_p(&o_done[2 * k + pc % C::kPBuf], (pc / C::kPBuf) & 1, fail, p.err)) {
-                    ok = false;
-                    break;
-                }
-            }
-            if (c >= 1 && rescale_o && C::kPBuf > 1) {
-                const int pc = c - 1;
-                if (!warp_wait_p(&o_done[2 * k + pc % C::kPBuf], (pc / C::kPBuf) & 1, fail, p.err)) {
-                    ok = false;
-                    break;
-                }
-            }
-            if (c >= 1) {
+            for (int hh = 0; hh < 2; ++hh) {
+                const int u = 2 * c + hh;   // unit: key half hh of this key tile
+                if (!warp_wait_p(&s_full[2 * k + hh], c & 1, fail, p.err)) { ok = false; break; }
                 tc_fence_after_sync();
-                if (rescale_o) {
-#pragma unroll 1
-                    for (int q = 0; q < D / 32; ++q) {
-                        float o[32];
-                        const uint32_t ta = tmem + lane_base + col_o + q * 32;
-                        tmem_ld_x32(ta, o);
+                if (hh == 0 && k0 + r >= len_k) {
+                    // keys past the end of the sequence may hold stale bytes
+                    // (NaN codes included): zero their V rows so that 0 * V
+                    // stays 0 in the MMA.  S of this tile being written means
+                    // the stage's TMA copies have landed.
+                    uint4 *q4 = reinterpret_cast<uint4 *>(smem + C::kOffStages +
+                                                          (j % C::kStages) * C::kStageBytes +
+                                                          C::kTileBytes + r * 128);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] *= alpha;
-                        tmem_st_x32(ta, o);
+                    for (int e = 0; e < 8; ++e) q4[e] = make_uint4(0, 0, 0, 0);
+                }
+                const int64_t kh = k0 + hh * C::kHalf;
+                const bool full_half = (kh + C::kHalf - 1 <= pos_first) &&
+                                       (p.window == 0 || pos_last - kh < p.window);
+                const bool bias_half = bias_row != nullptr && pos - kh >= 0 &&
+                                       pos - kh - (C::kHalf - 1) < p.rel_extent;
+                float x[C::kHalf];
+                tmem_ld_x32(tmem + lane_base + col_s + hh * C::kHalf, x);
+                tmem_ld_x32(tmem + lane_base + col_s + hh * C::kHalf + 32, x + 32);
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s_free[2 * k + hh]);
+
+                float mult, mx = -INFINITY;
+                if (full_half && !__any_sync(0xffffffffu, bias_half)) {
+                    // every key visible, no bias in this warp: max over the
+                    // raw scores (the scale is positive), scale folded into
+                    // the FMA
+                    float m2 = -INFINITY;
+#pragma unroll
+                    for (int e = 0; e < C::kHalf; e += 4) {
+                        mx = fmax3(mx, x[e], x[e + 1]);
+                        m2 = fmax3(m2, x[e + 2], x[e + 3]);
+                    }
+                    mx = fmaxf(mx, m2) * p.score_log2;
+                    mult = p.score_log2;
+                } else {
+                    // key e of the half sits at distance d0 - e from this row:
+                    // visible for e in [e_lo, e_hi] (causal, window, sequence
+                    // end); biased for e in [b_lo, d0] (distance below the
+                    // extent)
+                    const int32_t d0 = static_cast<int32_t>(pos - kh);   // positions are int32
+                    const int32_t keys_left =
+                        static_cast<int32_t>(len_k - kh < C::kHalf ? len_k - kh : C::kHalf);
+                    const int32_t e_hi = min(d0, keys_left - 1);
+                    const int32_t e_lo = p.window > 0 ? max(0, d0 - p.window + 1) : 0;
+                    const int32_t b_lo = bias_half ? max(0, d0 - p.rel_extent + 1) : 1 << 30;
+                    const uint16_t *brow = bias_half ? bias_row + d0 : nullptr;   // brow[-e] = bias(e)
+#pragma unroll
+                    for (int e = 0; e < C::kHalf; ++e) {
+                        float zz = x[e] * p.score_log2;
+                        if (e >= b_lo && e <= d0)
+                            zz = fmaf(bf16_bits_to_float(__ldg(brow - e)), kLog2eP, zz);
+                        zz = (e >= e_lo && e <= e_hi) ? zz : -INFINITY;
+                        x[e] = zz;
+                        mx = fmaxf(mx, zz);
+                    }
+                    mult = 1.0f;
+                }
+                // lazy rescale: move the reference max only when the row max
+                // grew by more than tau, so P <= 2^(8 + tau) stays below 448
+                const bool resc = mx > m_used + kRescaleTau;
+                const float m_new = resc ? mx : m_used;
+                const float alpha = (resc && m_used != -INFINITY) ? ex2_fast(m_used - m_new) : 1.0f;
+                const bool rescale_o = __any_sync(0xffffffffu, alpha != 1.0f);
+                // this P half was read by the PV of unit u - 2; rescaling O
+                // needs the PV of unit u - 1 (the other half) done as well
+                if (u >= 2 && !warp_wait_p(&o_done[2 * k + hh], ((u - 2) >> 1) & 1, fail, p.err)) {
+                    ok = false;
+                    break;
+                }
+                if (u >= 1 && rescale_o &&
+                    !warp_wait_p(&o_done[2 * k + (hh ^ 1)], ((u - 1) >> 1) & 1, fail, p.err)) {
+                    ok = false;
+                    break;
+                }
+                if (u >= 1) {
+                    tc_fence_after_sync();
+                    if (rescale_o) {
+#pragma unroll 1
+                        for (int q = 0; q < D / 32; ++q) {
+                            float o[32];
+                            const uint32_t ta = tmem + lane_base + col_o + q * 32;
+                            tmem_ld_x32(ta, o);
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) o[e] *= alpha;
+                            tmem_st_x32(ta, o);
+                        }
                     }
                 }
-            }
-            l0 *= alpha;
-            l1 *= alpha;
-            m_used = m_new;
-            const float neg_m8 = (m_used == -INFINITY) ? 0.0f : kPOffset - m_used;
-            uint8_t *p_hi = smem + C::kOffP + (k * C::kPBuf + c % C::kPBuf) * 2 * C::kPBytes;
-            uint8_t *p_lo = p_hi + C::kPBytes;
+                l0 *= alpha;
+                l1 *= alpha;
+                m_used = m_new;
+                const float neg_m8 = (m_used == -INFINITY) ? 0.0f : kPOffset - m_used;
+                uint8_t *p_hi = smem + C::kOffP + k * 2 * C::kPBytes;
+                uint8_t *p_lo = p_hi + C::kPBytes;
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                uint4 hi, lo;
-                p_chunk16(x + q * 16, mult, neg_m8, l0, l1, hi, lo);
-                const uint32_t off = r * 128 + ((q ^ sw) << 4);
-                *reinterpret_cast<uint4 *>(p_hi + off) = hi;
-                *reinterpret_cast<uint4 *>(p_lo + off) = lo;
+                for (int q = 0; q < C::kHalf / 16; ++q) {
+                    uint4 hi, lo;
+                    p_chunk16(x + q * 16, mult, neg_m8, l0, l1, hi, lo);
+                    const uint32_t off = r * 128 + (((hh * (C::kHalf / 16) + q) ^ sw) << 4);
+                    *reinterpret_cast<uint4 *>(p_hi + off) = hi;
+                    *reinterpret_cast<uint4 *>(p_lo + off) = lo;
+                }
+                fence_proxy_async_smem();
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&p_full[2 * k + hh]);
             }
-            // keys past the end of the sequence may hold stale bytes (NaN codes
-            // included): zero their V rows so that 0 * V stays 0 in the MMA
-            if (k0 + r >= len_k) {
-                uint4 *q4 = reinterpret_cast<uint4 *>(smem + C::kOffStages +
-                                                      (j % C::kStages) * C::kStageBytes +
-                                                      C::kTileBytes + r * 128);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) q4[e] = make_uint4(0, 0, 0, 0);
-            }
-            fence_proxy_async_smem();
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full[2 * k + c % C::kPBuf]);
-            ++c;
+            if (ok) ++c;
         }
-        if (ok && c > 0 &&
-            warp_wait_p(&o_done[2 * k + (c - 1) % C::kPBuf], ((c - 1) / C::kPBuf) & 1, fail, p.err)) {
+        // the last unit is the second half of the last key tile; its PV
+        // completing means every earlier MMA of this thread completed too
+        if (ok && c > 0 && warp_wait_p(&o_done[2 * k + 1], (c - 1) & 1, fail, p.err)) {
             tc_fence_after_sync();
             const float l = l0 + l1;
             const float f = (l > 0.0f) ? p.v_scale / l : 0.0f;
