@@ -66,6 +66,7 @@ struct PrefillParams {
     int32_t rel_extent;
     int32_t window;
     int32_t n_qtiles;
+    int32_t bias_vec;   // rows 16-byte aligned with an extent that is a multiple of 8
     QScale q_scale;
     float score_log2;   // softmax_scale * q_scale * k_scale * log2(e)
     float v_scale;
@@ -506,6 +507,53 @@ __device__ __forceinline__ void p_chunk16(const float *x, float mult, float neg_
     lo = make_uint4(lw[0], lw[1], lw[2], lw[3]);
 }
 
+// The bias of 64 consecutive keys of one row, fetched before any of it is
+// used: Y holds row[lo + i] at half i (i = 0 .. 63, lo = d0 - 63, so key e of
+// the half, at distance d0 - e, is half 63 - e) and 0 where lo + i is outside
+// [0, extent) or row is null.  With vec the row is read as 16-byte chunks
+// from the multiple of 8 at or below lo (a chunk lies wholly inside or
+// outside the extent) and shifted down by the remainder; otherwise as 64
+// independent 2-byte loads.
+__device__ __forceinline__ void load_bias64(const uint16_t *row, int32_t d0, int32_t extent,
+                                            bool vec, uint32_t (&Y)[32]) {
+    const int32_t lo = d0 - 63;
+    if (vec) {
+        const int32_t base = lo & ~7;
+        const int32_t rem = lo - base;   // 0 .. 7 halves
+        uint32_t w[36];
+#pragma unroll
+        for (int c = 0; c < 9; ++c) {
+            const int32_t i0 = base + 8 * c;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (row != nullptr && i0 >= 0 && i0 + 8 <= extent)
+                v = __ldg(reinterpret_cast<const uint4 *>(row + i0));
+            w[4 * c] = v.x;
+            w[4 * c + 1] = v.y;
+            w[4 * c + 2] = v.z;
+            w[4 * c + 3] = v.w;
+        }
+        // shift by rem halves: whole words by rem / 2 (two select stages),
+        // then the odd half with a funnel shift
+        const bool by1 = rem & 2, by2 = rem & 4, odd = rem & 1;
+#pragma unroll
+        for (int m = 0; m < 35; ++m) w[m] = by1 ? w[m + 1] : w[m];
+#pragma unroll
+        for (int m = 0; m < 33; ++m) w[m] = by2 ? w[m + 2] : w[m];
+#pragma unroll
+        for (int m = 0; m < 32; ++m) Y[m] = odd ? __funnelshift_r(w[m], w[m + 1], 16) : w[m];
+    } else {
+        uint16_t hv[64];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+            const int32_t j = lo + i;
+            hv[i] = (row != nullptr && j >= 0 && j < extent) ? __ldg(row + j) : uint16_t(0);
+        }
+#pragma unroll
+        for (int m = 0; m < 32; ++m)
+            Y[m] = static_cast<uint32_t>(hv[2 * m]) | (static_cast<uint32_t>(hv[2 * m + 1]) << 16);
+    }
+}
+
 __global__ void __launch_bounds__(kPre2Threads, 1)
 prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                 const PrefillParams p) {
@@ -784,42 +832,42 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&s_free[2 * k + hh]);
 
-                float mult, mx = -INFINITY;
-                if (full_half && !__any_sync(0xffffffffu, bias_half)) {
-                    // every key visible, no bias in this warp: max over the
-                    // raw scores (the scale is positive), scale folded into
-                    // the FMA
-                    float m2 = -INFINITY;
+                // Scores to log2 units: z = x * score_log2 (+ bias * log2(e)),
+                // -inf where masked.  Where no row of the warp has bias the
+                // scale stays folded into the FMA of P (mult); masking and the
+                // max do not need it, the scale being positive.
+                float mult = p.score_log2;
+                const bool any_bias = __any_sync(0xffffffffu, bias_half);
+                const int32_t d0 = static_cast<int32_t>(pos - kh);   // positions are int32
+                if (any_bias) {
+                    uint32_t Y[32];
+                    load_bias64(bias_half ? bias_row : nullptr, d0, p.rel_extent, p.bias_vec != 0, Y);
 #pragma unroll
-                    for (int e = 0; e < C::kHalf; e += 4) {
-                        mx = fmax3(mx, x[e], x[e + 1]);
-                        m2 = fmax3(m2, x[e + 2], x[e + 3]);
+                    for (int e = 0; e < C::kHalf; ++e) {
+                        const uint32_t wd = Y[(63 - e) >> 1];
+                        const float bv = __uint_as_float(((63 - e) & 1) ? (wd & 0xFFFF0000u) : (wd << 16));
+                        x[e] = fmaf(bv, kLog2eP, x[e] * p.score_log2);
                     }
-                    mx = fmaxf(mx, m2) * p.score_log2;
-                    mult = p.score_log2;
-                } else {
+                    mult = 1.0f;
+                }
+                if (!full_half) {
                     // key e of the half sits at distance d0 - e from this row:
-                    // visible for e in [e_lo, e_hi] (causal, window, sequence
-                    // end); biased for e in [b_lo, d0] (distance below the
-                    // extent)
-                    const int32_t d0 = static_cast<int32_t>(pos - kh);   // positions are int32
+                    // visible for e in [e_lo, e_hi] (causal, window, sequence end)
                     const int32_t keys_left =
                         static_cast<int32_t>(len_k - kh < C::kHalf ? len_k - kh : C::kHalf);
                     const int32_t e_hi = min(d0, keys_left - 1);
                     const int32_t e_lo = p.window > 0 ? max(0, d0 - p.window + 1) : 0;
-                    const int32_t b_lo = bias_half ? max(0, d0 - p.rel_extent + 1) : 1 << 30;
-                    const uint16_t *brow = bias_half ? bias_row + d0 : nullptr;   // brow[-e] = bias(e)
 #pragma unroll
-                    for (int e = 0; e < C::kHalf; ++e) {
-                        float zz = x[e] * p.score_log2;
-                        if (e >= b_lo && e <= d0)
-                            zz = fmaf(bf16_bits_to_float(__ldg(brow - e)), kLog2eP, zz);
-                        zz = (e >= e_lo && e <= e_hi) ? zz : -INFINITY;
-                        x[e] = zz;
-                        mx = fmaxf(mx, zz);
-                    }
-                    mult = 1.0f;
+                    for (int e = 0; e < C::kHalf; ++e)
+                        x[e] = (e >= e_lo && e <= e_hi) ? x[e] : -INFINITY;
                 }
+                float mx = -INFINITY, m2 = -INFINITY;
+#pragma unroll
+                for (int e = 0; e < C::kHalf; e += 4) {
+                    mx = fmax3(mx, x[e], x[e + 1]);
+                    m2 = fmax3(m2, x[e + 2], x[e + 3]);
+                }
+                mx = fmaxf(mx, m2) * mult;
                 // lazy rescale: move the reference max only when the row max
                 // grew by more than tau, so P <= 2^(8 + tau) stays below 448
                 const bool resc = mx > m_used + kRescaleTau;
@@ -1007,6 +1055,8 @@ extern "C" fp8kv_status attn_fp8_varlen_prefill(
     p.G = num_q_heads / Hkv;
     p.block_size = bs;
     p.rel_extent = rel_bias ? rel_extent : 0;
+    p.bias_vec = rel_bias && (reinterpret_cast<uintptr_t>(rel_bias) & 15) == 0 &&
+                 bias_tok_stride % 8 == 0 && rel_extent % 8 == 0;
     p.window = window;
     p.n_qtiles = (max_seqlen_q + kTile - 1) / kTile;
     p.q_scale = make_qscale(q_scale);
