@@ -473,6 +473,10 @@ struct Pre2Cfg {
     static constexpr int kHalf = kTile / 2;                 // keys per unit
 };
 
+__device__ __forceinline__ void prefetch_l2(const void *ptr) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
+
 __device__ __forceinline__ float ex2_fast(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -606,6 +610,7 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     uint64_t *p_full = bars + 16;       // P half written
     uint64_t *o_done = bars + 20;       // PV of the P half complete
     uint64_t *mma_done = bars + 24;     // [query tile]
+    uint64_t *q_full = bars + 26;       // [query tile] Q8 written
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc + 256);
     CtaFail *fail = reinterpret_cast<CtaFail *>(smem + C::kOffMisc + 260);
 
@@ -620,34 +625,14 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
             mbar_init(&p_full[i], 4);
             mbar_init(&o_done[i], 1);
         }
-        for (int k = 0; k < 2; ++k) mbar_init(&mma_done[k], 1);
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(&mma_done[k], 1);
+            mbar_init(&q_full[k], 4);
+        }
         fail->abort = 0;
         fence_mbar_init();
     }
     if (warp == 9) tmem_alloc(tmem_slot, C::kTmemCols);
-    if (warp < 8) {
-        // Q8 row r of query tile k = e4m3(q / q_scale); rows past the
-        // sequence's queries are zero.
-        const int k = warp >> 2, r = threadIdx.x & 127;
-        const int qt = 2 * pair + k;
-        const uint16_t *qrow = p.q + (static_cast<int64_t>(q_first) + qt * kTile + r) * p.Hq * D +
-                               static_cast<int64_t>(h) * D;
-        uint8_t *q8 = smem + C::kOffQ + k * C::kQBytes;
-#pragma unroll 4
-        for (int c = 0; c < D / 16; ++c) {
-            uint4 packed = make_uint4(0, 0, 0, 0);
-            if (r < n_rows[k]) {
-                const uint4 w0 = *reinterpret_cast<const uint4 *>(qrow + c * 16);
-                const uint4 w1 = *reinterpret_cast<const uint4 *>(qrow + c * 16 + 8);
-                packed.x = quantize_bf16x2(w0.x, p.q_scale) | (quantize_bf16x2(w0.y, p.q_scale) << 16);
-                packed.y = quantize_bf16x2(w0.z, p.q_scale) | (quantize_bf16x2(w0.w, p.q_scale) << 16);
-                packed.z = quantize_bf16x2(w1.x, p.q_scale) | (quantize_bf16x2(w1.y, p.q_scale) << 16);
-                packed.w = quantize_bf16x2(w1.z, p.q_scale) | (quantize_bf16x2(w1.w, p.q_scale) << 16);
-            }
-            *reinterpret_cast<uint4 *>(q8 + r * 128 + ((c ^ (r & 7)) << 4)) = packed;
-        }
-        fence_proxy_async_smem();
-    }
     if (warp == 8 && lane == 0) {
         tma_prefetch_map(&kmap);
         tma_prefetch_map(&vmap);
@@ -716,7 +701,7 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
             const uint32_t q_addr = smem_u32(smem + C::kOffQ + k * C::kQBytes);
             const uint32_t p_addr = smem_u32(smem + C::kOffP + k * 2 * C::kPBytes);
             int u = 0, last_j = -1;   // units whose QK was issued; last key tile used
-            bool ok = true;
+            bool ok = true, q_ready = false;
             // O_k += P_k[:, half] . V_jj[half, :] for unit v (half v & 1 of
             // key tile jj); the second half releases the stage
             auto issue_pv = [&](int v, int jj) -> bool {
@@ -751,6 +736,10 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
                 }
                 const uint32_t k_addr = smem_u32(smem + C::kOffStages + s * C::kStageBytes);
                 for (int hh = 0; hh < 2; ++hh) {
+                    if (!q_ready && !(q_ready = mbar_wait(&q_full[k], 0, fail, p.err))) {
+                        ok = false;
+                        break;
+                    }
                     if (!mbar_wait(&s_free[2 * k + hh], ((u >> 1) & 1) ^ 1, fail, p.err)) {
                         ok = false;
                         break;
@@ -798,6 +787,44 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
                                             p.bias_tok_stride + static_cast<int64_t>(h) * p.rel_extent
                               : nullptr;
         const int sw = r & 7;
+        {
+            // Q8 of this query tile = e4m3(q / q_scale), rows past the
+            // sequence's queries zero.  Warp wq loads rows 32 wq .. 32 wq + 31,
+            // two rows per load instruction (16 lanes x 16 bytes per row),
+            // with all sixteen loads in flight; meanwhile the producer has
+            // started on the first K/V tiles.
+            uint8_t *q8 = smem + C::kOffQ + k * C::kQBytes;
+            const int row_in_pair = lane >> 4, col = lane & 15;   // 8 bf16 per lane
+            uint4 v[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int row = 32 * wq + 2 * i + row_in_pair;
+                v[i] = make_uint4(0, 0, 0, 0);
+                if (row < my_rows)
+                    v[i] = __ldg(reinterpret_cast<const uint4 *>(
+                        p.q + (static_cast<int64_t>(q_first) + qt * kTile + row) * p.Hq * D +
+                        static_cast<int64_t>(h) * D + col * 8));
+            }
+            // this row's bias is read on the diagonal key tiles: start it
+            // toward L2 now
+            if (bias_row != nullptr) {
+                for (int off = 0; off < p.rel_extent; off += 64) prefetch_l2(bias_row + off);
+                prefetch_l2(bias_row + p.rel_extent - 1);
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int row = 32 * wq + 2 * i + row_in_pair;
+                const uint32_t lo = quantize_bf16x2(v[i].x, p.q_scale) |
+                                    (quantize_bf16x2(v[i].y, p.q_scale) << 16);
+                const uint32_t hi = quantize_bf16x2(v[i].z, p.q_scale) |
+                                    (quantize_bf16x2(v[i].w, p.q_scale) << 16);
+                *reinterpret_cast<uint2 *>(q8 + row * 128 + (((col >> 1) ^ (row & 7)) << 4) +
+                                           (col & 1) * 8) = make_uint2(lo, hi);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&q_full[k]);
+        }
         float m_used = -INFINITY, l0 = 0.0f, l1 = 0.0f;
         bool ok = true;
         int c = 0;   // key tiles processed by this query tile
