@@ -473,6 +473,17 @@ struct Pre2Cfg {
     static constexpr int kHalf = kTile / 2;                 // keys per unit
 };
 
+// 16 x 8 bf16 -> 16 x 8 e4m3 bytes, the scale's form fixed at compile time.
+template <bool kPow2>
+__device__ __forceinline__ void quantize_q16(const uint4 (&v)[16], uint2 (&o)[16],
+                                             const QScale &s) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        o[i].x = quantize_bf16x2_as<kPow2>(v[i].x, s) | (quantize_bf16x2_as<kPow2>(v[i].y, s) << 16);
+        o[i].y = quantize_bf16x2_as<kPow2>(v[i].z, s) | (quantize_bf16x2_as<kPow2>(v[i].w, s) << 16);
+    }
+}
+
 __device__ __forceinline__ void prefetch_l2(const void *ptr) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
 }
@@ -811,15 +822,16 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
                 for (int off = 0; off < p.rel_extent; off += 64) prefetch_l2(bias_row + off);
                 prefetch_l2(bias_row + p.rel_extent - 1);
             }
+            uint2 q8w[16];
+            if (p.q_scale.pow2)
+                quantize_q16<true>(v, q8w, p.q_scale);
+            else
+                quantize_q16<false>(v, q8w, p.q_scale);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const int row = 32 * wq + 2 * i + row_in_pair;
-                const uint32_t lo = quantize_bf16x2(v[i].x, p.q_scale) |
-                                    (quantize_bf16x2(v[i].y, p.q_scale) << 16);
-                const uint32_t hi = quantize_bf16x2(v[i].z, p.q_scale) |
-                                    (quantize_bf16x2(v[i].w, p.q_scale) << 16);
                 *reinterpret_cast<uint2 *>(q8 + row * 128 + (((col >> 1) ^ (row & 7)) << 4) +
-                                           (col & 1) * 8) = make_uint2(lo, hi);
+                                           (col & 1) * 8) = q8w[i];
             }
             fence_proxy_async_smem();
             __syncwarp();

@@ -72,24 +72,41 @@ __device__ __forceinline__ float scale_div(float x, const QScale &q) {
     return q.pow2 ? x * q.inv : __fdiv_rn(x, q.scale);
 }
 
-// Quantize two fp32 values (already in the value domain) by a per-tensor
-// scale: IEEE fp32 division, clamp to +-448 keeping NaN, nearest-even e4m3
-// with saturation.  `sign_a` / `sign_b` are the sign bits of the inputs,
-// copied into the bytes so that -NaN and -0 keep their sign (the division
+// Clamp two quotients x / s to +-448 keeping NaN, convert them to
+// nearest-even e4m3 with saturation, and set the sign bits `sign_a` /
+// `sign_b` of the inputs, so that -NaN and -0 keep their sign (the division
 // returns the canonical positive NaN).  Returns lo byte = a, hi byte = b.
-__device__ __forceinline__ uint32_t quantize_pair(float a, float b, const QScale &scale,
-                                                  uint32_t sign_a, uint32_t sign_b) {
-    a = scale_div(a, scale);
-    b = scale_div(b, scale);
+__device__ __forceinline__ uint32_t pack_quotients(float a, float b, uint32_t sign_a,
+                                                   uint32_t sign_b) {
     a = a > kE4M3Max ? kE4M3Max : (a < -kE4M3Max ? -kE4M3Max : a);
     b = b > kE4M3Max ? kE4M3Max : (b < -kE4M3Max ? -kE4M3Max : b);
     return static_cast<uint32_t>(f32x2_to_e4m3x2(a, b)) | (sign_a << 7) | (sign_b << 15);
+}
+
+// Quantize two fp32 values (already in the value domain) by a per-tensor
+// scale: IEEE fp32 division (an exact multiply for a power-of-two scale),
+// then pack_quotients.
+__device__ __forceinline__ uint32_t quantize_pair(float a, float b, const QScale &scale,
+                                                  uint32_t sign_a, uint32_t sign_b) {
+    return pack_quotients(scale_div(a, scale), scale_div(b, scale), sign_a, sign_b);
 }
 
 // Quantize the two bf16 elements packed in `word` (element 0 in the low half).
 __device__ __forceinline__ uint32_t quantize_bf16x2(uint32_t word, const QScale &scale) {
     return quantize_pair(__uint_as_float(word << 16), __uint_as_float(word & 0xFFFF0000u), scale,
                          (word >> 15) & 1u, word >> 31);
+}
+
+// quantize_bf16x2 with the scale's form fixed at compile time (kPow2: the
+// scale is a power of two and scale.inv its exact reciprocal), for loops
+// where the compiler would otherwise evaluate both the multiply and the
+// division for every element.
+template <bool kPow2>
+__device__ __forceinline__ uint32_t quantize_bf16x2_as(uint32_t word, const QScale &scale) {
+    const float a = __uint_as_float(word << 16), b = __uint_as_float(word & 0xFFFF0000u);
+    const float qa = kPow2 ? a * scale.inv : __fdiv_rn(a, scale.scale);
+    const float qb = kPow2 ? b * scale.inv : __fdiv_rn(b, scale.scale);
+    return pack_quotients(qa, qb, (word >> 15) & 1u, word >> 31);
 }
 
 // max(a, b, c) in one instruction (sm_100 and later); a NaN operand is
