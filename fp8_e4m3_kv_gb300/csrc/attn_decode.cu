@@ -146,6 +146,26 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, CtaFai
     return __all_sync(0xffffffffu, ok);
 }
 
+// Q8 = e4m3(q / q_scale) for one KV head's group of query heads (rows >= G
+// zero), 128-byte swizzled K-major (row = head, D bytes per row), written by
+// kThreads threads with 8 elements each per step.  The scale's form is a
+// template argument so that only one of multiply / divide is evaluated.
+template <bool kPow2, int D, int kThreads>
+__device__ __forceinline__ void load_q8(uint8_t *q8, const uint16_t *q_group, int G,
+                                        const QScale &s) {
+    for (int e = threadIdx.x * 8; e < kNPad * D; e += kThreads * 8) {
+        const int g = e / D, d = e % D;
+        uint2 packed = make_uint2(0u, 0u);
+        if (g < G) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(q_group + static_cast<int64_t>(g) * D + d);
+            packed.x = quantize_bf16x2_as<kPow2>(w.x, s) | (quantize_bf16x2_as<kPow2>(w.y, s) << 16);
+            packed.y = quantize_bf16x2_as<kPow2>(w.z, s) | (quantize_bf16x2_as<kPow2>(w.w, s) << 16);
+        }
+        *reinterpret_cast<uint2 *>(q8 + (d / 128) * (kNPad * 128) + sw128_offset(g, d % 128)) =
+            packed;
+    }
+}
+
 template <int D, int GMAX>
 __global__ void __launch_bounds__(DecCfg<D>::kThreads, DecCfg<D>::kCtasPerSm)
 decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
@@ -224,18 +244,11 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
         // Q8 = e4m3(q / q_scale) for the group's heads, rows >= G zero;
         // 128-byte swizzled, K-major (row = head, D bytes per row).
         uint8_t *q8 = smem + C::kOffQ;
-        for (int e = threadIdx.x * 8; e < kNPad * D; e += C::kConsumers * 8) {
-            const int g = e / D, d = e % D;
-            uint2 packed = make_uint2(0u, 0u);
-            if (g < p.G) {
-                const uint4 w = *reinterpret_cast<const uint4 *>(
-                    p.q + (static_cast<int64_t>(b) * p.Hq + h0 + g) * D + d);
-                packed.x = quantize_bf16x2(w.x, p.q_scale) | (quantize_bf16x2(w.y, p.q_scale) << 16);
-                packed.y = quantize_bf16x2(w.z, p.q_scale) | (quantize_bf16x2(w.w, p.q_scale) << 16);
-            }
-            *reinterpret_cast<uint2 *>(q8 + (d / 128) * (kNPad * 128) + sw128_offset(g, d % 128)) =
-                packed;
-        }
+        const uint16_t *qb = p.q + (static_cast<int64_t>(b) * p.Hq + h0) * D;
+        if (p.q_scale.pow2)
+            load_q8<true, D, C::kConsumers>(q8, qb, p.G, p.q_scale);
+        else
+            load_q8<false, D, C::kConsumers>(q8, qb, p.G, p.q_scale);
     }
     if (warp == C::kProducerWarp) {
         // zero the P buffers: rows past the group are never written

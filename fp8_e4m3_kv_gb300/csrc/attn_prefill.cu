@@ -494,20 +494,23 @@ __device__ __forceinline__ float ex2_fast(float x) {
     return y;
 }
 
-// P for 16 consecutive keys: p = 2^(x*mult - m8); adds them to l and writes
-// the P_hi and P_lo bytes (16 each) for this row.
-__device__ __forceinline__ void p_chunk16(const float *x, float mult, float neg_m8, float &l0,
-                                          float &l1, uint4 &hi, uint4 &lo) {
+// P for 16 consecutive keys: p = 2^(x*mult - m8); adds them to the two
+// partial row sums l and writes the P_hi and P_lo bytes (16 each) for this
+// row.  The scale and the sums use the packed two-lane fp32 instructions.
+__device__ __forceinline__ void p_chunk16(const float *x, float mult, float neg_m8, float2 &l,
+                                          uint4 &hi, uint4 &lo) {
+    const float2 mult2 = make_float2(mult, mult), off2 = make_float2(neg_m8, neg_m8);
     uint32_t hw[4], lw[4];
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
         uint32_t h2w[2], l2w[2];
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
-            const float p0 = ex2_fast(fmaf(x[4 * w + 2 * k], mult, neg_m8));
-            const float p1 = ex2_fast(fmaf(x[4 * w + 2 * k + 1], mult, neg_m8));
-            l0 += p0;
-            l1 += p1;
+            const float2 z =
+                __ffma2_rn(make_float2(x[4 * w + 2 * k], x[4 * w + 2 * k + 1]), mult2, off2);
+            const float p0 = ex2_fast(z.x);
+            const float p1 = ex2_fast(z.y);
+            l = __fadd2_rn(l, make_float2(p0, p1));
             const __half2 ph = __floats2half2_rn(p0, p1);
             const uint32_t h8 = __nv_cvt_halfraw2_to_fp8x2(ph, __NV_SATFINITE, __NV_E4M3);
             const __half2 hh = e4m3x2_to_half2(static_cast<uint16_t>(h8));
@@ -837,7 +840,8 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
             __syncwarp();
             if (lane == 0) mbar_arrive(&q_full[k]);
         }
-        float m_used = -INFINITY, l0 = 0.0f, l1 = 0.0f;
+        float m_used = -INFINITY;
+        float2 lsum = make_float2(0.0f, 0.0f);   // two partial row sums
         bool ok = true;
         int c = 0;   // key tiles processed by this query tile
         for (int j = static_cast<int>(my_lo - kt0); j <= static_cast<int>(my_hi - kt0) &&
@@ -865,8 +869,7 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
                 const bool bias_half = bias_row != nullptr && pos - kh >= 0 &&
                                        pos - kh - (C::kHalf - 1) < p.rel_extent;
                 float x[C::kHalf];
-                tmem_ld_x32(tmem + lane_base + col_s + hh * C::kHalf, x);
-                tmem_ld_x32(tmem + lane_base + col_s + hh * C::kHalf + 32, x + 32);
+                tmem_ld_x64(tmem + lane_base + col_s + hh * C::kHalf, x);
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&s_free[2 * k + hh]);
@@ -907,39 +910,24 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
                     m2 = fmax3(m2, x[e + 2], x[e + 3]);
                 }
                 mx = fmaxf(mx, m2) * mult;
-                // lazy rescale: move the reference max only when the row max
-                // grew by more than tau, so P <= 2^(8 + tau) stays below 448
+                // lazy rescale: a row must move its reference max when its
+                // max grew by more than tau (P <= 2^(8 + tau) stays below
+                // 448).  O is rescaled a whole warp at a time, so once any row
+                // of the warp needs it, every row whose max grew moves too.
                 const bool resc = mx > m_used + kRescaleTau;
-                const float m_new = resc ? mx : m_used;
-                const float alpha = (resc && m_used != -INFINITY) ? ex2_fast(m_used - m_new) : 1.0f;
-                const bool rescale_o = __any_sync(0xffffffffu, alpha != 1.0f);
-                // this P half was read by the PV of unit u - 2; rescaling O
-                // needs the PV of unit u - 1 (the other half) done as well
-                if (u >= 2 && !warp_wait_p(&o_done[2 * k + hh], ((u - 2) >> 1) & 1, fail, p.err)) {
-                    ok = false;
-                    break;
-                }
-                if (u >= 1 && rescale_o &&
-                    !warp_wait_p(&o_done[2 * k + (hh ^ 1)], ((u - 1) >> 1) & 1, fail, p.err)) {
-                    ok = false;
-                    break;
-                }
-                if (u >= 1) {
-                    tc_fence_after_sync();
-                    if (rescale_o) {
-#pragma unroll 1
-                        for (int q = 0; q < D / 32; ++q) {
-                            float o[32];
-                            const uint32_t ta = tmem + lane_base + col_o + q * 32;
-                            tmem_ld_x32(ta, o);
-#pragma unroll
-                            for (int e = 0; e < 32; ++e) o[e] *= alpha;
-                            tmem_st_x32(ta, o);
-                        }
+                const bool rescale_o = __any_sync(0xffffffffu, resc && m_used != -INFINITY);
+                const bool move = resc || (rescale_o && mx > m_used);
+                const float m_new = move ? mx : m_used;
+                const float alpha = (move && m_used != -INFINITY) ? ex2_fast(m_used - m_new) : 1.0f;
+                // this P half was read by the PV of unit u - 2
+                if (u >= 2) {
+                    if (!warp_wait_p(&o_done[2 * k + hh], ((u - 2) >> 1) & 1, fail, p.err)) {
+                        ok = false;
+                        break;
                     }
+                    tc_fence_after_sync();
                 }
-                l0 *= alpha;
-                l1 *= alpha;
+                lsum = __fmul2_rn(lsum, make_float2(alpha, alpha));
                 m_used = m_new;
                 const float neg_m8 = (m_used == -INFINITY) ? 0.0f : kPOffset - m_used;
                 uint8_t *p_hi = smem + C::kOffP + k * 2 * C::kPBytes;
@@ -947,10 +935,30 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
 #pragma unroll
                 for (int q = 0; q < C::kHalf / 16; ++q) {
                     uint4 hi, lo;
-                    p_chunk16(x + q * 16, mult, neg_m8, l0, l1, hi, lo);
+                    p_chunk16(x + q * 16, mult, neg_m8, lsum, hi, lo);
                     const uint32_t off = r * 128 + (((hh * (C::kHalf / 16) + q) ^ sw) << 4);
                     *reinterpret_cast<uint4 *>(p_hi + off) = hi;
                     *reinterpret_cast<uint4 *>(p_lo + off) = lo;
+                }
+                if (rescale_o) {
+                    // O holds the products up to unit u - 1 against the old
+                    // reference: scale it by alpha once the PV of unit u - 1
+                    // (the other half) is done, before this unit's PV is
+                    // issued.  Done after P so that the PV has had the whole
+                    // P phase to finish.
+                    if (!warp_wait_p(&o_done[2 * k + (hh ^ 1)], ((u - 1) >> 1) & 1, fail, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+#pragma unroll 1
+                    for (int q = 0; q < D / 64; ++q) {
+                        float o[64];
+                        tmem_ld_x64(tmem + lane_base + col_o + q * 64, o);
+#pragma unroll
+                        for (int e = 0; e < 64; ++e) o[e] *= alpha;
+                        tmem_st_x64(tmem + lane_base + col_o + q * 64, o);
+                    }
                 }
                 fence_proxy_async_smem();
                 tc_fence_before_sync();
@@ -963,25 +971,40 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
         // completing means every earlier MMA of this thread completed too
         if (ok && c > 0 && warp_wait_p(&o_done[2 * k + 1], (c - 1) & 1, fail, p.err)) {
             tc_fence_after_sync();
-            const float l = l0 + l1;
+            const float l = lsum.x + lsum.y;
             const float f = (l > 0.0f) ? p.v_scale / l : 0.0f;
-            uint16_t *orow = p.out + (static_cast<int64_t>(q_first) + qt * kTile + r) * p.Hq * D +
-                             static_cast<int64_t>(h) * D;
-#pragma unroll 1
-            for (int q = 0; q < D / 32; ++q) {
-                float o[32];
-                tmem_ld_x32(tmem + lane_base + col_o + q * 32, o);
-                if (row_ok) {
-                    uint32_t w[16];
+            // out = bf16(v_scale * O / l), staged through this query tile's P
+            // buffer (free: its last PV is done; 128 rows x 256 bytes, chunk
+            // c of row r at c ^ (r & 15)) so that the global stores are
+            // coalesced: each warp writes back its own 32 rows, two rows per
+            // store instruction.
+            float o[D];
+            tmem_ld_x128(tmem + lane_base + col_o, o);
+            uint8_t *stage = smem + C::kOffP + k * 2 * C::kPBytes;
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const __nv_bfloat162 v2 = __floats2bfloat162_rn(o[2 * e] * f, o[2 * e + 1] * f);
-                        w[e] = *reinterpret_cast<const uint32_t *>(&v2);
-                    }
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + q * 32);
+            for (int cch = 0; cch < D / 8; ++cch) {
+                uint32_t w[4];
 #pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+                for (int e = 0; e < 4; ++e) {
+                    const __nv_bfloat162 v2 =
+                        __floats2bfloat162_rn(o[8 * cch + 2 * e] * f, o[8 * cch + 2 * e + 1] * f);
+                    w[e] = *reinterpret_cast<const uint32_t *>(&v2);
+                }
+                *reinterpret_cast<uint4 *>(stage + r * 256 + ((cch ^ (r & 15)) << 4)) =
+                    make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            __syncwarp();
+            const int row_in_pair = lane >> 4, col = lane & 15;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int row = 32 * wq + 2 * i + row_in_pair;
+                if (row < my_rows) {
+                    const uint4 val =
+                        *reinterpret_cast<const uint4 *>(stage + row * 256 + ((col ^ (row & 15)) << 4));
+                    *reinterpret_cast<uint4 *>(p.out +
+                                               (static_cast<int64_t>(q_first) + qt * kTile + row) *
+                                                   p.Hq * D +
+                                               static_cast<int64_t>(h) * D + col * 8) = val;
                 }
             }
         }

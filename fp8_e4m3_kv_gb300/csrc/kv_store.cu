@@ -14,17 +14,22 @@ namespace {
 constexpr int kStoreThreads = 256;
 constexpr int kChunk = 16;   // elements per thread-step
 
-// 16 bf16 elements -> 16 e4m3 bytes (quantize_bf16x2: IEEE fp32 x / s,
-// clamp to +-448 keeping NaN, nearest-even saturating conversion, sign kept).
+// 16 bf16 elements -> 16 e4m3 bytes (IEEE fp32 x / s, an exact multiply for
+// a power-of-two scale; clamp to +-448 keeping NaN, nearest-even saturating
+// conversion, sign kept).  The scale's form is a template argument so that
+// only one of multiply / divide is evaluated.
+template <bool kPow2>
 __device__ __forceinline__ uint4 quantize16(const uint4 lo, const uint4 hi, const QScale &s) {
     const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
     uint32_t out[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-        out[i] = quantize_bf16x2(w[2 * i], s) | (quantize_bf16x2(w[2 * i + 1], s) << 16);
+        out[i] = quantize_bf16x2_as<kPow2>(w[2 * i], s) |
+                 (quantize_bf16x2_as<kPow2>(w[2 * i + 1], s) << 16);
     return make_uint4(out[0], out[1], out[2], out[3]);
 }
 
+template <bool kPowK, bool kPowV>
 __global__ void __launch_bounds__(kStoreThreads)
 kv_store_kernel(const uint16_t *__restrict__ k, const uint16_t *__restrict__ v, int64_t k_stride,
                 int64_t v_stride, const int64_t *__restrict__ slots, int64_t num_tokens,
@@ -51,8 +56,8 @@ kv_store_kernel(const uint16_t *__restrict__ k, const uint16_t *__restrict__ v, 
         const int32_t e = c * kChunk, h = e / head_dim, d = e - h * head_dim;
         const int64_t blk = slot / block_size, row = slot - blk * block_size;
         const int64_t dst = ((blk * num_kv_heads + h) * block_size + row) * head_dim + d;
-        *reinterpret_cast<uint4 *>(ck + dst) = quantize16(k0, k1, k_scale);
-        *reinterpret_cast<uint4 *>(cv + dst) = quantize16(v0, v1, v_scale);
+        *reinterpret_cast<uint4 *>(ck + dst) = quantize16<kPowK>(k0, k1, k_scale);
+        *reinterpret_cast<uint4 *>(cv + dst) = quantize16<kPowV>(v0, v1, v_scale);
     }
 }
 
@@ -150,10 +155,13 @@ extern "C" fp8kv_status kv_store_e4m3(const fp8kv_cache *cache, const fp8kv_bf16
     uint32_t *err = device_error_word();
     const int64_t capacity = cache->num_blocks * cache->block_size;
     const int grid = grid_for(num_tokens * (row / kChunk), sms);
-    kv_store_kernel<<<grid, kStoreThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+    const QScale ks = make_qscale(k_scale), vs = make_qscale(v_scale);
+    auto kernel = ks.pow2 ? (vs.pow2 ? kv_store_kernel<true, true> : kv_store_kernel<true, false>)
+                          : (vs.pow2 ? kv_store_kernel<false, true> : kv_store_kernel<false, false>);
+    kernel<<<grid, kStoreThreads, 0, static_cast<cudaStream_t>(stream)>>>(
         k, v, k_tok_stride, v_tok_stride, slot_mapping, num_tokens, static_cast<int32_t>(row),
-        cache->head_dim, cache->num_kv_heads, cache->block_size, capacity, cache->k, cache->v,
-        make_qscale(k_scale), make_qscale(v_scale), err);
+        cache->head_dim, cache->num_kv_heads, cache->block_size, capacity, cache->k, cache->v, ks,
+        vs, err);
     if (cudaGetLastError() != cudaSuccess) return FP8KV_ERR_LAUNCH;
     return FP8KV_OK;
 }
