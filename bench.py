@@ -49,6 +49,29 @@ def peaks():
             "source": "fallback"}
 
 
+# DRAM bytes (read + write) of one decode launch of the 64-sequence workload,
+# from the ncu capture summarised in profiles/ (decode launch list), keyed by a
+# hash of the kernel sources it was taken on: once the kernel changes, the
+# number no longer describes it and is reported as null.
+DECODE_TRAFFIC = {
+    "0f571c974ae68c0e4ce908108aa8cab780edf27c7116b404513a0d99d338bb50": 1084609024,
+}
+DECODE_SOURCES = ("fp8_e4m3_kv_gb300/csrc/attn_decode.cu", "fp8_e4m3_kv_gb300/csrc/common.cuh")
+
+
+def decode_sources_sha():
+    import hashlib
+    h = hashlib.sha256()
+    for rel in DECODE_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def decode_traffic_bytes():
+    return DECODE_TRAFFIC.get(decode_sources_sha())
+
+
 # ---------------------------------------------------------------------------
 # distributed plumbing (replicas only: no data-path collective)
 # ---------------------------------------------------------------------------
@@ -97,7 +120,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -345,7 +368,12 @@ def bench_prefill(fk, dev, steps, warmup, world, only_group=None):
     except Exception as e:  # noqa: BLE001
         return {"workload": spec.name, "unavailable": str(e)}
     ms = time_steps(step, steps, warmup, world)
+    pk = peaks()
+    fp8_peak = 2.0 * pk["bf16_tflops"]      # nominal fp8 : bf16 dense ratio of 2
     return {"workload": spec.name, "ms_per_step": ms, "tflops": flops / ms / 1e9,
+            "roofline": {"bound": "tensor", "achieved": flops / ms / 1e9, "peak": fp8_peak,
+                         "unit": "TFLOP/s", "frac": flops / ms / 1e9 / fp8_peak,
+                         "peak_source": "2 x %s bf16 burst" % pk["source"]},
             "flops_per_step": flops, "tokens": sum(q_lens)}
 
 
@@ -370,6 +398,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extra", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--settle-s", type=float, default=0.6,
+                    help="seconds of untimed steps before the timed ones, for the clock samples")
     ap.add_argument("--profile-decode", type=int, default=0, metavar="B",
                     help="profiling case: only the decode call of the 32K workload cut to B "
                          "sequences (still larger than L2), no JSON contract line")
@@ -431,8 +461,15 @@ def main():
     dev = torch.device("cuda", torch.cuda.current_device())
     pk = peaks()
     run = DecodeRun(fk, spec, dev)
-    # warm-up + timed region (clocks sampled during it)
+    # warm-up + timed region, clocks sampled during it; the untimed load
+    # before the timed steps lets the sampler see the clocks under this load
+    # even when K steps last only milliseconds
     with ClockSampler(dev.index) as clk:
+        load_until = time.time() + args.settle_s
+        while time.time() < load_until:
+            for _ in range(50):
+                run.step()
+            torch.cuda.synchronize()
         ms = time_steps(run.step, args.steps, args.warmup, world)
         # the dominant kernel's call, timed alone on its stream
         dms = time_steps(run.decode, args.steps, args.warmup, world)
@@ -445,7 +482,8 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
             "data": "synthetic", "config": cfg,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
-                         "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": None,
+                         "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
+                         "traffic": decode_traffic_bytes(),
                          "kernel": "paged_attn_fp8_decode (decode + split merge)",
                          "peak_source": pk["source"]},
             "e2e": {"value": run.step_bytes * world / e2e_ms / 1e6, "unit": "GB/s",
