@@ -158,8 +158,8 @@ __device__ __forceinline__ void load_q8(uint8_t *q8, const uint16_t *q_group, in
         uint2 packed = make_uint2(0u, 0u);
         if (g < G) {
             const uint4 w = *reinterpret_cast<const uint4 *>(q_group + static_cast<int64_t>(g) * D + d);
-            packed.x = quantize_bf16x2_as<kPow2>(w.x, s) | (quantize_bf16x2_as<kPow2>(w.y, s) << 16);
-            packed.y = quantize_bf16x2_as<kPow2>(w.z, s) | (quantize_bf16x2_as<kPow2>(w.w, s) << 16);
+            packed.x = quantize_q_bf16x2<kPow2>(w.x, s) | (quantize_q_bf16x2<kPow2>(w.y, s) << 16);
+            packed.y = quantize_q_bf16x2<kPow2>(w.z, s) | (quantize_q_bf16x2<kPow2>(w.w, s) << 16);
         }
         *reinterpret_cast<uint2 *>(q8 + (d / 128) * (kNPad * 128) + sw128_offset(g, d % 128)) =
             packed;

@@ -479,8 +479,8 @@ __device__ __forceinline__ void quantize_q16(const uint4 (&v)[16], uint2 (&o)[16
                                              const QScale &s) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-        o[i].x = quantize_bf16x2_as<kPow2>(v[i].x, s) | (quantize_bf16x2_as<kPow2>(v[i].y, s) << 16);
-        o[i].y = quantize_bf16x2_as<kPow2>(v[i].z, s) | (quantize_bf16x2_as<kPow2>(v[i].w, s) << 16);
+        o[i].x = quantize_q_bf16x2<kPow2>(v[i].x, s) | (quantize_q_bf16x2<kPow2>(v[i].y, s) << 16);
+        o[i].y = quantize_q_bf16x2<kPow2>(v[i].z, s) | (quantize_q_bf16x2<kPow2>(v[i].w, s) << 16);
     }
 }
 

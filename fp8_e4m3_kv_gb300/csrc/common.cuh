@@ -101,6 +101,18 @@ __device__ __forceinline__ uint32_t quantize_bf16x2(uint32_t word, const QScale 
 // scale is a power of two and scale.inv its exact reciprocal), for loops
 // where the compiler would otherwise evaluate both the multiply and the
 // division for every element.
+// Query quantization inside the attention kernels: the same quotient and
+// conversion without the NaN sign fix-up.  Q8 is never stored, and a NaN
+// query gives NaN scores whichever NaN code it gets, so -NaN need not stay
+// 0xFF here (-0 keeps its sign through the multiply or divide).
+template <bool kPow2>
+__device__ __forceinline__ uint32_t quantize_q_bf16x2(uint32_t word, const QScale &scale) {
+    const float2 v = make_float2(__uint_as_float(word << 16), __uint_as_float(word & 0xFFFF0000u));
+    const float2 q = kPow2 ? __fmul2_rn(v, make_float2(scale.inv, scale.inv))
+                           : make_float2(__fdiv_rn(v.x, scale.scale), __fdiv_rn(v.y, scale.scale));
+    return static_cast<uint32_t>(f32x2_to_e4m3x2(q.x, q.y));
+}
+
 template <bool kPow2>
 __device__ __forceinline__ uint32_t quantize_bf16x2_as(uint32_t word, const QScale &scale) {
     const float a = __uint_as_float(word << 16), b = __uint_as_float(word & 0xFFFF0000u);
