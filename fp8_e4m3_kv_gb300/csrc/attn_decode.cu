@@ -166,6 +166,12 @@ __device__ __forceinline__ void load_q8(uint8_t *q8, const uint16_t *q_group, in
     }
 }
 
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 template <int D, int GMAX>
 __global__ void __launch_bounds__(DecCfg<D>::kThreads, DecCfg<D>::kCtasPerSm)
 decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
@@ -173,7 +179,7 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
     using C = DecCfg<D>;
     constexpr int HS = C::kHS;
     constexpr int GH = GMAX / HS;                      // heads per consumer warpgroup
-    static_assert(GH * HS == GMAX && GH >= 1, "head split");
+    static_assert(GH * HS == GMAX && GH % 2 == 0, "head split: an even number of heads per warpgroup");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -463,7 +469,7 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
             __syncwarp();
             if (lane == 0) mbar_arrive(&red_bar[i & 1]);
             if (!warp_wait(&red_bar[i & 1], (i >> 1) & 1, fail, p.err)) { ok = false; break; }
-            float alpha[GH];
+            float alpha[GH], neg_m8[GH];
             uint8_t *phi = smem + C::kOffP + (i % C::kOBuf) * 2 * C::kPBytes;
             uint8_t *plo = phi + C::kPBytes;
 #pragma unroll
@@ -472,21 +478,37 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
                     fmaxf(fmaxf(rb[g], rb[16 + g]), fmaxf(rb[32 + g], rb[48 + g]));
                 const float m_new = fmaxf(m_run[g], tile_max);
                 alpha[g] = (m_new == -INFINITY) ? 1.0f : exp2f(m_run[g] - m_new);
-                float lsum = 0.0f;
+                // P = 2^(z - m + 8); with no visible key yet (m = -inf) every
+                // z is -inf and P is 0
+                neg_m8[g] = (m_new == -INFINITY) ? 0.0f : 8.0f - m_new;
+                m_run[g] = m_new;
+            }
+            // Two heads at a time: P of heads g and g + 1 for this key as a
+            // packed f16 pair, split into two e4m3 terms, hi = e4m3(P) and
+            // lo = e4m3(P - hi) (the difference is exact in f16).
+#pragma unroll
+            for (int g = 0; g < GH; g += 2) {
+                float ls0 = 0.0f, ls1 = 0.0f;
 #pragma unroll
                 for (int kb = 0; kb < C::kKB; ++kb) {
-                    const float pv = (z[kb][g] == -INFINITY) ? 0.0f : exp2f(z[kb][g] - m_new + 8.0f);
-                    // two-term e4m3 split of P: hi = e4m3(P), lo = e4m3(P - hi)
-                    const uint16_t hi2 = f32x2_to_e4m3x2(pv, 0.0f);
-                    const float hi_val = __low2float(e4m3x2_to_half2(hi2));
-                    const uint16_t lo2 = f32x2_to_e4m3x2(pv - hi_val, 0.0f);
-                    lsum += pv;
-                    const uint32_t off = kb * (kNPad * 128) + sw128_offset(gbase + g, t);
-                    phi[off] = static_cast<uint8_t>(hi2 & 0xFF);
-                    plo[off] = static_cast<uint8_t>(lo2 & 0xFF);
+                    const float p0 = ex2_approx(z[kb][g] + neg_m8[g]);
+                    const float p1 = ex2_approx(z[kb][g + 1] + neg_m8[g + 1]);
+                    ls0 += p0;
+                    ls1 += p1;
+                    const __half2 ph = __floats2half2_rn(p0, p1);
+                    const uint32_t h8 = __nv_cvt_halfraw2_to_fp8x2(ph, __NV_SATFINITE, __NV_E4M3);
+                    const __half2 hh = e4m3x2_to_half2(static_cast<uint16_t>(h8));
+                    const uint32_t l8 =
+                        __nv_cvt_halfraw2_to_fp8x2(__hsub2(ph, hh), __NV_SATFINITE, __NV_E4M3);
+                    const uint32_t off0 = kb * (kNPad * 128) + sw128_offset(gbase + g, t);
+                    const uint32_t off1 = kb * (kNPad * 128) + sw128_offset(gbase + g + 1, t);
+                    phi[off0] = static_cast<uint8_t>(h8 & 0xFF);
+                    phi[off1] = static_cast<uint8_t>((h8 >> 8) & 0xFF);
+                    plo[off0] = static_cast<uint8_t>(l8 & 0xFF);
+                    plo[off1] = static_cast<uint8_t>((l8 >> 8) & 0xFF);
                 }
-                l_part[g] = fmaf(l_part[g], alpha[g], lsum);
-                m_run[g] = m_new;
+                l_part[g] = fmaf(l_part[g], alpha[g], ls0);
+                l_part[g + 1] = fmaf(l_part[g + 1], alpha[g + 1], ls1);
             }
             // Keys past the sequence end may hold stale bytes (NaN codes
             // included); zero their V rows so that 0 * V stays 0 in the MMA.
