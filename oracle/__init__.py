@@ -76,6 +76,8 @@ def _load():
     lib.or_amax.restype = f32
     lib.or_amax.argtypes = [P, i64, P, i64, i32, i32, f32]
     lib.or_scale_from_amax.restype = ctypes.c_int
+    lib.or_band_counts.argtypes = [P, i64, P, i64, i32, f32, P, P]
+    lib.or_band_counts.restype = None
     lib.or_scale_from_amax.argtypes = [f32, ctypes.c_int, ctypes.POINTER(f32)]
     lib.or_attend_row.restype = None
     lib.or_attend_row.argtypes = [i32, P, P, P, i64, i64, i64, f64, f64, f64, f64,
@@ -157,6 +159,20 @@ def amax(x_bf16, slot_mapping=None, amax_in: float = 0.0) -> float:
     row = int(np.prod(x.shape[1:]))
     sm = None if slot_mapping is None else np.ascontiguousarray(slot_mapping, dtype=np.int64)
     return float(_load().or_amax(_ptr(x), row, _ptr(sm), T, 1, row, float(amax_in)))
+
+
+def band_counts(x_bf16, scale: float, slot_mapping=None) -> dict:
+    """Clip / flush-to-zero counters and round-trip error sum of quantizing
+    the stored values (rows of x, skipping tokens with slot < 0) at scale."""
+    x = _u16(x_bf16)
+    T = x.shape[0]
+    row = int(np.prod(x.shape[1:]))
+    sm = None if slot_mapping is None else np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    counts = np.zeros(4, dtype=np.int64)
+    err = np.zeros(1, dtype=np.float64)
+    _load().or_band_counts(_ptr(x), row, _ptr(sm), T, row, float(scale), _ptr(counts), _ptr(err))
+    return {"count": int(counts[0]), "nonzero": int(counts[1]), "clipped": int(counts[2]),
+            "flushed": int(counts[3]), "rt_err_sum": float(err[0])}
 
 
 def scale_from_amax(a: float, rule: int = 0) -> float:

@@ -190,6 +190,50 @@ float or_amax(const uint16_t *x, int64_t tok_stride, const int64_t *slot_mapping
     return m;
 }
 
+/* Band counters of quantizing the stored values at one scale [PR "Evidence
+ * document", Tier 2: exact e4m3 band counters at scale 1.0 and 3.0 over
+ * exactly the values stored at each call's slot mapping, giving the clip
+ * rate, the flush-to-zero rate and the round-trip error of its table].
+ * READING: an element is counted when it is finite; it is clipped when its
+ * quotient |x/s| is above 448 (e4m3 saturates it); it is flushed when it is
+ * not zero but its code is +-0 (it lies below the smallest e4m3 magnitude
+ * after rounding); its round-trip error is |s*dec(enc(x/s)) - x| / |x|, over
+ * the non-zero elements, clipped and flushed ones included.  The quotient
+ * and the code are those of or_quantize.
+ * Adds into counts[0..3] = (finite, non-zero, clipped, flushed) and into
+ * *err_sum. */
+void or_band_counts(const uint16_t *x, int64_t tok_stride, const int64_t *slot_mapping,
+                    int64_t num_tokens, int32_t row, float scale, int64_t *counts,
+                    double *err_sum)
+{
+    int64_t t, i;
+    for (t = 0; t < num_tokens; ++t) {
+        if (slot_mapping && slot_mapping[t] < 0)
+            continue;
+        for (i = 0; i < row; ++i) {
+            uint16_t bits = x[t * tok_stride + i];
+            float xf = bf16_to_float(bits);
+            float q;
+            uint8_t c;
+            double back;
+            if (!isfinite(xf))
+                continue;
+            counts[0] += 1;
+            if (xf == 0.0f)
+                continue;
+            counts[1] += 1;
+            q = (float)((double)xf / (double)scale);
+            if (fabsf(q) > 448.0f)
+                counts[2] += 1;
+            c = or_e4m3_encode(q);
+            if ((c & 0x7F) == 0)
+                counts[3] += 1;
+            back = or_e4m3_decode(c) * (double)scale;
+            *err_sum += fabs(back - (double)xf) / fabs((double)xf);
+        }
+    }
+}
+
 /* Scale from a measured amax.
  *  rule 0: amax/448                 [CAL "What it fixes", scale table]
  *  rule 1: ceil_to_bfloat16(amax/448), kept as fp32

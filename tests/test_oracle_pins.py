@@ -148,6 +148,66 @@ def test_round_trip_error_matches_tier2_statistic(oracle_lib):
         assert pv["rt_err_lo"] - 0.003 <= err <= pv["rt_err_hi"] + 0.002, (dist, err)
 
 
+# ----------------------------------------------------------------- band counters
+def test_band_counts_hand_cases(oracle_lib):
+    """Every band by hand at unity scale: 1000 and 450 clip (to 448), 2^-11 and
+    2^-10 flush (the latter a tie to the even code 0), 2^-9 is the smallest
+    subnormal, 1.0625 is a tie between 1 and 1.125 going to the even code 1.0;
+    zeros are counted but have no error term; Inf and NaN are not counted."""
+    vals = [1000.0, -1000.0, 448.0, 450.0, 2.0 ** -11, 2.0 ** -10, 2.0 ** -9, 1.0625, 0.0,
+            -0.0, 3.0, float("inf"), float("nan")]
+    got = oracle_lib.band_counts(bf16_bits_of(vals).reshape(1, -1), 1.0)
+    assert (got["count"], got["nonzero"], got["clipped"], got["flushed"]) == (11, 9, 3, 2)
+    want_err = 2 * (1000 - 448) / 1000 + 2 / 450 + 2 * 1.0 + 0.0625 / 1.0625
+    assert abs(got["rt_err_sum"] - want_err) < 1e-12
+    # at scale 3 nothing clips (1000/3, 450/3 < 448) and 2^-9/3 < 2^-10 flushes too
+    got3 = oracle_lib.band_counts(bf16_bits_of(vals).reshape(1, -1), 3.0)
+    assert (got3["clipped"], got3["flushed"]) == (0, 3)
+
+
+def test_band_counts_skip_unstored_tokens(oracle_lib):
+    g = torch.Generator().manual_seed(11)
+    x = workloads.bf16_bits(workloads.draw_values((50, 64), "v_t3", g, "cpu"))
+    slots = np.where(np.arange(50) % 3 == 0, -1, np.arange(50)).astype(np.int64)
+    a = oracle_lib.band_counts(x, 1.0, slot_mapping=slots)
+    b = oracle_lib.band_counts(x[slots >= 0], 1.0)
+    assert a == b
+    assert a["count"] == int((slots >= 0).sum()) * 64
+
+
+def test_band_counts_flush_band_grows_with_the_scale(oracle_lib):
+    """Values flush when |x|/s <= 2^-10, so for N(0,1) the flushed fraction is
+    ~2*phi(0)*2^-10*s, and the band at s = 3 is ~3x the band at s = 1 (the
+    pages report ~3x on real activations)."""
+    pv = pages_values()
+    g = torch.Generator().manual_seed(5)
+    x = workloads.bf16_bits(workloads.draw_values((4_000_000,), "normal", g, "cpu"))
+    f1 = oracle_lib.band_counts(x.reshape(1, -1), 1.0)["flushed"]
+    f3 = oracle_lib.band_counts(x.reshape(1, -1), 3.0)["flushed"]
+    expect1 = 4_000_000 * 2 * (1 / math.sqrt(2 * math.pi)) * 2.0 ** -10
+    assert abs(f1 - expect1) < 0.1 * expect1, (f1, expect1)
+    assert abs(f3 / f1 - pv["flush_growth_s3"]) < 0.3, f3 / f1
+
+
+def test_band_counts_clip_rate_matches_the_t3_tail(oracle_lib):
+    """The synthetic global-layer V is 17.47*t(3) (clamped to +-1272): at unity
+    scale it clips where |t| > 448/17.47, the two-sided t(3) tail, which is
+    of the order the pages measure (1.3e-4 pooled); at scale 3 nothing clips."""
+    stats = pytest.importorskip("scipy.stats")
+    pv = pages_values()
+    g = torch.Generator().manual_seed(9)
+    n = 4_000_000
+    x = workloads.bf16_bits(workloads.draw_values((n,), "v_t3", g, "cpu")).reshape(1, -1)
+    c1 = oracle_lib.band_counts(x, 1.0)
+    tail = 2 * stats.t.sf(448.0 / workloads.V_T3_SCALE, 3)
+    assert abs(c1["clipped"] / n - tail) < 0.15 * tail, (c1["clipped"] / n, tail)
+    assert pv["v_clip_rate_s1_global"] / 2.5 < c1["clipped"] / n < pv["v_clip_rate_s1_global"] * 2.5
+    c3 = oracle_lib.band_counts(x, pv["v_no_clip_at_scale"])
+    assert c3["clipped"] == 0
+    rt = c1["rt_err_sum"] / c1["nonzero"]
+    assert pv["rt_err_lo"] - 0.003 <= rt <= pv["rt_err_hi"] + 0.003, rt
+
+
 def test_rescale_bound_constant():
     pv = pages_values()
     assert abs((math.log2(pv["e4m3_max"]) - 8) - pv["rescale_slack_bound"]) < 5e-4
