@@ -62,6 +62,7 @@ _prefill = _sig("attn_fp8_varlen_prefill", ctypes.c_int,
                 [ctypes.POINTER(CacheStruct), P, i32, P, P, P, i32, i32, i32, f32, f32, f32,
                  f32, P, i64, i32, i32, P, P, sz, P])
 _amax = _sig("kv_amax_calibrate", ctypes.c_int, [P, P, i64, i64, P, i64, i32, i32, P, P, P])
+_band_counts = _sig("kv_band_counts", ctypes.c_int, [P, i64, P, i64, i32, f32, P, P])
 _scale_from_amax = _sig("fp8kv_scale_from_amax", ctypes.c_int, [f32, i32, ctypes.POINTER(f32)])
 _cache_bytes = _sig("fp8kv_cache_bytes", sz, [i64, i32, i32, i32])
 _device_error = _sig("fp8kv_device_error", ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), i32])
@@ -70,6 +71,7 @@ _status_string = _sig("fp8kv_status_string", ctypes.c_char_p, [ctypes.c_int])
 EXPORTED = ("kv_store_e4m3", "paged_attn_fp8_decode", "paged_attn_fp8_decode_ex",
             "paged_attn_fp8_decode_noalloc",
             "fp8kv_decode_workspace_size", "attn_fp8_varlen_prefill", "kv_amax_calibrate",
+            "kv_band_counts",
             "fp8kv_scale_from_amax", "fp8kv_cache_bytes", "fp8kv_device_error",
             "fp8kv_status_string")
 
@@ -186,6 +188,36 @@ def kv_amax_calibrate(k: Optional[torch.Tensor], v: Optional[torch.Tensor],
         _need(slot_mapping, torch.int64, "slot_mapping")
     _check(_amax(_ptr(k), _ptr(v), ks, vs, _ptr(slot_mapping), ref.shape[0], H, D, _ptr(amax_k),
                  _ptr(amax_v), _stream(stream)), "kv_amax_calibrate")
+
+
+BAND_COUNTS_BYTES = 40   # fp8kv_band_counts: four uint64 counters and a double
+
+
+def kv_band_counts(x: torch.Tensor, scale: float, slot_mapping: Optional[torch.Tensor] = None,
+                   counts: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Adds the clip / flush-to-zero counters and the round-trip error sum of
+    quantizing the stored rows of x ([T][H][D] or [T][H*D] bf16) at `scale`
+    into `counts` (a zeroed device uint8 tensor of BAND_COUNTS_BYTES when
+    None) and returns it; read it with band_counts_dict."""
+    row = int(x.shape[1] * (x.shape[2] if x.dim() == 3 else 1))
+    stride = _rows(x, "x", row)
+    if counts is None:
+        counts = torch.zeros(BAND_COUNTS_BYTES, dtype=torch.uint8, device=x.device)
+    _need(counts, torch.uint8, "counts", x.device)
+    if counts.numel() < BAND_COUNTS_BYTES or not counts.is_contiguous():
+        raise ValueError("counts must be a contiguous uint8 tensor of %d bytes" % BAND_COUNTS_BYTES)
+    if slot_mapping is not None:
+        _need(slot_mapping, torch.int64, "slot_mapping", x.device)
+    _check(_band_counts(_ptr(x), stride, _ptr(slot_mapping), x.shape[0], row, float(scale),
+                        _ptr(counts), _stream(stream)), "kv_band_counts")
+    return counts
+
+
+def band_counts_dict(counts: torch.Tensor) -> dict:
+    """The fields of a fp8kv_band_counts tensor (copies it to the host)."""
+    import struct
+    c, nz, clip, flush, err = struct.unpack("<4Qd", bytes(counts[:BAND_COUNTS_BYTES].cpu().numpy()))
+    return {"count": c, "nonzero": nz, "clipped": clip, "flushed": flush, "rt_err_sum": err}
 
 
 def scale_from_amax(amax: float, rule: int = 0) -> float:
@@ -307,7 +339,8 @@ def device_error(clear: bool = True) -> int:
     return int(w.value)
 
 
-__all__ = ["KVCache", "Fp8KVError", "kv_store_e4m3", "kv_amax_calibrate", "scale_from_amax",
+__all__ = ["KVCache", "Fp8KVError", "kv_store_e4m3", "kv_amax_calibrate", "kv_band_counts",
+           "band_counts_dict", "BAND_COUNTS_BYTES", "scale_from_amax",
            "paged_attn_fp8_decode", "paged_attn_fp8_decode_noalloc", "attn_fp8_varlen_prefill",
            "decode_workspace_size",
            "cache_bytes", "device_error", "status_string", "LIB_PATH", "EXPORTED"]

@@ -125,6 +125,81 @@ int grid_for(int64_t work_items, int num_sms) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Band counters of one stream at one scale: the quotient and code of
+// quantize16, then per element the finite / non-zero / clipped / flushed
+// counts and the relative round-trip error (summed in fp32 over a thread's
+// 16 elements, then in fp64).  One 64-bit atomic per counter and block.
+template <bool kPow2>
+__global__ void __launch_bounds__(kStoreThreads)
+kv_band_kernel(const uint16_t *__restrict__ x, int64_t stride, const int64_t *__restrict__ slots,
+               int64_t num_tokens, int32_t row_elems, const QScale s, fp8kv_band_counts *out) {
+    __shared__ unsigned long long red_n[4][kStoreThreads / 32];
+    __shared__ double red_e[kStoreThreads / 32];
+    const int32_t chunks = row_elems / kChunk;
+    const int64_t total = num_tokens * chunks;
+    unsigned long long n_fin = 0, n_nz = 0, n_clip = 0, n_flush = 0;
+    double err = 0.0;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t t = i / chunks;
+        const int32_t c = static_cast<int32_t>(i - t * chunks);
+        if (slots && __ldg(slots + t) < 0) continue;
+        const uint4 *p = reinterpret_cast<const uint4 *>(x + t * stride + c * kChunk);
+        const uint4 lo = __ldcs(p), hi = __ldcs(p + 1);
+        const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+        float e16 = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const uint32_t bits = (w[k >> 1] >> (16 * (k & 1))) & 0xFFFFu;
+            if ((bits & 0x7F80u) == 0x7F80u) continue;   // NaN, +-Inf
+            ++n_fin;
+            const float xf = __uint_as_float(bits << 16);
+            if (xf == 0.0f) continue;
+            ++n_nz;
+            const float q = kPow2 ? xf * s.inv : __fdiv_rn(xf, s.scale);
+            n_clip += fabsf(q) > kE4M3Max;
+            const uint16_t code = f32x2_to_e4m3x2(q, 0.0f) & 0xFFu;
+            n_flush += (code & 0x7Fu) == 0;
+            const float back = __low2float(e4m3x2_to_half2(code)) * s.scale;
+            e16 += fabsf(back - xf) / fabsf(xf);
+        }
+        err += static_cast<double>(e16);
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        n_fin += __shfl_xor_sync(0xffffffffu, n_fin, o);
+        n_nz += __shfl_xor_sync(0xffffffffu, n_nz, o);
+        n_clip += __shfl_xor_sync(0xffffffffu, n_clip, o);
+        n_flush += __shfl_xor_sync(0xffffffffu, n_flush, o);
+        err += __shfl_xor_sync(0xffffffffu, err, o);
+    }
+    if (lane == 0) {
+        red_n[0][warp] = n_fin;
+        red_n[1][warp] = n_nz;
+        red_n[2][warp] = n_clip;
+        red_n[3][warp] = n_flush;
+        red_e[warp] = err;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned long long a[4] = {0, 0, 0, 0};
+        double e = 0.0;
+        for (int w2 = 0; w2 < kStoreThreads / 32; ++w2) {
+#pragma unroll
+            for (int f = 0; f < 4; ++f) a[f] += red_n[f][w2];
+            e += red_e[w2];
+        }
+        if (a[0]) {
+            atomicAdd(&out->count, a[0]);
+            atomicAdd(&out->nonzero, a[1]);
+            atomicAdd(&out->clipped, a[2]);
+            atomicAdd(&out->flushed, a[3]);
+            atomicAdd(&out->rt_err_sum, e);
+        }
+    }
+}
+
 }  // namespace
 }  // namespace fp8kv
 
@@ -187,6 +262,29 @@ extern "C" fp8kv_status kv_amax_calibrate(const fp8kv_bf16 *k, const fp8kv_bf16 
     kv_amax_kernel<<<grid, kStoreThreads, 0, static_cast<cudaStream_t>(stream)>>>(
         k, v, k_tok_stride, v_tok_stride, slot_mapping, num_tokens, static_cast<int32_t>(row),
         amax_k_inout, amax_v_inout);
+    if (cudaGetLastError() != cudaSuccess) return FP8KV_ERR_LAUNCH;
+    return FP8KV_OK;
+}
+
+extern "C" fp8kv_status kv_band_counts(const fp8kv_bf16 *x, int64_t tok_stride,
+                                       const int64_t *slot_mapping, int64_t num_tokens,
+                                       int32_t row_elems, float scale, fp8kv_band_counts *counts,
+                                       void *stream) {
+    if (num_tokens < 0 || row_elems <= 0) return FP8KV_ERR_ARG;
+    if (!scale_ok(scale)) return FP8KV_ERR_SCALE;
+    if (row_elems % kChunk != 0 || row_elems > (1 << 30)) return FP8KV_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return FP8KV_OK;
+    if (!x || !counts || tok_stride < row_elems || (tok_stride % 8) || !aligned16(x) ||
+        (reinterpret_cast<uintptr_t>(counts) & 7))
+        return FP8KV_ERR_ARG;
+    int sms = 0;
+    fp8kv_status st = check_device(&sms);
+    if (st != FP8KV_OK) return st;
+    const int grid = grid_for(num_tokens * (row_elems / kChunk), sms);
+    const QScale qs = make_qscale(scale);
+    auto kernel = qs.pow2 ? kv_band_kernel<true> : kv_band_kernel<false>;
+    kernel<<<grid, kStoreThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        x, tok_stride, slot_mapping, num_tokens, row_elems, qs, counts);
     if (cudaGetLastError() != cudaSuccess) return FP8KV_ERR_LAUNCH;
     return FP8KV_OK;
 }

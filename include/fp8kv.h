@@ -218,6 +218,43 @@ fp8kv_status attn_fp8_varlen_prefill(const fp8kv_cache *cache, const fp8kv_bf16 
                                      void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * kv_band_counts -- clip and flush-to-zero counters and the round-trip error
+ * of quantizing the stored values at one scale: the KV value-range
+ * instrument of vLLM PR 54705 (evidence document, Tier 2: exact e4m3 band
+ * counters at scale 1.0 and 3.0 over exactly the values at each call's slot
+ * mapping).  For every finite element x of a stored token:
+ *   count    += 1
+ *   nonzero  += x != 0
+ *   clipped  += |x / scale| > 448   (the store saturates it to +-448)
+ *   flushed  += x != 0 and its e4m3 code is +-0
+ *   rt_err_sum += |scale * dec(enc(x / scale)) - x| / |x|   (x != 0)
+ * The quotient x / scale and the code are bit-identical to kv_store_e4m3's,
+ * so the counts are exact; rt_err_sum is added in parallel, so its last bits
+ * depend on the order of the additions.
+ * x:             device bf16 [num_tokens] rows of row_elems elements (a
+ *                multiple of 16), tok_stride elements apart (a multiple of
+ *                8, >= row_elems), 16-byte aligned; NaN and +-Inf are not
+ *                counted.
+ * slot_mapping:  NULL (every token counts) or device int64 [num_tokens];
+ *                tokens with slot < 0 are skipped.
+ * scale:         finite and > 0, else FP8KV_ERR_SCALE.
+ * counts:        device fp8kv_band_counts, 8-byte aligned; added into, so
+ *                zero it before the first call of a measurement.
+ * Runs asynchronously on `stream`.
+ */
+typedef struct {
+    unsigned long long count;
+    unsigned long long nonzero;
+    unsigned long long clipped;
+    unsigned long long flushed;
+    double rt_err_sum;
+} fp8kv_band_counts;
+
+fp8kv_status kv_band_counts(const fp8kv_bf16 *x, int64_t tok_stride, const int64_t *slot_mapping,
+                            int64_t num_tokens, int32_t row_elems, float scale,
+                            fp8kv_band_counts *counts, void *stream);
+
+/*
  * kv_amax_calibrate -- running max |x| over the tokens that are stored
  * (model card "Qwen3.8-27B-FP8-KVcal", "What it fixes": amax at the
  * cache-write point; vLLM PR 54705 Tier 2: only the values at each call's

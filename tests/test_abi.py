@@ -37,7 +37,7 @@ def test_header_declares_the_entry_points():
     for n in ("kv_store_e4m3", "paged_attn_fp8_decode", "attn_fp8_varlen_prefill",
               "kv_amax_calibrate", "fp8kv_scale_from_amax", "fp8kv_decode_workspace_size",
               "fp8kv_status_string", "fp8kv_device_error", "fp8kv_cache_bytes",
-              "paged_attn_fp8_decode_ex"):
+              "paged_attn_fp8_decode_ex", "kv_band_counts"):
         assert n in names, n
 
 
@@ -140,3 +140,20 @@ def test_workspace_size_is_host_only_with_explicit_splits(lib):
     n2 = lib.decode_workspace_size(1, 4, 1, 256, 64, 16, 0, 256)
     assert n2 % per_slot(1, 4, 256) == 0 and (n2 // per_slot(1, 4, 256)) % 4 == 0
     assert lib.decode_workspace_size(1, 4, 1, 64, 4, 16, 0, 128) == 0
+
+
+def test_band_counts_rejects_bad_arguments_on_host(lib):
+    f = _c(lib).kv_band_counts
+    # (x, stride, slots, tokens, row, scale, counts, stream); the pointers are
+    # fakes, and every case below is rejected (or is empty) before any CUDA call
+    for bad in (0.0, -1.0, float("nan"), float("inf")):
+        assert f(16, 128, None, 4, 128, bad, 16, None) == lib.ERR_SCALE
+    assert f(16, 128, None, -1, 128, 1.0, 16, None) == lib.ERR_ARG
+    assert f(16, 128, None, 4, 0, 1.0, 16, None) == lib.ERR_ARG
+    assert f(16, 128, None, 4, 100, 1.0, 16, None) == lib.ERR_UNSUPPORTED   # row % 16
+    assert f(16, 128, None, 0, 128, 1.0, None, None) == lib.OK               # nothing to do
+    assert f(None, 128, None, 4, 128, 1.0, 16, None) == lib.ERR_ARG
+    assert f(16, 64, None, 4, 128, 1.0, 16, None) == lib.ERR_ARG             # stride < row
+    assert f(8, 128, None, 4, 128, 1.0, 16, None) == lib.ERR_ARG             # x not 16-byte aligned
+    assert f(16, 128, None, 4, 128, 1.0, 12, None) == lib.ERR_ARG            # counts not 8-byte aligned
+    assert f(16, 128, None, 4, 128, 1.0, None, None) == lib.ERR_ARG
