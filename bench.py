@@ -3,11 +3,14 @@
 
 One step = one decode step of the 64-sequence full-attention workload
 (64 seqs, 32 q / 4 KV heads, head_dim 128, contexts U[1K, 32K], block 16,
-bf16 relative bias of extent 1,024):
-  kv_amax_calibrate on the step's new K/V tokens   (calibration pass)
-  kv_store_e4m3 of the new tokens                   (quant-on-store)
-  paged_attn_fp8_decode over the whole cache        (fp8 attention)
-`value` is the step's algorithmic HBM bytes / step time (GB/s).  The other
+bf16 relative bias of extent 1,024), made by paged_attn_fp8_decode_store in
+two launches:
+  the running amax over the step's new K/V tokens  (calibration pass)
+  the store of the new tokens into the cache        (quant-on-store)
+  fp8 attention over the whole cache + split merge  (fp8 attention)
+`value` is the step's algorithmic HBM bytes / step time (GB/s); the same step
+as separate calls (kv_amax_calibrate, kv_store_e4m3, paged_attn_fp8_decode)
+is timed beside it under "separate_calls".  The other
 workloads (varlen prefill, 128K calibrated decode, 1M decode) are measured the
 same way and reported under "extra".
 
@@ -206,20 +209,28 @@ class DecodeRun:
         self.store_bytes = nt * 2 * (2 + 1)     # read bf16 K and V, write e4m3 K and V
         self.amax_bytes = nt * 2 * 2
         self.step_bytes = self.decode_bytes + self.store_bytes + self.amax_bytes
-        self.launches_per_step = 4              # amax, store, decode, merge
+        self.launches_per_step = 2              # fused store + amax + decode, merge
 
-    def step(self, q=None, k_new=None, v_new=None, slot_new=None, seq_lens=None, out=None):
+    def step(self, q=None, k_new=None, v_new=None, seq_lens=None, out=None):
+        """One decode step in one call: store each sequence's new token, raise
+        the running amax over it, attend."""
         fk, kv = self.fk, self.kv
         sq, sk, sv = self.scales
-        q = self.q if q is None else q
-        k_new = self.k_new if k_new is None else k_new
-        v_new = self.v_new if v_new is None else v_new
-        slot_new = self.slot_new if slot_new is None else slot_new
-        seq_lens = kv.seq_lens if seq_lens is None else seq_lens
-        out = self.out if out is None else out
-        fk.kv_amax_calibrate(k_new, v_new, self.step_amax[0:1], self.step_amax[1:2], slot_new)
-        fk.kv_store_e4m3(self.cache, k_new, v_new, slot_new, sk, sv)
-        return self.decode(q, seq_lens, out)
+        return fk.paged_attn_fp8_decode_store(
+            self.cache, self.q if q is None else q, self.k_new if k_new is None else k_new,
+            self.v_new if v_new is None else v_new, kv.block_table,
+            kv.seq_lens if seq_lens is None else seq_lens, sq, sk, sv, rel_bias=self.rel,
+            window=self.spec.window, amax_k=self.step_amax[0:1], amax_v=self.step_amax[1:2],
+            out=self.out if out is None else out, workspace=self.ws)
+
+    def step_separate(self):
+        """The same step as three calls (amax, store, decode): four launches."""
+        fk = self.fk
+        sq, sk, sv = self.scales
+        fk.kv_amax_calibrate(self.k_new, self.v_new, self.step_amax[0:1], self.step_amax[1:2],
+                             self.slot_new)
+        fk.kv_store_e4m3(self.cache, self.k_new, self.v_new, self.slot_new, sk, sv)
+        return self.decode()
 
     def decode(self, q=None, seq_lens=None, out=None):
         sq, sk, sv = self.scales
@@ -251,11 +262,10 @@ def time_steps(fn, steps, warmup, world):
 
 def e2e_decode(run, steps, warmup, world):
     """Same step through the public API from pinned host buffers: per step,
-    copy q / new K / new V / slots / lengths to the device, run, read back out."""
+    copy q / new K / new V / lengths to the device, run, read back out."""
     host = {
         "q": run.q.cpu().pin_memory(), "k_new": run.k_new.cpu().pin_memory(),
-        "v_new": run.v_new.cpu().pin_memory(), "slot_new": run.slot_new.cpu().pin_memory(),
-        "seq_lens": run.kv.seq_lens.cpu().pin_memory()}
+        "v_new": run.v_new.cpu().pin_memory(), "seq_lens": run.kv.seq_lens.cpu().pin_memory()}
     dev = {k: torch.empty_like(v, device=run.dev) for k, v in host.items()}
     out_h = torch.empty(run.out.shape, dtype=run.out.dtype).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in host.values())
@@ -473,6 +483,8 @@ def main():
         ms = time_steps(run.step, args.steps, args.warmup, world)
         # the dominant kernel's call, timed alone on its stream
         dms = time_steps(run.decode, args.steps, args.warmup, world)
+        # the same step as separate calls, for comparison
+        sep_ms = time_steps(run.step_separate, args.steps, args.warmup, world)
     clocks = clk.summary()
     value = run.step_bytes * world / ms / 1e6          # GB/s over all ranks
     achieved = run.decode_bytes / dms / 1e6
@@ -490,6 +502,8 @@ def main():
                     "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": run.launches_per_step * args.steps,
+            "separate_calls": {"ms_per_step": sep_ms, "value": run.step_bytes * world / sep_ms / 1e6,
+                               "launches_per_step": 4},
             "clocks": clocks}
     scales = run.scales
     inp_cpu = None

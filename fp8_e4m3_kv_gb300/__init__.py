@@ -57,6 +57,9 @@ _decode = _sig("paged_attn_fp8_decode", ctypes.c_int,
 _decode_noalloc = _sig("paged_attn_fp8_decode_noalloc", ctypes.c_int,
                        [ctypes.POINTER(CacheStruct), P, i32, P, i32, P, i32, f32, f32, f32, f32,
                         P, i64, i32, i32, P, P])
+_decode_store = _sig("paged_attn_fp8_decode_store", ctypes.c_int,
+                     [ctypes.POINTER(CacheStruct), P, i32, P, P, P, i32, P, i32, f32, f32, f32,
+                      f32, P, i64, i32, i32, P, P, P, P, sz, P])
 _ws_size = _sig("fp8kv_decode_workspace_size", sz, [i32, i32, i32, i32, i32, i32, i32, i32])
 _prefill = _sig("attn_fp8_varlen_prefill", ctypes.c_int,
                 [ctypes.POINTER(CacheStruct), P, i32, P, P, P, i32, i32, i32, f32, f32, f32,
@@ -69,7 +72,7 @@ _device_error = _sig("fp8kv_device_error", ctypes.c_int, [ctypes.POINTER(ctypes.
 _status_string = _sig("fp8kv_status_string", ctypes.c_char_p, [ctypes.c_int])
 
 EXPORTED = ("kv_store_e4m3", "paged_attn_fp8_decode", "paged_attn_fp8_decode_ex",
-            "paged_attn_fp8_decode_noalloc",
+            "paged_attn_fp8_decode_noalloc", "paged_attn_fp8_decode_store",
             "fp8kv_decode_workspace_size", "attn_fp8_varlen_prefill", "kv_amax_calibrate",
             "kv_band_counts",
             "fp8kv_scale_from_amax", "fp8kv_cache_bytes", "fp8kv_device_error",
@@ -276,6 +279,51 @@ def paged_attn_fp8_decode(cache: KVCache, q: torch.Tensor, block_table: torch.Te
     return out
 
 
+def paged_attn_fp8_decode_store(cache: KVCache, q: torch.Tensor, k_new: torch.Tensor,
+                                v_new: torch.Tensor, block_table: torch.Tensor,
+                                seq_lens: torch.Tensor, q_scale: float, k_scale: float,
+                                v_scale: float, softmax_scale: Optional[float] = None,
+                                rel_bias: Optional[torch.Tensor] = None, window: int = 0,
+                                amax_k: Optional[torch.Tensor] = None,
+                                amax_v: Optional[torch.Tensor] = None,
+                                out: Optional[torch.Tensor] = None,
+                                workspace: Optional[torch.Tensor] = None,
+                                stream=None) -> torch.Tensor:
+    """One decode step: store k_new / v_new [B][Hkv][D] (each sequence's new
+    token, at position seq_len-1) into the cache, raise amax_k / amax_v
+    (device float32 scalars, optional), and attend; returns out [B][Hq][D]."""
+    _need(q, torch.bfloat16, "q", cache.device)
+    if q.dim() != 3 or not q.is_contiguous() or q.shape[2] != cache.head_dim:
+        raise ValueError("q must be contiguous [B][Hq][D]")
+    B, Hq, D = q.shape
+    for name, t in (("k_new", k_new), ("v_new", v_new)):
+        _need(t, torch.bfloat16, name, cache.device)
+        if tuple(t.shape) != (B, cache.num_kv_heads, D) or not t.is_contiguous():
+            raise ValueError("%s must be contiguous [B][Hkv][D]" % name)
+    for a in (amax_k, amax_v):
+        if a is not None:
+            _need(a, torch.float32, "amax", cache.device)
+    _need(block_table, torch.int32, "block_table", cache.device)
+    _need(seq_lens, torch.int32, "seq_lens", cache.device)
+    if block_table.dim() != 2 or block_table.shape[0] != B or not block_table.is_contiguous():
+        raise ValueError("block_table must be contiguous [B][max_blocks]")
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    rel, bstride, E = _bias_args(rel_bias, Hq)
+    if out is None:
+        out = torch.empty_like(q)
+    mb = block_table.shape[1]
+    if workspace is None:
+        n = decode_workspace_size(B, Hq, cache.num_kv_heads, D, mb, cache.block_size, window, 0)
+        workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=cache.device)
+    _check(_decode_store(cache.c(), _ptr(q), Hq, _ptr(k_new), _ptr(v_new), _ptr(block_table), mb,
+                         _ptr(seq_lens), B, q_scale, k_scale, v_scale, softmax_scale, _ptr(rel),
+                         bstride, E, window, _ptr(amax_k), _ptr(amax_v), _ptr(out),
+                         _ptr(workspace), workspace.numel() * workspace.element_size(),
+                         _stream(stream)), "paged_attn_fp8_decode_store")
+    return out
+
+
 def paged_attn_fp8_decode_noalloc(cache: KVCache, q: torch.Tensor, block_table: torch.Tensor,
                                   seq_lens: torch.Tensor, q_scale: float, k_scale: float,
                                   v_scale: float, softmax_scale: Optional[float] = None,
@@ -341,6 +389,7 @@ def device_error(clear: bool = True) -> int:
 
 __all__ = ["KVCache", "Fp8KVError", "kv_store_e4m3", "kv_amax_calibrate", "kv_band_counts",
            "band_counts_dict", "BAND_COUNTS_BYTES", "scale_from_amax",
-           "paged_attn_fp8_decode", "paged_attn_fp8_decode_noalloc", "attn_fp8_varlen_prefill",
+           "paged_attn_fp8_decode", "paged_attn_fp8_decode_noalloc", "paged_attn_fp8_decode_store",
+           "attn_fp8_varlen_prefill",
            "decode_workspace_size",
            "cache_bytes", "device_error", "status_string", "LIB_PATH", "EXPORTED"]

@@ -116,6 +116,18 @@ struct DecodeParams {
     int32_t num_slots;      // partial slots per (sequence, head) = splits
     QScale q_scale;
     float score_log2;       // softmax_scale * q_scale * k_scale * log2(e)
+    // fused store of the step's new token (k_new == nullptr: none): row
+    // [b][kv head][D] of k_new / v_new goes to the cache slot of position
+    // seq_len - 1, quantized exactly as kv_store_e4m3 does
+    const uint16_t *k_new;
+    const uint16_t *v_new;
+    uint8_t *cache_k;
+    uint8_t *cache_v;
+    float *amax_k;          // nullable: running max |k_new|
+    float *amax_v;
+    int32_t num_kv_heads;
+    QScale k_scale;
+    QScale v_scale;
 };
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -144,6 +156,33 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, CtaFai
                                           uint32_t *err) {
     const bool ok = mbar_wait(bar, parity, fail, err);
     return __all_sync(0xffffffffu, ok);
+}
+
+// Eight bf16 values -> eight e4m3 bytes, as the store quantizes them (the
+// multiply and the divide give the same IEEE quotient for a power-of-two
+// scale, so either branch is bit-exact).
+__device__ __forceinline__ uint2 store_quantize8(const uint4 w, const QScale &s) {
+    uint2 r;
+    if (s.pow2) {
+        r.x = quantize_bf16x2_as<true>(w.x, s) | (quantize_bf16x2_as<true>(w.y, s) << 16);
+        r.y = quantize_bf16x2_as<true>(w.z, s) | (quantize_bf16x2_as<true>(w.w, s) << 16);
+    } else {
+        r.x = quantize_bf16x2_as<false>(w.x, s) | (quantize_bf16x2_as<false>(w.y, s) << 16);
+        r.y = quantize_bf16x2_as<false>(w.z, s) | (quantize_bf16x2_as<false>(w.w, s) << 16);
+    }
+    return r;
+}
+
+__device__ __forceinline__ float absmax8(const uint4 w) {
+    // fmaxf ignores NaN operands, so NaN elements never win
+    const uint32_t a[4] = {w.x, w.y, w.z, w.w};
+    float m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        m = fmaxf(m, fabsf(__uint_as_float(a[i] << 16)));
+        m = fmaxf(m, fabsf(__uint_as_float(a[i] & 0xFFFF0000u)));
+    }
+    return m;
 }
 
 // Q8 = e4m3(q / q_scale) for one KV head's group of query heads (rows >= G
@@ -246,6 +285,31 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
         fence_mbar_init();
     }
     if (warp == C::kMmaWarp) tmem_alloc(tmem_slot, C::kTmemCols);
+    if (p.k_new != nullptr && len > 0 && t0 + ntiles == t_end && threadIdx.x < D / 8) {
+        // Fused store: this CTA reads the sequence's last tile, so it writes
+        // the step's new token (position len - 1) for its KV head first; the
+        // proxy fence orders these generic writes before the tile's TMA copy.
+        const int64_t lb = (len - 1) / p.block_size;
+        const int32_t id = lb < p.max_blocks
+                               ? __ldg(p.block_table + static_cast<int64_t>(b) * p.max_blocks + lb)
+                               : -1;
+        if (id >= 0 && id < p.num_blocks) {
+            const int d = threadIdx.x * 8;
+            const int64_t src = (static_cast<int64_t>(b) * p.num_kv_heads + kvh) * D + d;
+            const int64_t dst = ((static_cast<int64_t>(id) * p.num_kv_heads + kvh) * p.block_size +
+                                 (len - 1) % p.block_size) * D + d;
+            const uint4 kw = *reinterpret_cast<const uint4 *>(p.k_new + src);
+            const uint4 vw = *reinterpret_cast<const uint4 *>(p.v_new + src);
+            *reinterpret_cast<uint2 *>(p.cache_k + dst) = store_quantize8(kw, p.k_scale);
+            *reinterpret_cast<uint2 *>(p.cache_v + dst) = store_quantize8(vw, p.v_scale);
+            // non-negative floats order like their bit patterns
+            if (p.amax_k) atomicMax(reinterpret_cast<unsigned int *>(p.amax_k), __float_as_uint(absmax8(kw)));
+            if (p.amax_v) atomicMax(reinterpret_cast<unsigned int *>(p.amax_v), __float_as_uint(absmax8(vw)));
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+        } else if (threadIdx.x == 0) {
+            atomicOr(p.err, FP8KV_DEVERR_BAD_BLOCK);
+        }
+    }
     if (warp < 4 * HS) {
         // Q8 = e4m3(q / q_scale) for the group's heads, rows >= G zero;
         // 128-byte swizzled, K-major (row = head, D bytes per row).
@@ -732,12 +796,22 @@ extern "C" size_t fp8kv_decode_workspace_size(int32_t num_seqs, int32_t num_q_he
     return workspace_bytes_for(num_seqs, num_q_heads, head_dim, slots_for(head_dim, plan.num_splits));
 }
 
-extern "C" fp8kv_status paged_attn_fp8_decode_ex(
-    const fp8kv_cache *cache, const fp8kv_bf16 *q, int32_t num_q_heads, const int32_t *block_table,
-    int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t num_seqs, float q_scale,
-    float k_scale, float v_scale, float softmax_scale, const fp8kv_bf16 *rel_bias,
-    int64_t bias_tok_stride, int32_t rel_extent, int32_t window, fp8kv_bf16 *out, void *workspace,
-    size_t workspace_bytes, int32_t split_tokens, void *stream) {
+namespace {
+// The step's new tokens, stored by the decode launch itself.
+struct FusedStore {
+    const fp8kv_bf16 *k_new;
+    const fp8kv_bf16 *v_new;
+    float *amax_k;
+    float *amax_v;
+};
+
+fp8kv_status decode_impl(const fp8kv_cache *cache, const fp8kv_bf16 *q, int32_t num_q_heads,
+                         const int32_t *block_table, int32_t max_blocks_per_seq,
+                         const int32_t *seq_lens, int32_t num_seqs, float q_scale, float k_scale,
+                         float v_scale, float softmax_scale, const fp8kv_bf16 *rel_bias,
+                         int64_t bias_tok_stride, int32_t rel_extent, int32_t window,
+                         fp8kv_bf16 *out, void *workspace, size_t workspace_bytes,
+                         int32_t split_tokens, const FusedStore *fs, void *stream) {
     if (!cache || num_seqs < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || window < 0 ||
         split_tokens < 0)
         return FP8KV_ERR_ARG;
@@ -753,6 +827,11 @@ extern "C" fp8kv_status paged_attn_fp8_decode_ex(
     if (split_tokens % (D == 128 ? DecCfg<128>::kKeys : DecCfg<256>::kKeys)) return FP8KV_ERR_ARG;
     if (num_seqs == 0) return FP8KV_OK;
     if (!q || !block_table || !seq_lens || !out || !cache->k || !cache->v) return FP8KV_ERR_ARG;
+    if (fs && (!fs->k_new || !fs->v_new || (reinterpret_cast<uintptr_t>(fs->k_new) & 15) ||
+               (reinterpret_cast<uintptr_t>(fs->v_new) & 15) ||
+               (reinterpret_cast<uintptr_t>(fs->amax_k) & 3) ||
+               (reinterpret_cast<uintptr_t>(fs->amax_v) & 3)))
+        return FP8KV_ERR_ARG;
     if ((reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(cache->k) & 15) ||
         (reinterpret_cast<uintptr_t>(cache->v) & 15) || (reinterpret_cast<uintptr_t>(out) & 1))
         return FP8KV_ERR_ARG;
@@ -792,6 +871,15 @@ extern "C" fp8kv_status paged_attn_fp8_decode_ex(
     p.q_scale = make_qscale(q_scale);
     p.score_log2 = static_cast<float>(static_cast<double>(softmax_scale) * q_scale * k_scale *
                                       1.4426950408889634);
+    p.k_new = fs ? fs->k_new : nullptr;
+    p.v_new = fs ? fs->v_new : nullptr;
+    p.cache_k = cache->k;
+    p.cache_v = cache->v;
+    p.amax_k = fs ? fs->amax_k : nullptr;
+    p.amax_v = fs ? fs->amax_v : nullptr;
+    p.num_kv_heads = Hkv;
+    p.k_scale = make_qscale(k_scale);
+    p.v_scale = make_qscale(v_scale);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (D == 128)
         st = G <= 8 ? launch_decode<128, 8>(km, vm, p, Hkv, num_seqs, s)
@@ -808,6 +896,33 @@ extern "C" fp8kv_status paged_attn_fp8_decode_ex(
             p.part_o, p.part_ml, out, num_q_heads, slots, v_scale);
     if (cudaGetLastError() != cudaSuccess) return FP8KV_ERR_LAUNCH;
     return FP8KV_OK;
+}
+}  // namespace
+
+extern "C" fp8kv_status paged_attn_fp8_decode_ex(
+    const fp8kv_cache *cache, const fp8kv_bf16 *q, int32_t num_q_heads, const int32_t *block_table,
+    int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t num_seqs, float q_scale,
+    float k_scale, float v_scale, float softmax_scale, const fp8kv_bf16 *rel_bias,
+    int64_t bias_tok_stride, int32_t rel_extent, int32_t window, fp8kv_bf16 *out, void *workspace,
+    size_t workspace_bytes, int32_t split_tokens, void *stream) {
+    return decode_impl(cache, q, num_q_heads, block_table, max_blocks_per_seq, seq_lens, num_seqs,
+                       q_scale, k_scale, v_scale, softmax_scale, rel_bias, bias_tok_stride,
+                       rel_extent, window, out, workspace, workspace_bytes, split_tokens, nullptr,
+                       stream);
+}
+
+extern "C" fp8kv_status paged_attn_fp8_decode_store(
+    const fp8kv_cache *cache, const fp8kv_bf16 *q, int32_t num_q_heads, const fp8kv_bf16 *k_new,
+    const fp8kv_bf16 *v_new, const int32_t *block_table, int32_t max_blocks_per_seq,
+    const int32_t *seq_lens, int32_t num_seqs, float q_scale, float k_scale, float v_scale,
+    float softmax_scale, const fp8kv_bf16 *rel_bias, int64_t bias_tok_stride, int32_t rel_extent,
+    int32_t window, float *amax_k_inout, float *amax_v_inout, fp8kv_bf16 *out, void *workspace,
+    size_t workspace_bytes, void *stream) {
+    if (num_seqs > 0 && (!k_new || !v_new)) return FP8KV_ERR_ARG;
+    const FusedStore fs{k_new, v_new, amax_k_inout, amax_v_inout};
+    return decode_impl(cache, q, num_q_heads, block_table, max_blocks_per_seq, seq_lens, num_seqs,
+                       q_scale, k_scale, v_scale, softmax_scale, rel_bias, bias_tok_stride,
+                       rel_extent, window, out, workspace, workspace_bytes, 0, &fs, stream);
 }
 
 extern "C" fp8kv_status paged_attn_fp8_decode(

@@ -149,6 +149,40 @@ fp8kv_status paged_attn_fp8_decode_ex(const fp8kv_cache *cache, const fp8kv_bf16
                                       int32_t split_tokens, void *stream);
 
 /*
+ * paged_attn_fp8_decode_store -- one decode step in one call: quantize and
+ * write each sequence's new token into the cache (as kv_store_e4m3 does),
+ * optionally raise the running amax over it (as kv_amax_calibrate does), and
+ * attend (as paged_attn_fp8_decode does).  The pages' write path quantizes
+ * K/V on store inside the fused small-batch prep kernel that also emits q
+ * (vLLM PR 54705 "Purpose", quant-on-store); here the store rides on the
+ * decode launch that reads the token's tile, so the step costs the decode
+ * and merge launches only.
+ * k_new, v_new:  device bf16 [num_seqs][num_kv_heads][head_dim], contiguous,
+ *                16-byte aligned: the step's new token of each sequence.  It
+ *                is the sequence's last key: position seq_lens[b] - 1, in
+ *                cache block block_table[b][(seq_lens[b]-1) / block_size],
+ *                row (seq_lens[b]-1) % block_size.  A sequence with
+ *                seq_lens[b] == 0 stores nothing.
+ * amax_k_inout, amax_v_inout: NULL, or device float >= 0: raised to the max
+ *                |k_new| (|v_new|) over all sequences (NaN ignored).
+ * Other arguments and the result are those of paged_attn_fp8_decode; the
+ * cache bytes written are bit-identical to kv_store_e4m3's, and the output
+ * equals that of kv_store_e4m3 followed by paged_attn_fp8_decode.  An
+ * invalid block-table entry for the new token's block sets
+ * FP8KV_DEVERR_BAD_BLOCK and stores nothing.
+ */
+fp8kv_status paged_attn_fp8_decode_store(const fp8kv_cache *cache, const fp8kv_bf16 *q,
+                                         int32_t num_q_heads, const fp8kv_bf16 *k_new,
+                                         const fp8kv_bf16 *v_new, const int32_t *block_table,
+                                         int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                                         int32_t num_seqs, float q_scale, float k_scale,
+                                         float v_scale, float softmax_scale,
+                                         const fp8kv_bf16 *rel_bias, int64_t bias_tok_stride,
+                                         int32_t rel_extent, int32_t window, float *amax_k_inout,
+                                         float *amax_v_inout, fp8kv_bf16 *out, void *workspace,
+                                         size_t workspace_bytes, void *stream);
+
+/*
  * paged_attn_fp8_decode_noalloc -- paged_attn_fp8_decode for callers that
  * cannot provide a workspace.  (The pages describe no such call; it exists
  * for users of this library.)  Some callers cannot allocate device memory at
