@@ -387,6 +387,55 @@ def bench_prefill(fk, dev, steps, warmup, world, only_group=None):
             "flops_per_step": flops, "tokens": sum(q_lens)}
 
 
+def bench_chunked_prefill(fk, dev, steps, warmup, world):
+    """One 4,096-query chunk attending over 65,536 keys (a cached prefix)."""
+    spec = workloads.PREFILL_CHUNK_64K
+    inp = workloads.make_prefill(spec, device=dev, seed=0)
+    kv = inp["kv"]
+    cache = fk.KVCache.empty(kv.num_blocks, kv.block_size, spec.Hkv, spec.D, device=dev)
+    fk.kv_store_e4m3(cache, kv.k, kv.v, kv.slot_mapping, 1.0, 1.0)
+    out = torch.empty_like(inp["q"])
+    maxq = max(inp["q_lens"])
+    pairs = sum(sum(kl - ql + i + 1 for i in range(ql))
+                for ql, kl in zip(inp["q_lens"], inp["k_lens"]))
+    flops = 4 * spec.Hq * spec.D * pairs
+
+    def step():
+        fk.attn_fp8_varlen_prefill(cache, inp["q"], inp["cu_seqlens_q"], kv.seq_lens,
+                                   kv.block_table, maxq, 1.0, 1.0, 1.0, rel_bias=inp["rel"],
+                                   window=0, out=out)
+    ms = time_steps(step, steps, warmup, world)
+    fp8_peak = 2.0 * peaks()["bf16_tflops"]
+    return {"workload": spec.name, "ms_per_step": ms, "tflops": flops / ms / 1e9,
+            "roofline": {"bound": "tensor", "achieved": flops / ms / 1e9, "peak": fp8_peak,
+                         "unit": "TFLOP/s", "frac": flops / ms / 1e9 / fp8_peak}}
+
+
+def bench_store_and_bands(fk, dev, steps, warmup, world):
+    """Quant-on-store of the whole 64-sequence pool (1.08M tokens) and the band
+    counters over its V, each against the measured HBM bandwidth."""
+    spec = workloads.DECODE_32K
+    inp = workloads.make_decode(spec, device=dev, seed=0)
+    kv = inp["kv"]
+    cache = fk.KVCache.empty(kv.num_blocks, kv.block_size, spec.Hkv, spec.D, device=dev)
+    elems = kv.k.shape[0] * spec.Hkv * spec.D
+    counts = torch.zeros(fk.BAND_COUNTS_BYTES, dtype=torch.uint8, device=dev)
+    hbm = peaks()["hbm_gbs"]
+    res = []
+    for name, fn, nbytes in (
+            ("kv_store_e4m3 of the 64-sequence pool (K and V)",
+             lambda: fk.kv_store_e4m3(cache, kv.k, kv.v, kv.slot_mapping, 1.0, 3.0),
+             elems * 2 * (2 + 1)),
+            ("kv_band_counts over the pool's V at scale 3",
+             lambda: fk.kv_band_counts(kv.v, 3.0, counts=counts), elems * 2)):
+        ms = time_steps(fn, steps, warmup, world)
+        gbs = nbytes / ms / 1e6
+        res.append({"workload": name, "ms_per_step": ms, "gbs": gbs,
+                    "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                                 "frac": gbs / hbm}})
+    return res
+
+
 def bench_decode_extra(fk, spec, dev, steps, warmup, world, calibrate=False):
     run = DecodeRun(fk, spec, dev, calibrate=calibrate)
     ms = time_steps(run.step, steps, warmup, world)
@@ -514,12 +563,16 @@ def main():
     if not args.no_extra:
         extra = []
         for fn in (lambda: bench_prefill(fk, dev, args.steps, args.warmup, world),
+                   lambda: bench_chunked_prefill(fk, dev, max(3, args.steps // 4), args.warmup,
+                                                 world),
+                   lambda: bench_store_and_bands(fk, dev, args.steps, args.warmup, world),
                    lambda: bench_decode_extra(fk, workloads.DECODE_128K_CAL, dev, args.steps,
                                               args.warmup, world, calibrate=True),
                    lambda: bench_decode_extra(fk, workloads.DECODE_1M, dev, args.steps,
                                               args.warmup, world)):
             try:
-                extra.append(fn())
+                r = fn()
+                extra.extend(r if isinstance(r, list) else [r])
             except Exception as e:  # noqa: BLE001
                 extra.append({"error": repr(e)[:300]})
             torch.cuda.empty_cache()

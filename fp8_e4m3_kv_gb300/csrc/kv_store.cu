@@ -128,7 +128,9 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // Band counters of one stream at one scale: the quotient and code of
 // quantize16, then per element the finite / non-zero / clipped / flushed
 // counts and the relative round-trip error (summed in fp32 over a thread's
-// 16 elements, then in fp64).  One 64-bit atomic per counter and block.
+// 16 elements, then in fp64).  A flushed element decodes to 0, so its error
+// term is exactly 1; any other non-zero element's term uses the fast
+// division (a few ulp).  One 64-bit atomic per counter and block.
 template <bool kPow2>
 __global__ void __launch_bounds__(kStoreThreads)
 kv_band_kernel(const uint16_t *__restrict__ x, int64_t stride, const int64_t *__restrict__ slots,
@@ -137,7 +139,7 @@ kv_band_kernel(const uint16_t *__restrict__ x, int64_t stride, const int64_t *__
     __shared__ double red_e[kStoreThreads / 32];
     const int32_t chunks = row_elems / kChunk;
     const int64_t total = num_tokens * chunks;
-    unsigned long long n_fin = 0, n_nz = 0, n_clip = 0, n_flush = 0;
+    uint32_t c_fin = 0, c_nz = 0, c_clip = 0, c_flush = 0;   // this thread's counts
     double err = 0.0;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
@@ -151,20 +153,26 @@ kv_band_kernel(const uint16_t *__restrict__ x, int64_t stride, const int64_t *__
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
             const uint32_t bits = (w[k >> 1] >> (16 * (k & 1))) & 0xFFFFu;
-            if ((bits & 0x7F80u) == 0x7F80u) continue;   // NaN, +-Inf
-            ++n_fin;
+            const bool fin = (bits & 0x7F80u) != 0x7F80u;       // not NaN or +-Inf
+            const bool nz = fin && (bits & 0x7FFFu) != 0;
             const float xf = __uint_as_float(bits << 16);
-            if (xf == 0.0f) continue;
-            ++n_nz;
             const float q = kPow2 ? xf * s.inv : __fdiv_rn(xf, s.scale);
-            n_clip += fabsf(q) > kE4M3Max;
             const uint16_t code = f32x2_to_e4m3x2(q, 0.0f) & 0xFFu;
-            n_flush += (code & 0x7Fu) == 0;
+            const bool flushed = nz && (code & 0x7Fu) == 0;
             const float back = __low2float(e4m3x2_to_half2(code)) * s.scale;
-            e16 += fabsf(back - xf) / fabsf(xf);
+            c_fin += fin;
+            c_nz += nz;
+            c_clip += nz && fabsf(q) > kE4M3Max;
+            c_flush += flushed;
+            // the fast division wants its divisor within 2^-126 .. 2^126:
+            // move both operands by the same power of two first
+            const float ax = fabsf(xf);
+            const float f = ax > 0x1p64f ? 0x1p-64f : (ax < 0x1p-64f ? 0x1p64f : 1.0f);
+            e16 += flushed ? 1.0f : (nz ? __fdividef(fabsf(back - xf) * f, ax * f) : 0.0f);
         }
         err += static_cast<double>(e16);
     }
+    unsigned long long n_fin = c_fin, n_nz = c_nz, n_clip = c_clip, n_flush = c_flush;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {

@@ -141,3 +141,33 @@ def test_full_prefill_causal_group(fk):
 
 def test_full_prefill_window_group(fk):
     _full_group(fk, 1)
+
+
+def test_full_chunk_over_64k_prefix(fk):
+    """One 4,096-query chunk over 65,536 keys (a 61,440-key cached prefix), the
+    bench's chunked-prefill workload, on sampled rows."""
+    spec = workloads.PREFILL_CHUNK_64K
+    inp = workloads.make_prefill(spec, device=DEV, seed=0)
+    kv = inp["kv"]
+    cache = fk.KVCache.empty(kv.num_blocks, kv.block_size, spec.Hkv, spec.D, device=DEV)
+    fk.kv_store_e4m3(cache, kv.k, kv.v, kv.slot_mapping, 1.0, 1.0)
+    out = fk.attn_fp8_varlen_prefill(cache, inp["q"], inp["cu_seqlens_q"], kv.seq_lens,
+                                     kv.block_table, max(inp["q_lens"]), 1.0, 1.0, 1.0,
+                                     rel_bias=inp["rel"], window=0)
+    torch.cuda.synchronize()
+    assert fk.device_error() == 0
+    got = out.float().cpu().numpy()
+    assert np.isfinite(got).all()
+    rng = np.random.default_rng(2)
+    n = inp["q_lens"][0]
+    picks = sorted({0, 1, 127, 128, n - 1} | set(int(x) for x in rng.integers(0, n, 10)))
+    rows = [(i, int(rng.integers(spec.Hq))) for i in picks]
+    host = dict(inp)
+    host["kv"] = workloads.PagedKV(k=kv.k.cpu(), v=kv.v.cpu(), seq_lens=kv.seq_lens.cpu(),
+                                   tok_start=kv.tok_start.cpu(), block_table=kv.block_table.cpu(),
+                                   slot_mapping=kv.slot_mapping.cpu(), num_blocks=kv.num_blocks,
+                                   block_size=kv.block_size)
+    host["q"] = inp["q"].cpu()
+    host["rel"] = inp["rel"].cpu()
+    ref = oracle_prefill_rows(host, rows, 1.0, 1.0, 1.0, window=0, rel=host["rel"])
+    assert_close(np.stack([got[t, h] for t, h in rows]), ref, spec.name)

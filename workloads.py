@@ -174,6 +174,7 @@ class PrefillSpec:
     rel_extent: int = 0
     bias_std: float = 0.5
     windows: tuple = (0,)        # window of each group of sequences
+    prefix: int = 0              # cached keys before each chunk (seq_len_k = q_len + prefix)
     scales: tuple = (1.0, 1.0, 1.0)
 
 
@@ -185,6 +186,11 @@ DECODE_32K = DecodeSpec("decode_b64_h32x4_d128_ctx1k-32k_bias1024", B=64, Hq=32,
 PREFILL_16K = PrefillSpec("prefill_8seq_q512-4096_h32x4_d128_causal_sw512", q_lens=None,
                           q_lo=512, q_hi=4096, n_seqs=8, Hq=32, Hkv=4, D=128,
                           block_size=16, rel_extent=128, windows=(0, 512))
+# one 4,096-query chunk over a 61,440-key cached prefix (65,536 keys in all):
+# the pages' "chunked prefill 64K" kernel case
+PREFILL_CHUNK_64K = PrefillSpec("prefill_chunk_q4096_k65536_h32x4_d128", q_lens=[4096], q_lo=4096,
+                                q_hi=4096, n_seqs=1, Hq=32, Hkv=4, D=128, block_size=16,
+                                rel_extent=128, windows=(0,), prefix=61440)
 DECODE_128K_CAL = DecodeSpec("decode_b8_h24x4_d256_ctx128k_calibrated", B=8, Hq=24, Hkv=4,
                              D=256, block_size=16, ctx_lo=131072, ctx_hi=131072,
                              k_dist="n_amax", v_dist="t3_amax",
@@ -193,8 +199,8 @@ DECODE_128K_CAL = DecodeSpec("decode_b8_h24x4_d256_ctx128k_calibrated", B=8, Hq=
 DECODE_1M = DecodeSpec("decode_b1_h32x4_d128_ctx1m", B=1, Hq=32, Hkv=4, D=128,
                        block_size=16, ctx_lo=1048576, ctx_hi=1048576)
 
-WORKLOADS = {w.name: w for w in (TINY_DECODE, DECODE_32K, PREFILL_16K, DECODE_128K_CAL,
-                                 DECODE_1M)}
+WORKLOADS = {w.name: w for w in (TINY_DECODE, DECODE_32K, PREFILL_16K, PREFILL_CHUNK_64K,
+                                 DECODE_128K_CAL, DECODE_1M)}
 
 
 def make_decode(spec: DecodeSpec, *, device="cpu", seed: int = 0, lens=None,
@@ -238,7 +244,7 @@ def make_prefill(spec: PrefillSpec, *, device="cpu", seed: int = 0, q_lens=None,
                                               generator=g, device=device).tolist()
     q_lens = [int(x) for x in q_lens]
     if k_lens is None:
-        k_lens = list(q_lens)
+        k_lens = [L + spec.prefix for L in q_lens]
     kv = make_paged_kv(list(k_lens), spec.Hkv, spec.D, spec.block_size, g=g, device=device)
     Tq = sum(q_lens)
     q = draw_values((Tq, spec.Hq, spec.D), "normal", g, device)
@@ -262,5 +268,6 @@ def ceil_div(a: int, b: int) -> int:
 
 
 __all__ = ["PagedKV", "DecodeSpec", "PrefillSpec", "TINY_DECODE", "DECODE_32K", "PREFILL_16K",
+           "PREFILL_CHUNK_64K",
            "DECODE_128K_CAL", "DECODE_1M", "WORKLOADS", "make_decode", "make_prefill",
            "make_paged_kv", "draw_values", "bf16_bits", "ceil_div"]
