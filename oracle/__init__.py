@@ -76,6 +76,12 @@ def _load():
     lib.or_amax.restype = f32
     lib.or_amax.argtypes = [P, i64, P, i64, i32, i32, f32]
     lib.or_scale_from_amax.restype = ctypes.c_int
+    lib.or_row_scale.argtypes = [P, i32]
+    lib.or_row_scale.restype = f32
+    lib.or_quantize_per_token.argtypes = [P, i64, i32, P, P]
+    lib.or_quantize_per_token.restype = None
+    lib.or_attend_row_pt.argtypes = [i32, P, P, P, i64, P, P, i64, i64, f64, f64, P, i32, i32, P]
+    lib.or_attend_row_pt.restype = None
     lib.or_band_counts.argtypes = [P, i64, P, i64, i32, f32, P, P]
     lib.or_band_counts.restype = None
     lib.or_scale_from_amax.argtypes = [f32, ctypes.c_int, ctypes.POINTER(f32)]
@@ -173,6 +179,34 @@ def band_counts(x_bf16, scale: float, slot_mapping=None) -> dict:
     _load().or_band_counts(_ptr(x), row, _ptr(sm), T, row, float(scale), _ptr(counts), _ptr(err))
     return {"count": int(counts[0]), "nonzero": int(counts[1]), "clipped": int(counts[2]),
             "flushed": int(counts[3]), "rt_err_sum": float(err[0])}
+
+
+def quantize_per_token(x_bf16, row_len: int):
+    """Rows of row_len bf16 values -> (codes uint8 [rows][row_len], scales
+    float32 [rows]), one scale per row (a token's head)."""
+    x = _u16(x_bf16).reshape(-1, row_len)
+    codes = np.zeros(x.shape, dtype=np.uint8)
+    scales = np.zeros(x.shape[0], dtype=np.float32)
+    _load().or_quantize_per_token(_ptr(x), x.shape[0], row_len, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def attend_row_pt(q8, k8, v8, sk, sv, pos_q, sigma, s_q, bias=None, window=0):
+    """One query row over keys with per-token scales (k8, v8 [len][D] codes,
+    sk, sv [len] float32)."""
+    q8 = np.ascontiguousarray(q8, dtype=np.uint8)
+    k8 = np.ascontiguousarray(k8, dtype=np.uint8)
+    v8 = np.ascontiguousarray(v8, dtype=np.uint8)
+    sk = np.ascontiguousarray(sk, dtype=np.float32)
+    sv = np.ascontiguousarray(sv, dtype=np.float32)
+    D = q8.shape[0]
+    out = np.zeros(D, dtype=np.float64)
+    b = None if bias is None else _u16(bias)
+    E = 0 if b is None else b.shape[0]
+    _load().or_attend_row_pt(D, _ptr(q8), _ptr(k8), _ptr(v8), D, _ptr(sk), _ptr(sv), k8.shape[0],
+                             int(pos_q), float(sigma), float(s_q), _ptr(b), E, int(window),
+                             _ptr(out))
+    return out
 
 
 def scale_from_amax(a: float, rule: int = 0) -> float:

@@ -355,6 +355,92 @@ void or_attend_row(int32_t head_dim, const uint8_t *q8, const uint8_t *k8,
     free(qd);
 }
 
+/* ------------------------------------------------------------------ */
+/* Per-token scales                                                    */
+/* ------------------------------------------------------------------ */
+
+/* Per-token dynamic scale [local-inference-lab/vllm PR 189, per-token scale:
+ * each cached token carries its own scale beside its codes, so no calibrated
+ * per-tensor scale is needed].
+ * READING: one scale per token and KV head (one row of head_dim values):
+ * s = max |x| / 448 over the row's finite elements (NaN and +-Inf do not take
+ * part), as the correctly rounded fp32 quotient, and s = 1 for a row whose
+ * finite elements are all zero; each element is then quantized with
+ * or_quantize at that scale. */
+float or_row_scale(const uint16_t *x, int32_t n)
+{
+    int32_t i;
+    float m = 0.0f;
+    for (i = 0; i < n; ++i) {
+        float a = fabsf(bf16_to_float(x[i]));
+        if (isfinite(a) && a > m)
+            m = a;
+    }
+    return m > 0.0f ? (float)((double)m / (double)OR_E4M3_MAX) : 1.0f;
+}
+
+/* n_rows rows of row_len bf16 values -> codes (same shape) and one scale per
+ * row. */
+void or_quantize_per_token(const uint16_t *x, int64_t n_rows, int32_t row_len, uint8_t *codes,
+                           float *scales)
+{
+    int64_t r;
+    int32_t i;
+    for (r = 0; r < n_rows; ++r) {
+        float s = or_row_scale(x + r * row_len, row_len);
+        scales[r] = s;
+        for (i = 0; i < row_len; ++i)
+            codes[r * row_len + i] = or_quantize(x[r * row_len + i], s);
+    }
+}
+
+/* One query row over keys with per-token scales: key j is k_j = sk[j] *
+ * dec(k8_j) and v_j = sv[j] * dec(v8_j) (dequantize-then-attend); z_j =
+ * sigma * (s_q q8) . k_j + bias, o = softmax(z) . v.  Visibility, bias and
+ * the empty row as in or_attend_row. */
+void or_attend_row_pt(int32_t head_dim, const uint8_t *q8, const uint8_t *k8,
+                      const uint8_t *v8, int64_t ld, const float *sk, const float *sv,
+                      int64_t len_k, int64_t pos_q, double sigma, double s_q,
+                      const uint16_t *bias, int32_t rel_extent, int32_t window, double *out)
+{
+    int64_t j, lo = 0, hi, n;
+    int32_t d;
+    double *z, zmax = -INFINITY, wsum = 0.0;
+    for (d = 0; d < head_dim; ++d)
+        out[d] = 0.0;
+    hi = pos_q + 1 < len_k ? pos_q + 1 : len_k;
+    if (window > 0 && pos_q - window + 1 > lo)
+        lo = pos_q - window + 1;
+    n = hi - lo;
+    if (n <= 0)
+        return;
+    z = (double *)malloc(sizeof(double) * (size_t)n);
+    for (j = lo; j < hi; ++j) {
+        const uint8_t *kr = k8 + j * ld;
+        double dot = 0.0, zj;
+        int64_t dist = pos_q - j;
+        for (d = 0; d < head_dim; ++d)
+            dot += (s_q * or_e4m3_decode(q8[d])) * ((double)sk[j] * or_e4m3_decode(kr[d]));
+        zj = sigma * dot;
+        if (bias && dist >= 0 && dist < rel_extent)
+            zj += or_bf16_to_double(bias[dist]);
+        z[j - lo] = zj;
+        if (zj > zmax)
+            zmax = zj;
+    }
+    for (j = 0; j < n; ++j) {
+        z[j] = exp(z[j] - zmax);
+        wsum += z[j];
+    }
+    for (j = lo; j < hi; ++j) {
+        const uint8_t *vr = v8 + j * ld;
+        double w = z[j - lo] / wsum;
+        for (d = 0; d < head_dim; ++d)
+            out[d] += w * ((double)sv[j] * or_e4m3_decode(vr[d]));
+    }
+    free(z);
+}
+
 /* Many rows, one per (sequence, query, head) the caller lists.  Row r reads
  * q8 + q_off[r], k8 + kv_off[r], v8 + kv_off[r] (rows ld apart), bias +
  * bias_off[r] (bias_off < 0: no bias), and writes head_dim doubles at

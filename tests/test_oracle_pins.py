@@ -347,6 +347,60 @@ def test_zero_bias_full_window_is_textbook_softmax_attention(oracle_lib):
     assert np.allclose(out99, ref99, rtol=1e-12, atol=1e-14)
 
 
+# ----------------------------------------------------------------- per-token scales
+def test_per_token_scale_maps_each_row_max_onto_448(oracle_lib):
+    """With s = max|x|/448 per row, every row's largest element encodes to
+    +-448 (0x7E / 0xFE), the scale is the fp32 quotient, a zero row gets 1 and
+    non-finite elements do not enter the max."""
+    g = torch.Generator().manual_seed(31)
+    x = workloads.draw_values((64, 128), "v_t3", g, "cpu")
+    x[5] = 0.0
+    x[7, 3] = float("inf")
+    x[9, 0] = float("nan")
+    bits = workloads.bf16_bits(x)
+    codes, scales = oracle_lib.quantize_per_token(bits, 128)
+    xf = x.float().numpy()
+    for r in range(64):
+        fin = np.isfinite(xf[r])
+        amax = float(np.abs(xf[r][fin]).max())
+        if amax == 0.0:
+            assert scales[r] == 1.0 and (codes[r] & 0x7F == 0).all()
+            continue
+        assert scales[r] == np.float32(np.float32(amax) / np.float32(448.0))
+        i = int(np.argmax(np.where(fin, np.abs(xf[r]), -1.0)))
+        assert codes[r, i] & 0x7F == 0x7E, r
+    assert codes[7, 3] == 0x7E          # +inf saturates at its row's scale
+
+
+def test_per_token_attention_with_equal_scales_is_the_per_tensor_oracle(oracle_lib):
+    rng = np.random.default_rng(32)
+    D, L = 128, 200
+    q8, k8, v8 = _rand_e4m3(rng, (D,)), _rand_e4m3(rng, (L, D)), _rand_e4m3(rng, (L, D))
+    sk = np.full(L, 0.75, dtype=np.float32)
+    sv = np.full(L, 1.5, dtype=np.float32)
+    bias = bf16_bits_of(list(rng.normal(0, 0.5, 64)))
+    for pos, w in ((L - 1, 0), (150, 40)):
+        a = oracle_lib.attend_row_pt(q8, k8, v8, sk, sv, pos, 0.09, 0.5, bias=bias, window=w)
+        b = oracle_lib.attend_row(q8, k8, v8, pos, 0.09, 0.5, 0.75, 1.5, bias=bias, window=w,
+                                  form=5)
+        assert np.allclose(a, b, rtol=1e-12, atol=1e-14)
+
+
+def test_per_token_attention_is_textbook_attention_on_dequantized_keys(oracle_lib):
+    from scipy.special import softmax
+    rng = np.random.default_rng(33)
+    D, L = 128, 90
+    q8, k8, v8 = _rand_e4m3(rng, (D,)), _rand_e4m3(rng, (L, D)), _rand_e4m3(rng, (L, D))
+    sk = rng.uniform(0.01, 5.0, L).astype(np.float32)
+    sv = rng.uniform(0.01, 5.0, L).astype(np.float32)
+    Q = 0.5 * oracle_lib.decode_array(q8)
+    K = sk.astype(np.float64)[:, None] * oracle_lib.decode_array(k8)
+    V = sv.astype(np.float64)[:, None] * oracle_lib.decode_array(v8)
+    ref = softmax(0.1 * (K @ Q)) @ V
+    out = oracle_lib.attend_row_pt(q8, k8, v8, sk, sv, L - 1, 0.1, 0.5)
+    assert np.allclose(out, ref, rtol=1e-12, atol=1e-14)
+
+
 def test_descale_fold_equals_dequantize_then_attend(oracle_lib):
     rng = np.random.default_rng(9)
     D, L = 128, 97
