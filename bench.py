@@ -436,6 +436,36 @@ def bench_store_and_bands(fk, dev, steps, warmup, world):
     return res
 
 
+def bench_decode_per_token(fk, dev, steps, warmup, world):
+    """The 64-sequence decode over a cache with per-token scales (written by
+    kv_store_e4m3_per_token): KV bytes plus 4 bytes of K and V scale per key
+    and KV head."""
+    spec = workloads.DECODE_32K
+    inp = workloads.make_decode(spec, device=dev, seed=0)
+    kv = inp["kv"]
+    cache = fk.KVCache.empty(kv.num_blocks, kv.block_size, spec.Hkv, spec.D, device=dev)
+    ks = torch.empty((kv.num_blocks, spec.Hkv, kv.block_size), dtype=torch.float32, device=dev)
+    vs = torch.empty_like(ks)
+    fk.kv_store_e4m3_per_token(cache, kv.k, kv.v, kv.slot_mapping, ks, vs)
+    q, rel = inp["q"], inp["rel"]
+    out = torch.empty_like(q)
+    n = fk.decode_workspace_size(q.shape[0], spec.Hq, spec.Hkv, spec.D, kv.max_blocks,
+                                 kv.block_size, 0, 0)
+    ws = torch.empty(n, dtype=torch.uint8, device=dev)
+    keys = sum(inp["lens"]) * spec.Hkv
+    nbytes = keys * (2 * spec.D + 8) + 2 * q.numel() * 2 + rel.numel() * 2
+
+    def step():
+        fk.paged_attn_fp8_decode_per_token(cache, q, kv.block_table, kv.seq_lens, 1.0, ks, vs,
+                                           rel_bias=rel, out=out, workspace=ws)
+    ms = time_steps(step, steps, warmup, world)
+    gbs = nbytes / ms / 1e6
+    hbm = peaks()["hbm_gbs"]
+    return {"workload": spec.name + "_per_token_scales", "ms_per_step": ms, "gbs": gbs,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                         "frac": gbs / hbm}}
+
+
 def bench_decode_extra(fk, spec, dev, steps, warmup, world, calibrate=False):
     run = DecodeRun(fk, spec, dev, calibrate=calibrate)
     ms = time_steps(run.step, steps, warmup, world)
@@ -566,6 +596,7 @@ def main():
                    lambda: bench_chunked_prefill(fk, dev, max(3, args.steps // 4), args.warmup,
                                                  world),
                    lambda: bench_store_and_bands(fk, dev, args.steps, args.warmup, world),
+                   lambda: bench_decode_per_token(fk, dev, args.steps, args.warmup, world),
                    lambda: bench_decode_extra(fk, workloads.DECODE_128K_CAL, dev, args.steps,
                                               args.warmup, world, calibrate=True),
                    lambda: bench_decode_extra(fk, workloads.DECODE_1M, dev, args.steps,

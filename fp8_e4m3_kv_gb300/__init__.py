@@ -60,6 +60,11 @@ _decode_noalloc = _sig("paged_attn_fp8_decode_noalloc", ctypes.c_int,
 _decode_store = _sig("paged_attn_fp8_decode_store", ctypes.c_int,
                      [ctypes.POINTER(CacheStruct), P, i32, P, P, P, i32, P, i32, f32, f32, f32,
                       f32, P, i64, i32, i32, P, P, P, P, sz, P])
+_store_pt = _sig("kv_store_e4m3_per_token", ctypes.c_int,
+                 [ctypes.POINTER(CacheStruct), P, P, i64, i64, P, i64, P, P, P])
+_decode_pt = _sig("paged_attn_fp8_decode_per_token", ctypes.c_int,
+                  [ctypes.POINTER(CacheStruct), P, i32, P, i32, P, i32, f32, f32, P, P, P, i64,
+                   i32, i32, P, P, sz, P])
 _ws_size = _sig("fp8kv_decode_workspace_size", sz, [i32, i32, i32, i32, i32, i32, i32, i32])
 _prefill = _sig("attn_fp8_varlen_prefill", ctypes.c_int,
                 [ctypes.POINTER(CacheStruct), P, i32, P, P, P, i32, i32, i32, f32, f32, f32,
@@ -73,6 +78,7 @@ _status_string = _sig("fp8kv_status_string", ctypes.c_char_p, [ctypes.c_int])
 
 EXPORTED = ("kv_store_e4m3", "paged_attn_fp8_decode", "paged_attn_fp8_decode_ex",
             "paged_attn_fp8_decode_noalloc", "paged_attn_fp8_decode_store",
+            "kv_store_e4m3_per_token", "paged_attn_fp8_decode_per_token",
             "fp8kv_decode_workspace_size", "attn_fp8_varlen_prefill", "kv_amax_calibrate",
             "kv_band_counts",
             "fp8kv_scale_from_amax", "fp8kv_cache_bytes", "fp8kv_device_error",
@@ -279,6 +285,63 @@ def paged_attn_fp8_decode(cache: KVCache, q: torch.Tensor, block_table: torch.Te
     return out
 
 
+def kv_store_e4m3_per_token(cache: KVCache, k: torch.Tensor, v: torch.Tensor,
+                            slot_mapping: torch.Tensor, k_scales: torch.Tensor,
+                            v_scales: torch.Tensor, stream=None) -> None:
+    """Quantize k, v [T][Hkv][D] bf16 with one scale per token and head
+    (max|x|/448) into the cache; the scales go to k_scales / v_scales, float32
+    [num_blocks][Hkv][block_size] on the cache's device."""
+    row = cache.num_kv_heads * cache.head_dim
+    ks, vs = _rows(k, "k", row), _rows(v, "v", row)
+    _need(slot_mapping, torch.int64, "slot_mapping", cache.device)
+    shape = (cache.num_blocks, cache.num_kv_heads, cache.block_size)
+    for name, t in (("k_scales", k_scales), ("v_scales", v_scales)):
+        _need(t, torch.float32, name, cache.device)
+        if tuple(t.shape) != shape or not t.is_contiguous():
+            raise ValueError("%s must be contiguous float32 %s" % (name, shape))
+    _check(_store_pt(cache.c(), _ptr(k), _ptr(v), ks, vs, _ptr(slot_mapping), k.shape[0],
+                     _ptr(k_scales), _ptr(v_scales), _stream(stream)), "kv_store_e4m3_per_token")
+
+
+def paged_attn_fp8_decode_per_token(cache: KVCache, q: torch.Tensor, block_table: torch.Tensor,
+                                    seq_lens: torch.Tensor, q_scale: float,
+                                    k_scales: torch.Tensor, v_scales: torch.Tensor,
+                                    softmax_scale: Optional[float] = None,
+                                    rel_bias: Optional[torch.Tensor] = None, window: int = 0,
+                                    out: Optional[torch.Tensor] = None,
+                                    workspace: Optional[torch.Tensor] = None,
+                                    stream=None) -> torch.Tensor:
+    """Decode over a cache written by kv_store_e4m3_per_token (its scale
+    arrays k_scales, v_scales); returns out [B][Hq][D] bf16."""
+    _need(q, torch.bfloat16, "q", cache.device)
+    if q.dim() != 3 or not q.is_contiguous() or q.shape[2] != cache.head_dim:
+        raise ValueError("q must be contiguous [B][Hq][D]")
+    B, Hq, D = q.shape
+    shape = (cache.num_blocks, cache.num_kv_heads, cache.block_size)
+    for name, t in (("k_scales", k_scales), ("v_scales", v_scales)):
+        _need(t, torch.float32, name, cache.device)
+        if tuple(t.shape) != shape or not t.is_contiguous():
+            raise ValueError("%s must be contiguous float32 %s" % (name, shape))
+    _need(block_table, torch.int32, "block_table", cache.device)
+    _need(seq_lens, torch.int32, "seq_lens", cache.device)
+    if block_table.dim() != 2 or block_table.shape[0] != B or not block_table.is_contiguous():
+        raise ValueError("block_table must be contiguous [B][max_blocks]")
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    rel, bstride, E = _bias_args(rel_bias, Hq)
+    if out is None:
+        out = torch.empty_like(q)
+    mb = block_table.shape[1]
+    if workspace is None:
+        n = decode_workspace_size(B, Hq, cache.num_kv_heads, D, mb, cache.block_size, window, 0)
+        workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=cache.device)
+    _check(_decode_pt(cache.c(), _ptr(q), Hq, _ptr(block_table), mb, _ptr(seq_lens), B, q_scale,
+                      softmax_scale, _ptr(k_scales), _ptr(v_scales), _ptr(rel), bstride, E, window,
+                      _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                      _stream(stream)), "paged_attn_fp8_decode_per_token")
+    return out
+
+
 def paged_attn_fp8_decode_store(cache: KVCache, q: torch.Tensor, k_new: torch.Tensor,
                                 v_new: torch.Tensor, block_table: torch.Tensor,
                                 seq_lens: torch.Tensor, q_scale: float, k_scale: float,
@@ -390,6 +453,7 @@ def device_error(clear: bool = True) -> int:
 __all__ = ["KVCache", "Fp8KVError", "kv_store_e4m3", "kv_amax_calibrate", "kv_band_counts",
            "band_counts_dict", "BAND_COUNTS_BYTES", "scale_from_amax",
            "paged_attn_fp8_decode", "paged_attn_fp8_decode_noalloc", "paged_attn_fp8_decode_store",
+           "kv_store_e4m3_per_token", "paged_attn_fp8_decode_per_token",
            "attn_fp8_varlen_prefill",
            "decode_workspace_size",
            "cache_bytes", "device_error", "status_string", "LIB_PATH", "EXPORTED"]

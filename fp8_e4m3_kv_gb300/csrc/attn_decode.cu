@@ -128,6 +128,10 @@ struct DecodeParams {
     int32_t num_kv_heads;
     QScale k_scale;
     QScale v_scale;
+    // per-token scales (the per-token variant of the kernel only):
+    // float[num_blocks][num_kv_heads][block_size], one per cached token and head
+    const float *k_tok_scale;
+    const float *v_tok_scale;
 };
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -211,7 +215,10 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
-template <int D, int GMAX>
+// kPT: per-token scales.  Key j's score is multiplied by its K scale; its P
+// by its V scale relative to the tile's largest V scale S (so P stays in the
+// e4m3 range), and the tile's O^T by S when it is accumulated.
+template <int D, int GMAX, bool kPT>
 __global__ void __launch_bounds__(DecCfg<D>::kThreads, DecCfg<D>::kCtasPerSm)
 decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
               const DecodeParams p) {
@@ -219,6 +226,7 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
     constexpr int HS = C::kHS;
     constexpr int GH = GMAX / HS;                      // heads per consumer warpgroup
     static_assert(GH * HS == GMAX && GH % 2 == 0, "head split: an even number of heads per warpgroup");
+    static_assert(!kPT || GH < 16, "the per-token variant keeps the V-scale max in head slot 15");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -469,7 +477,7 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
         }
         // Accumulate this warpgroup's heads of O^T of tile j (rescaled) into
         // the registers.
-        auto take_o = [&](int j, const float *alpha) -> bool {
+        auto take_o = [&](int j, const float *alpha, float sfac) -> bool {
             const int ob = j % C::kOBuf;
             if (!warp_wait(&o_full[ob], (j / C::kOBuf) & 1, fail, p.err)) return false;
             tc_fence_after_sync();
@@ -478,7 +486,8 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
                 float o[16];
                 tmem_ld_x16(tmem + lane_base + C::kColO + (ob * C::kCB + mh) * kNPad + gbase, o);
 #pragma unroll
-                for (int g = 0; g < GH; ++g) o_acc[mh][g] = fmaf(o_acc[mh][g], alpha[g], o[g]);
+                for (int g = 0; g < GH; ++g)
+                    o_acc[mh][g] = fmaf(o_acc[mh][g], alpha[g], kPT ? o[g] * sfac : o[g]);
             }
             tc_fence_before_sync();
             __syncwarp();
@@ -486,7 +495,28 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
             return true;
         };
 
+        float s_1 = 1.0f, s_2 = 1.0f;   // V-scale factors of tiles j - 1, j - 2 (kPT)
         for (int i = 0; i < ntiles; ++i) {
+            // per-token scales of this thread's keys (0 where not visible)
+            float tsk[C::kKB], tsv[C::kKB];
+            if constexpr (kPT) {
+#pragma unroll
+                for (int kb = 0; kb < C::kKB; ++kb) {
+                    const int64_t key = (t0 + i) * C::kKeys + kb * 128 + t;
+                    const int64_t lb = key / p.block_size;
+                    tsk[kb] = tsv[kb] = 0.0f;
+                    if (key < len && key >= lo && lb < p.max_blocks) {
+                        const int32_t id =
+                            __ldg(p.block_table + static_cast<int64_t>(b) * p.max_blocks + lb);
+                        if (id >= 0 && id < p.num_blocks) {
+                            const int64_t si = (static_cast<int64_t>(id) * p.num_kv_heads + kvh) *
+                                                   p.block_size + key % p.block_size;
+                            tsk[kb] = __ldg(p.k_tok_scale + si);
+                            tsv[kb] = __ldg(p.v_tok_scale + si);
+                        }
+                    }
+                }
+            }
             if (!warp_wait(&s_full[i & 1], (i >> 1) & 1, fail, p.err)) { ok = false; break; }
             tc_fence_after_sync();
             float sc[C::kKB][16];
@@ -511,7 +541,7 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
                 for (int g = 0; g < GH; ++g) {
                     float zz = -INFINITY;
                     if (valid && gbase + g < p.G) {
-                        zz = sc[kb][g] * p.score_log2;
+                        zz = sc[kb][g] * (kPT ? p.score_log2 * tsk[kb] : p.score_log2);
                         if (has_bias)
                             zz = fmaf(bf16_bits_to_float(__ldg(bias + g * p.rel_extent + dist)),
                                       kLog2e, zz);
@@ -530,10 +560,24 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
                 mx = warp_max(mx);
                 if (lane == 0) rb[wq * 16 + g] = mx;
             }
+            if constexpr (kPT) {
+                float mv = tsv[0];
+#pragma unroll
+                for (int kb = 1; kb < C::kKB; ++kb) mv = fmaxf(mv, tsv[kb]);
+                mv = warp_max(mv);
+                if (lane == 0) rb[wq * 16 + 15] = mv;
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(&red_bar[i & 1]);
             if (!warp_wait(&red_bar[i & 1], (i >> 1) & 1, fail, p.err)) { ok = false; break; }
             float alpha[GH], neg_m8[GH];
+            // kPT: the tile's largest V scale, and each key's V scale relative to it
+            float s_tile = 1.0f, vr[C::kKB];
+            if constexpr (kPT) {
+                s_tile = fmaxf(fmaxf(rb[15], rb[31]), fmaxf(rb[47], rb[63]));
+#pragma unroll
+                for (int kb = 0; kb < C::kKB; ++kb) vr[kb] = s_tile > 0.0f ? tsv[kb] / s_tile : 0.0f;
+            }
             uint8_t *phi = smem + C::kOffP + (i % C::kOBuf) * 2 * C::kPBytes;
             uint8_t *plo = phi + C::kPBytes;
 #pragma unroll
@@ -559,7 +603,8 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
                     const float p1 = ex2_approx(z[kb][g + 1] + neg_m8[g + 1]);
                     ls0 += p0;
                     ls1 += p1;
-                    const __half2 ph = __floats2half2_rn(p0, p1);
+                    const __half2 ph =
+                        kPT ? __floats2half2_rn(p0 * vr[kb], p1 * vr[kb]) : __floats2half2_rn(p0, p1);
                     const uint32_t h8 = __nv_cvt_halfraw2_to_fp8x2(ph, __NV_SATFINITE, __NV_E4M3);
                     const __half2 hh = e4m3x2_to_half2(static_cast<uint16_t>(h8));
                     const uint32_t l8 =
@@ -594,15 +639,17 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_full[i % C::kOBuf]);
-            if (i >= 2 && !take_o(i - 2, alpha_2)) { ok = false; break; }
+            if (i >= 2 && !take_o(i - 2, alpha_2, s_2)) { ok = false; break; }
 #pragma unroll
             for (int g = 0; g < GH; ++g) {
                 alpha_2[g] = alpha_1[g];
                 alpha_1[g] = alpha[g];
             }
+            s_2 = s_1;
+            s_1 = s_tile;
         }
-        if (ok && ntiles >= 2) ok = take_o(ntiles - 2, alpha_2);
-        if (ok && ntiles >= 1) ok = take_o(ntiles - 1, alpha_1);
+        if (ok && ntiles >= 2) ok = take_o(ntiles - 2, alpha_2, s_2);
+        if (ok && ntiles >= 1) ok = take_o(ntiles - 1, alpha_1, s_1);
 
         // l per head: sum of the thread partials of the warpgroup
 #pragma unroll
@@ -759,11 +806,11 @@ size_t workspace_bytes_for(int32_t num_seqs, int32_t num_q_heads, int32_t head_d
     return static_cast<size_t>(num_seqs) * num_q_heads * slots * (head_dim + 2) * sizeof(float);
 }
 
-template <int D, int GMAX>
+template <int D, int GMAX, bool kPT>
 fp8kv_status launch_decode(const CUtensorMap &km, const CUtensorMap &vm, const DecodeParams &p,
                            int num_kv_heads, int num_seqs, cudaStream_t stream) {
     using C = DecCfg<D>;
-    auto kern = decode_kernel<D, GMAX>;
+    auto kern = decode_kernel<D, GMAX, kPT>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
         cudaSuccess) {
         cudaGetLastError();
@@ -805,13 +852,20 @@ struct FusedStore {
     float *amax_v;
 };
 
+// Per-token scales of the cached K and V (float[num_blocks][Hkv][block_size]).
+struct PerToken {
+    const float *k_scales;
+    const float *v_scales;
+};
+
 fp8kv_status decode_impl(const fp8kv_cache *cache, const fp8kv_bf16 *q, int32_t num_q_heads,
                          const int32_t *block_table, int32_t max_blocks_per_seq,
                          const int32_t *seq_lens, int32_t num_seqs, float q_scale, float k_scale,
                          float v_scale, float softmax_scale, const fp8kv_bf16 *rel_bias,
                          int64_t bias_tok_stride, int32_t rel_extent, int32_t window,
                          fp8kv_bf16 *out, void *workspace, size_t workspace_bytes,
-                         int32_t split_tokens, const FusedStore *fs, void *stream) {
+                         int32_t split_tokens, const FusedStore *fs, const PerToken *pt,
+                         void *stream) {
     if (!cache || num_seqs < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || window < 0 ||
         split_tokens < 0)
         return FP8KV_ERR_ARG;
@@ -827,6 +881,9 @@ fp8kv_status decode_impl(const fp8kv_cache *cache, const fp8kv_bf16 *q, int32_t 
     if (split_tokens % (D == 128 ? DecCfg<128>::kKeys : DecCfg<256>::kKeys)) return FP8KV_ERR_ARG;
     if (num_seqs == 0) return FP8KV_OK;
     if (!q || !block_table || !seq_lens || !out || !cache->k || !cache->v) return FP8KV_ERR_ARG;
+    if (pt && (!pt->k_scales || !pt->v_scales || (reinterpret_cast<uintptr_t>(pt->k_scales) & 3) ||
+               (reinterpret_cast<uintptr_t>(pt->v_scales) & 3)))
+        return FP8KV_ERR_ARG;
     if (fs && (!fs->k_new || !fs->v_new || (reinterpret_cast<uintptr_t>(fs->k_new) & 15) ||
                (reinterpret_cast<uintptr_t>(fs->v_new) & 15) ||
                (reinterpret_cast<uintptr_t>(fs->amax_k) & 3) ||
@@ -880,13 +937,23 @@ fp8kv_status decode_impl(const fp8kv_cache *cache, const fp8kv_bf16 *q, int32_t 
     p.num_kv_heads = Hkv;
     p.k_scale = make_qscale(k_scale);
     p.v_scale = make_qscale(v_scale);
+    p.k_tok_scale = pt ? pt->k_scales : nullptr;
+    p.v_tok_scale = pt ? pt->v_scales : nullptr;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (D == 128)
-        st = G <= 8 ? launch_decode<128, 8>(km, vm, p, Hkv, num_seqs, s)
-                    : launch_decode<128, 16>(km, vm, p, Hkv, num_seqs, s);
-    else
-        st = G <= 8 ? launch_decode<256, 8>(km, vm, p, Hkv, num_seqs, s)
-                    : launch_decode<256, 16>(km, vm, p, Hkv, num_seqs, s);
+    if (pt) {
+        if (D == 128)
+            st = G <= 8 ? launch_decode<128, 8, true>(km, vm, p, Hkv, num_seqs, s)
+                        : launch_decode<128, 16, true>(km, vm, p, Hkv, num_seqs, s);
+        else
+            st = G <= 8 ? launch_decode<256, 8, true>(km, vm, p, Hkv, num_seqs, s)
+                        : launch_decode<256, 16, true>(km, vm, p, Hkv, num_seqs, s);
+    } else if (D == 128) {
+        st = G <= 8 ? launch_decode<128, 8, false>(km, vm, p, Hkv, num_seqs, s)
+                    : launch_decode<128, 16, false>(km, vm, p, Hkv, num_seqs, s);
+    } else {
+        st = G <= 8 ? launch_decode<256, 8, false>(km, vm, p, Hkv, num_seqs, s)
+                    : launch_decode<256, 16, false>(km, vm, p, Hkv, num_seqs, s);
+    }
     if (st != FP8KV_OK) return st;
     if (D == 128)
         decode_merge_kernel<128><<<dim3(num_q_heads, num_seqs), kMergeWarps * 32, 0, s>>>(
@@ -908,7 +975,7 @@ extern "C" fp8kv_status paged_attn_fp8_decode_ex(
     return decode_impl(cache, q, num_q_heads, block_table, max_blocks_per_seq, seq_lens, num_seqs,
                        q_scale, k_scale, v_scale, softmax_scale, rel_bias, bias_tok_stride,
                        rel_extent, window, out, workspace, workspace_bytes, split_tokens, nullptr,
-                       stream);
+                       nullptr, stream);
 }
 
 extern "C" fp8kv_status paged_attn_fp8_decode_store(
@@ -922,7 +989,22 @@ extern "C" fp8kv_status paged_attn_fp8_decode_store(
     const FusedStore fs{k_new, v_new, amax_k_inout, amax_v_inout};
     return decode_impl(cache, q, num_q_heads, block_table, max_blocks_per_seq, seq_lens, num_seqs,
                        q_scale, k_scale, v_scale, softmax_scale, rel_bias, bias_tok_stride,
-                       rel_extent, window, out, workspace, workspace_bytes, 0, &fs, stream);
+                       rel_extent, window, out, workspace, workspace_bytes, 0, &fs, nullptr,
+                       stream);
+}
+
+extern "C" fp8kv_status paged_attn_fp8_decode_per_token(
+    const fp8kv_cache *cache, const fp8kv_bf16 *q, int32_t num_q_heads, const int32_t *block_table,
+    int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t num_seqs, float q_scale,
+    float softmax_scale, const float *k_scales, const float *v_scales, const fp8kv_bf16 *rel_bias,
+    int64_t bias_tok_stride, int32_t rel_extent, int32_t window, fp8kv_bf16 *out, void *workspace,
+    size_t workspace_bytes, void *stream) {
+    if (num_seqs > 0 && (!k_scales || !v_scales)) return FP8KV_ERR_ARG;
+    const PerToken pt{k_scales, v_scales};
+    // the per-token scales replace k_scale and v_scale (1 in the fold and the merge)
+    return decode_impl(cache, q, num_q_heads, block_table, max_blocks_per_seq, seq_lens, num_seqs,
+                       q_scale, 1.0f, 1.0f, softmax_scale, rel_bias, bias_tok_stride, rel_extent,
+                       window, out, workspace, workspace_bytes, 0, nullptr, &pt, stream);
 }
 
 extern "C" fp8kv_status paged_attn_fp8_decode(

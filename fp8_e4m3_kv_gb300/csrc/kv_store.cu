@@ -208,6 +208,75 @@ kv_band_kernel(const uint16_t *__restrict__ x, int64_t stride, const int64_t *__
     }
 }
 
+// Per-token store: one warp per (token, KV head) row of D values.  The
+// row's scale is max |x| / 448 over its finite values (the IEEE quotient; 1
+// for an all-zero row), then every value is quantized with it exactly as
+// quantize16 does (division).  Lane l holds D/32 consecutive values.
+template <int D>
+__global__ void __launch_bounds__(kStoreThreads)
+kv_store_pt_kernel(const uint16_t *__restrict__ k, const uint16_t *__restrict__ v,
+                   int64_t k_stride, int64_t v_stride, const int64_t *__restrict__ slots,
+                   int64_t num_tokens, int32_t num_kv_heads, int32_t block_size, int64_t capacity,
+                   uint8_t *__restrict__ ck, uint8_t *__restrict__ cv, float *__restrict__ sk,
+                   float *__restrict__ sv, uint32_t *err) {
+    constexpr int kPer = D / 32;                  // values per lane (4 or 8)
+    const int lane = threadIdx.x & 31;
+    const int64_t rows = num_tokens * num_kv_heads;
+    for (int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5; w < rows;
+         w += ((int64_t)gridDim.x * blockDim.x) >> 5) {
+        const int64_t t = w / num_kv_heads;
+        const int32_t h = static_cast<int32_t>(w - t * num_kv_heads);
+        const int64_t slot = __ldg(slots + t);
+        if (slot < 0) continue;
+        if (slot >= capacity) {
+            if (lane == 0) atomicOr(err, FP8KV_DEVERR_BAD_SLOT);
+            continue;
+        }
+        const int64_t blk = slot / block_size, row = slot - blk * block_size;
+        const int64_t dst = ((blk * num_kv_heads + h) * block_size + row) * D + lane * kPer;
+        const int64_t sdst = (blk * num_kv_heads + h) * block_size + row;
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+            const uint16_t *src = (which ? v + t * v_stride : k + t * k_stride) + h * D + lane * kPer;
+            uint32_t wd[kPer / 2];
+            if constexpr (kPer == 4) {
+                const uint2 a = *reinterpret_cast<const uint2 *>(src);
+                wd[0] = a.x;
+                wd[1] = a.y;
+            } else {
+                const uint4 a = *reinterpret_cast<const uint4 *>(src);
+                wd[0] = a.x;
+                wd[1] = a.y;
+                wd[2] = a.z;
+                wd[3] = a.w;
+            }
+            float m = 0.0f;
+#pragma unroll
+            for (int i = 0; i < kPer; ++i) {
+                const uint32_t bits = (wd[i >> 1] >> (16 * (i & 1))) & 0xFFFFu;
+                if ((bits & 0x7F80u) != 0x7F80u) m = fmaxf(m, fabsf(__uint_as_float(bits << 16)));
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            QScale qs;
+            qs.scale = m > 0.0f ? __fdiv_rn(m, kE4M3Max) : 1.0f;
+            qs.inv = 0.0f;
+            qs.pow2 = 0u;
+            uint32_t out[kPer / 4];
+#pragma unroll
+            for (int i = 0; i < kPer / 4; ++i)
+                out[i] = quantize_bf16x2_as<false>(wd[2 * i], qs) |
+                         (quantize_bf16x2_as<false>(wd[2 * i + 1], qs) << 16);
+            uint8_t *c = which ? cv : ck;
+            if constexpr (kPer == 4)
+                *reinterpret_cast<uint32_t *>(c + dst) = out[0];
+            else
+                *reinterpret_cast<uint2 *>(c + dst) = make_uint2(out[0], out[1]);
+            if (lane == 0) (which ? sv : sk)[sdst] = qs.scale;
+        }
+    }
+}
+
 }  // namespace
 }  // namespace fp8kv
 
@@ -293,6 +362,42 @@ extern "C" fp8kv_status kv_band_counts(const fp8kv_bf16 *x, int64_t tok_stride,
     auto kernel = qs.pow2 ? kv_band_kernel<true> : kv_band_kernel<false>;
     kernel<<<grid, kStoreThreads, 0, static_cast<cudaStream_t>(stream)>>>(
         x, tok_stride, slot_mapping, num_tokens, row_elems, qs, counts);
+    if (cudaGetLastError() != cudaSuccess) return FP8KV_ERR_LAUNCH;
+    return FP8KV_OK;
+}
+
+extern "C" fp8kv_status kv_store_e4m3_per_token(const fp8kv_cache *cache, const fp8kv_bf16 *k,
+                                                const fp8kv_bf16 *v, int64_t k_tok_stride,
+                                                int64_t v_tok_stride,
+                                                const int64_t *slot_mapping, int64_t num_tokens,
+                                                float *k_scales, float *v_scales, void *stream) {
+    if (!cache || num_tokens < 0) return FP8KV_ERR_ARG;
+    const int32_t D = cache->head_dim, Hkv = cache->num_kv_heads, bs = cache->block_size;
+    if (Hkv <= 0 || bs <= 0 || cache->num_blocks < 0) return FP8KV_ERR_ARG;
+    if (D != 128 && D != 256) return FP8KV_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return FP8KV_OK;
+    const int64_t row = static_cast<int64_t>(Hkv) * D;
+    if (!k || !v || !slot_mapping || !k_scales || !v_scales || !cache->k || !cache->v ||
+        k_tok_stride < row || v_tok_stride < row || (k_tok_stride % 8) || (v_tok_stride % 8))
+        return FP8KV_ERR_ARG;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(cache->k) || !aligned16(cache->v) ||
+        (reinterpret_cast<uintptr_t>(k_scales) & 3) || (reinterpret_cast<uintptr_t>(v_scales) & 3))
+        return FP8KV_ERR_ARG;
+    int sms = 0;
+    fp8kv_status st = check_device(&sms);
+    if (st != FP8KV_OK) return st;
+    const int64_t warps = num_tokens * Hkv;
+    const int grid = grid_for(warps * 32, sms);
+    const int64_t capacity = cache->num_blocks * bs;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (D == 128)
+        kv_store_pt_kernel<128><<<grid, kStoreThreads, 0, s>>>(
+            k, v, k_tok_stride, v_tok_stride, slot_mapping, num_tokens, Hkv, bs, capacity,
+            cache->k, cache->v, k_scales, v_scales, device_error_word());
+    else
+        kv_store_pt_kernel<256><<<grid, kStoreThreads, 0, s>>>(
+            k, v, k_tok_stride, v_tok_stride, slot_mapping, num_tokens, Hkv, bs, capacity,
+            cache->k, cache->v, k_scales, v_scales, device_error_word());
     if (cudaGetLastError() != cudaSuccess) return FP8KV_ERR_LAUNCH;
     return FP8KV_OK;
 }

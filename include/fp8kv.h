@@ -252,6 +252,50 @@ fp8kv_status attn_fp8_varlen_prefill(const fp8kv_cache *cache, const fp8kv_bf16 
                                      void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * kv_store_e4m3_per_token -- quant-on-store with a dynamic scale per token
+ * and KV head, kept beside the cache (local-inference-lab/vllm PR 189: a
+ * per-token scale stored with each cached token, so that no calibrated
+ * per-tensor scale is needed).  For each stored token and KV head h, over
+ * the head's head_dim values x:
+ *   s = max |x| / 448 over the finite values (fp32 IEEE quotient; 1 if they
+ *       are all zero)
+ *   code = e4m3(x / s) exactly as kv_store_e4m3 quantizes at scale s
+ * The codes go to the cache like kv_store_e4m3's; s goes to
+ * k_scales[blk][h][row] (v_scales likewise), blk = slot / block_size,
+ * row = slot % block_size: float[num_blocks][num_kv_heads][block_size],
+ * device, 4-byte aligned, owned by the caller.
+ * k, v, strides, slot_mapping: as for kv_store_e4m3 (slot_mapping required);
+ * head_dim 128 or 256.
+ */
+fp8kv_status kv_store_e4m3_per_token(const fp8kv_cache *cache, const fp8kv_bf16 *k,
+                                     const fp8kv_bf16 *v, int64_t k_tok_stride,
+                                     int64_t v_tok_stride, const int64_t *slot_mapping,
+                                     int64_t num_tokens, float *k_scales, float *v_scales,
+                                     void *stream);
+
+/*
+ * paged_attn_fp8_decode_per_token -- paged_attn_fp8_decode over a cache
+ * written by kv_store_e4m3_per_token: key j of a sequence is
+ * k_j = k_scales[j] * dec(k8_j) and v_j = v_scales[j] * dec(v8_j) (its
+ * block's entries of the scale arrays), so the score is
+ * softmax_scale * q_scale * k_scales[j] * (q8 . k8_j) (+ bias) and the output
+ * sum_j P_j * v_scales[j] * v8_j.  In the kernel P_j is multiplied by
+ * v_scales[j] / S, S the largest V scale of its 128-key tile, before the
+ * two-term e4m3 split (P stays in range), and the tile's partial O by S.
+ * Other arguments, the workspace (fp8kv_decode_workspace_size with
+ * split_tokens 0) and the result are those of paged_attn_fp8_decode.
+ */
+fp8kv_status paged_attn_fp8_decode_per_token(const fp8kv_cache *cache, const fp8kv_bf16 *q,
+                                             int32_t num_q_heads, const int32_t *block_table,
+                                             int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                                             int32_t num_seqs, float q_scale, float softmax_scale,
+                                             const float *k_scales, const float *v_scales,
+                                             const fp8kv_bf16 *rel_bias, int64_t bias_tok_stride,
+                                             int32_t rel_extent, int32_t window, fp8kv_bf16 *out,
+                                             void *workspace, size_t workspace_bytes,
+                                             void *stream);
+
+/*
  * kv_band_counts -- clip and flush-to-zero counters and the round-trip error
  * of quantizing the stored values at one scale: the KV value-range
  * instrument of vLLM PR 54705 (evidence document, Tier 2: exact e4m3 band

@@ -1,0 +1,131 @@
+"""Per-token scales on the GPU against the oracle: the store's codes and
+scales bit-exact, decode within 2e-2 abs + 2e-2 rel of the float64 oracle
+attending over keys dequantized with their own scales."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from helpers import assert_close, bits, to_device
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def fk():
+    import fp8_e4m3_kv_gb300 as m
+    return m
+
+
+def store(fk, kv, Hkv, D, bs):
+    kd = to_device(kv, DEV)
+    cache = fk.KVCache.empty(kv.num_blocks, bs, Hkv, D, device=DEV, fill=0x7F)
+    ks = torch.full((kv.num_blocks, Hkv, bs), float("nan"), dtype=torch.float32, device=DEV)
+    vs = torch.full_like(ks, float("nan"))
+    fk.kv_store_e4m3_per_token(cache, kd.k, kd.v, kd.slot_mapping, ks, vs)
+    torch.cuda.synchronize()
+    assert fk.device_error() == 0
+    return cache, ks, vs, kd
+
+
+def check_store(fk, oracle_lib, kv, Hkv, D, bs):
+    cache, ks, vs, _ = store(fk, kv, Hkv, D, bs)
+    slots = kv.slot_mapping.cpu().numpy()
+    for name, x, c, sc in (("k", kv.k, cache.k, ks), ("v", kv.v, cache.v, vs)):
+        codes, scales = oracle_lib.quantize_per_token(bits(x.cpu()), D)
+        codes = codes.reshape(-1, Hkv, D)
+        scales = scales.reshape(-1, Hkv)
+        cc = c.cpu().numpy()
+        ss = sc.cpu().numpy()
+        keep = slots >= 0
+        blk, row = slots[keep] // bs, slots[keep] % bs
+        got_c = cc[blk, :, row, :]
+        got_s = ss[blk, :, row]
+        assert np.array_equal(got_c, codes[keep]), name
+        assert np.array_equal(got_s.view(np.uint32), scales[keep].view(np.uint32)), name
+    return cache, ks, vs
+
+
+@pytest.mark.parametrize("D,bs", [(128, 16), (256, 32)])
+def test_store_codes_and_scales_bit_exact(fk, oracle_lib, D, bs):
+    g = torch.Generator().manual_seed(41)
+    lens = [1, 17, 300]
+    kv = workloads.make_paged_kv(lens, 4, D, bs, g=g, device="cpu", v_dist="v_t3")
+    # rows of special values: all zero, +-Inf, NaN, tiny, one huge outlier
+    kv.k[0, 0] = 0.0
+    kv.k[1, 1, :3] = torch.tensor([float("inf"), -float("inf"), float("nan")])
+    kv.k[2, 2] = 1e-38
+    kv.v[3, 3, 5] = 3.0e38
+    kv.slot_mapping[4] = -1                      # an unstored token
+    check_store(fk, oracle_lib, kv, 4, D, bs)
+
+
+def oracle_rows_pt(oracle_lib, inp, rows, q_scale, window=0):
+    kv, q = inp["kv"], inp["q"]
+    B, Hq, D = q.shape
+    Hkv = kv.k.shape[1]
+    G = Hq // Hkv
+    starts = kv.tok_start.cpu().tolist()
+    lens = kv.seq_lens.cpu().tolist()
+    rel = inp["rel"]
+    memo = {}
+    out = []
+    for b, h in rows:
+        kvh = h // G
+        if (b, kvh) not in memo:
+            s, L = starts[b], lens[b]
+            k8, sk = oracle_lib.quantize_per_token(bits(kv.k[s:s + L, kvh].cpu()), D)
+            v8, sv = oracle_lib.quantize_per_token(bits(kv.v[s:s + L, kvh].cpu()), D)
+            memo[(b, kvh)] = (k8, sk, v8, sv)
+        k8, sk, v8, sv = memo[(b, kvh)]
+        q8 = oracle_lib.quantize(bits(q[b, h].cpu()), q_scale)
+        bias = None if rel is None else bits(rel[b, h].cpu())
+        out.append(oracle_lib.attend_row_pt(q8, k8, v8, sk, sv, lens[b] - 1, 1 / math.sqrt(D),
+                                            q_scale, bias=bias, window=window))
+    return np.stack(out)
+
+
+def run_decode(fk, oracle_lib, lens, Hq, Hkv, D, bs, window=0, E=0, v_dist="normal", seed=0,
+               q_scale=1.0):
+    spec = workloads.DecodeSpec("case", B=len(lens), Hq=Hq, Hkv=Hkv, D=D, block_size=bs,
+                                ctx_lo=1, ctx_hi=1, v_dist=v_dist, rel_extent=E, plant_v=True)
+    inp = workloads.make_decode(spec, device="cpu", seed=seed, lens=lens)
+    kv = inp["kv"]
+    cache, ks, vs, kd = store(fk, kv, Hkv, D, bs)
+    rel = None if inp["rel"] is None else inp["rel"].to(DEV)
+    out = fk.paged_attn_fp8_decode_per_token(cache, inp["q"].to(DEV), kd.block_table, kd.seq_lens,
+                                             q_scale, ks, vs, rel_bias=rel, window=window)
+    torch.cuda.synchronize()
+    assert fk.device_error() == 0
+    got = out.float().cpu().numpy()
+    assert np.isfinite(got).all()
+    rng = np.random.default_rng(seed)
+    rows = [(b, int(h)) for b in range(len(lens)) if lens[b] > 0
+            for h in rng.choice(Hq, min(Hq, 6), replace=False)]
+    ref = oracle_rows_pt(oracle_lib, inp, rows, q_scale, window=window)
+    assert_close(np.stack([got[b, h] for b, h in rows]), ref, "per-token decode")
+    if 0 in lens:
+        assert (got[lens.index(0)] == 0).all()
+
+
+def test_decode_heavy_tailed_v_with_bias(fk, oracle_lib):
+    """V = 17.47 t(3) with a planted 1,272: it would clip at a unity per-tensor
+    scale, not with its own scale."""
+    run_decode(fk, oracle_lib, [1, 2, 127, 128, 129, 1000, 3000], 32, 4, 128, 16, E=1024,
+               v_dist="v_t3", seed=1)
+
+
+def test_decode_window_and_empty(fk, oracle_lib):
+    run_decode(fk, oracle_lib, [0, 50, 511, 513, 1500], 8, 1, 128, 16, window=512, E=128, seed=2,
+               q_scale=0.5)
+
+
+def test_decode_head_dim_256_block_32(fk, oracle_lib):
+    run_decode(fk, oracle_lib, [90, 700], 24, 4, 256, 32, seed=3)
+
+
+def test_decode_sixteen_heads_per_kv_head(fk, oracle_lib):
+    run_decode(fk, oracle_lib, [77, 400], 32, 2, 128, 16, seed=4)
