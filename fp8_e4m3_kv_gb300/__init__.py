@@ -73,13 +73,15 @@ _amax = _sig("kv_amax_calibrate", ctypes.c_int, [P, P, i64, i64, P, i64, i32, i3
 _band_counts = _sig("kv_band_counts", ctypes.c_int, [P, i64, P, i64, i32, f32, P, P])
 _scale_from_amax = _sig("fp8kv_scale_from_amax", ctypes.c_int, [f32, i32, ctypes.POINTER(f32)])
 _cache_bytes = _sig("fp8kv_cache_bytes", sz, [i64, i32, i32, i32])
+_prefill_max_ctas = _sig("fp8kv_set_prefill_max_ctas", ctypes.c_int, [i32])
 _device_error = _sig("fp8kv_device_error", ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), i32])
 _status_string = _sig("fp8kv_status_string", ctypes.c_char_p, [ctypes.c_int])
 
 EXPORTED = ("kv_store_e4m3", "paged_attn_fp8_decode", "paged_attn_fp8_decode_ex",
             "paged_attn_fp8_decode_noalloc", "paged_attn_fp8_decode_store",
             "kv_store_e4m3_per_token", "paged_attn_fp8_decode_per_token",
-            "fp8kv_decode_workspace_size", "attn_fp8_varlen_prefill", "kv_amax_calibrate",
+            "fp8kv_decode_workspace_size", "attn_fp8_varlen_prefill",
+            "fp8kv_set_prefill_max_ctas", "kv_amax_calibrate",
             "kv_band_counts",
             "fp8kv_scale_from_amax", "fp8kv_cache_bytes", "fp8kv_device_error",
             "fp8kv_status_string")
@@ -443,6 +445,11 @@ def attn_fp8_varlen_prefill(cache: KVCache, q: torch.Tensor, cu_seqlens_q: torch
     return out
 
 
+def set_prefill_max_ctas(max_ctas: int) -> None:
+    """Caps the CTAs of the persistent head_dim-128 prefill (0: one per SM)."""
+    _check(_prefill_max_ctas(int(max_ctas)), "fp8kv_set_prefill_max_ctas")
+
+
 def device_error(clear: bool = True) -> int:
     """The current device's error word (synchronizes); 0 when clean."""
     w = ctypes.c_uint32()
@@ -454,6 +461,6 @@ __all__ = ["KVCache", "Fp8KVError", "kv_store_e4m3", "kv_amax_calibrate", "kv_ba
            "band_counts_dict", "BAND_COUNTS_BYTES", "scale_from_amax",
            "paged_attn_fp8_decode", "paged_attn_fp8_decode_noalloc", "paged_attn_fp8_decode_store",
            "kv_store_e4m3_per_token", "paged_attn_fp8_decode_per_token",
-           "attn_fp8_varlen_prefill",
+           "attn_fp8_varlen_prefill", "set_prefill_max_ctas",
            "decode_workspace_size",
            "cache_bytes", "device_error", "status_string", "LIB_PATH", "EXPORTED"]

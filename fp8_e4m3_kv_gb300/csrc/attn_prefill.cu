@@ -21,6 +21,8 @@
 // the FP8 tensor cores while the weights keep about 8 significant bits.
 #include <math.h>
 
+#include <atomic>
+
 #include "common.cuh"
 
 namespace fp8kv {
@@ -67,6 +69,8 @@ struct PrefillParams {
     int32_t window;
     int32_t n_qtiles;
     int32_t bias_vec;   // rows 16-byte aligned with an extent that is a multiple of 8
+    int32_t num_seqs;
+    int32_t persist;    // head_dim 128: one CTA per SM walking the sorted item list
     QScale q_scale;
     float score_log2;   // softmax_scale * q_scale * k_scale * log2(e)
     float v_scale;
@@ -433,45 +437,58 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
 }
 
 // ---------------------------------------------------------------------------
-// head_dim 128: two query tiles per CTA
+// head_dim 128: two independent query-tile pipelines per CTA
 //
-// One CTA computes query tiles 2c and 2c + 1 (256 rows) of one head of one
-// sequence.  Both tiles share every K/V tile the producer loads; TMEM holds
-// S0, S1 (128 columns each) and O0, O1 (128 columns each).  Warpgroup k (warps
-// 4k .. 4k + 3) runs the softmax of query tile k; one MMA thread per query
-// tile issues its QK and PV products.  Each key tile is worked in two halves
-// of 64 keys, each with its own half of S and of P, so that S and P are
-// double-buffered within the same TMEM and shared memory and the lazy rescale
-// is decided per half.  Per element the softmax is one FMA (the
-// folded score scale and the running max), one ex2, the row sum, and the
-// two-term e4m3 split done on packed f16 pairs.
+// A work item is one query tile (128 rows) of one head of one sequence.  A
+// CTA runs two pipelines, k = 0 and 1, each with its own items, K/V ring, Q8
+// and P buffers and TMEM columns (S_k: 128, O_k: 128), sharing only the
+// tensor cores and the issue slots; neither waits on the other, so one
+// pipeline's per-item work (loading and quantizing Q, writing the output)
+// overlaps the other's MMAs and softmax.  Pipeline k: warp 8 + 3k is its
+// producer (TMA-loads the item's key tiles into a 2-stage ring), warp 9 + k
+// its MMA issuer, warps 4k .. 4k + 3 its softmax warpgroup.  For up to 64
+// sequences the kernel is persistent: one CTA per SM, each pipeline working
+// through a list of items; within a pipeline the producer runs on into the
+// next item's key tiles, and the softmax warpgroup, as soon as the last P of
+// an item is written, loads the next item's Q (the issuer starts its QKs)
+// and then writes the finished item's output while those QKs run.  Each key
+// tile is worked in two halves of 64 keys, each with its own half of S and
+// of P, so that S and P are double-buffered within the same TMEM and shared
+// memory and the lazy rescale is decided per half.  Per element the softmax
+// is one FMA (the folded score scale and the running max), one ex2, the row
+// sum, and the two-term e4m3 split done on packed f16 pairs.
 // ---------------------------------------------------------------------------
-// Three warpgroups: two softmax warpgroups, then the producer warp, the MMA
-// warp and two idle warps.  The kernel is built for 384 threads at 168
-// registers; at run time the third warpgroup gives registers back
-// (setmaxnreg.dec to kRegsIo) and the softmax warpgroups take them
-// (setmaxnreg.inc to kRegsSoftmax): 2*128*224 + 128*56 = 384*168.
+// Three warpgroups: two softmax warpgroups, then the two producer warps and
+// the two MMA warps.  The kernel is built for 384 threads at 168 registers;
+// at run time the third warpgroup gives registers back (setmaxnreg.dec to
+// kRegsIo) and the softmax warpgroups take them (setmaxnreg.inc to
+// kRegsSoftmax): 2*128*224 + 128*56 = 384*168.
 constexpr int kPre2Threads = 384;
 constexpr int kRegsLaunch = 168;
 constexpr int kRegsSoftmax = 224;
 constexpr int kRegsIo = 56;
 static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsIo <= kPre2Threads * kRegsLaunch,
               "register split exceeds the launch's registers");
+// Batches of up to this many sequences run persistent (each CTA sorts them by
+// query count); larger ones get one CTA per two query tiles.
+constexpr int kPre2SchedSeqs = 64;
 
 struct Pre2Cfg {
-    static constexpr int kStages = 3;
+    static constexpr int kStages = 2;                       // per pipeline
     static constexpr int kTileBytes = kTile * 128;          // K or V tile, 16 KB
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kQBytes = kTile * 128;             // one Q8 tile, 16 KB
     static constexpr int kPBytes = kTile * kTile;           // one P term, 16 KB
-    static constexpr int kOffQ = 0;                         // [2] Q8 tiles
-    static constexpr int kOffStages = 2 * kQBytes;
-    static constexpr int kOffP = kOffStages + kStages * kStageBytes;   // [query tile][hi, lo]
+    static constexpr int kOffQ = 0;                         // [pipeline] Q8
+    static constexpr int kOffStages = 2 * kQBytes;          // [pipeline][stage]
+    static constexpr int kOffP = kOffStages + 2 * kStages * kStageBytes;   // [pipeline][hi, lo]
     static constexpr int kOffMisc = kOffP + 2 * 2 * kPBytes;
-    static constexpr int kSmemBytes = kOffMisc + 512 + 1024;
-    static constexpr uint32_t kTmemCols = 512;              // S0 S1 O0 O1
+    static constexpr int kOffSched = kOffMisc + 512;        // sorted sequence tables
+    static constexpr int kSmemBytes = kOffSched + 4 * 4 * kPre2SchedSeqs + 1024;
+    static constexpr uint32_t kTmemCols = 512;              // S0 O0 | S1 O1
     static constexpr int kHalf = kTile / 2;                 // keys per unit
 };
+static_assert(Pre2Cfg::kSmemBytes <= 227 * 1024, "shared memory");
 
 // 16 x 8 bf16 -> 16 x 8 e4m3 bytes, the scale's form fixed at compile time.
 template <bool kPow2>
@@ -572,6 +589,95 @@ __device__ __forceinline__ void load_bias64(const uint16_t *row, int32_t d0, int
     }
 }
 
+// One work item: query tile qt (128 rows) of head h of sequence b, and the
+// key tiles kt_lo .. kt_hi it reads.
+struct Pre2Item {
+    int32_t b, h, qt, q_first, n_rows;
+    int32_t len_k, P0, kt_lo, kt_hi;   // positions fit in int32: key counts are int32
+};
+
+// Fills the item; false when it holds no query (past the sequence's queries,
+// or fewer keys than queries).
+__device__ __forceinline__ bool pre2_item(const PrefillParams &p, int32_t b, int32_t q_first,
+                                          int32_t len_q, int32_t len_k, int32_t h, int32_t qt,
+                                          Pre2Item &it) {
+    if (qt < 0 || qt * kTile >= len_q || len_k < len_q) return false;
+    it.b = b;
+    it.h = h;
+    it.qt = qt;
+    it.q_first = q_first;
+    it.len_k = len_k;
+    it.n_rows = min(kTile, len_q - qt * kTile);
+    it.P0 = len_k - len_q + qt * kTile;
+    const int32_t key_lo = (p.window > 0 && it.P0 - p.window + 1 > 0) ? it.P0 - p.window + 1 : 0;
+    it.kt_lo = key_lo / kTile;
+    it.kt_hi = (it.P0 + it.n_rows - 1) / kTile;
+    return true;
+}
+
+// The sorted sequence table of a persistent launch: entry r describes the
+// sequence with the r-th most queries (ties by index).
+struct Pre2Seqs {
+    int32_t *seq, *q_first, *len_q, *len_k;   // len_q 0: no query to compute
+};
+
+// The items of one pipeline.  Every role of the pipeline walks them with
+// its own copy of this state and gets the same items in the same order.
+//
+// Persistent launch: the items are ordered by query tile index, highest first
+// (for causal and windowed rows, the items with the most key tiles first),
+// then by sequence in table order, then by head; empty items are left out.
+// With V = 2 x CTAs pipelines, pipeline v takes positions v, 2V - 1 - v,
+// 2V + v, 4V - 1 - v, ... of that list, so that each gets one of the
+// costliest and one of the cheapest items of every 2V.
+//
+// Flat launch (more sequences than the table holds): CTA (x, h, b) has query
+// tiles 2 x' and 2 x' + 1 of head h of sequence b, x' = pairs - 1 - x, one per
+// pipeline.
+struct Pre2Sched {
+    int32_t step = 0;        // items taken so far
+    int32_t lev_start = 0;   // list position of the current query tile level
+    int32_t lev_n = 0;       // items in it
+    int32_t lev = -1;        // levels passed, highest query tile first
+};
+
+__device__ __forceinline__ bool pre2_next(const PrefillParams &p, const Pre2Seqs &t, int k,
+                                          Pre2Sched &sc, Pre2Item &it) {
+    if (!p.persist) {
+        if (sc.step++ > 0) return false;
+        const int b = static_cast<int>(blockIdx.z);
+        const int q_first = __ldg(p.cu_q + b);
+        const int n_pairs = (p.n_qtiles + 1) / 2;
+        return pre2_item(p, b, q_first, __ldg(p.cu_q + b + 1) - q_first, __ldg(p.lens_k + b),
+                         static_cast<int>(blockIdx.y),
+                         2 * (n_pairs - 1 - static_cast<int>(blockIdx.x)) + k, it);
+    }
+    // list positions fit in int32 (checked when the launch is set up)
+    const int32_t V = 2 * static_cast<int32_t>(gridDim.x), v = 2 * blockIdx.x + k;
+    const int32_t blk = sc.step++;
+    const int32_t i = blk * V + ((blk & 1) ? V - 1 - v : v);
+    while (i >= sc.lev_start + sc.lev_n) {
+        if (sc.lev + 1 >= p.n_qtiles) return false;
+        sc.lev_start += sc.lev_n;
+        ++sc.lev;
+        // sequences with more than kTile * qt queries: a prefix of the table
+        const int32_t floor_q = kTile * (p.n_qtiles - 1 - sc.lev);
+        int lo = 0, hi = p.num_seqs;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (t.len_q[mid] > floor_q)
+                lo = mid + 1;
+            else
+                hi = mid;
+        }
+        sc.lev_n = lo * p.Hq;
+    }
+    const int32_t rem = i - sc.lev_start;
+    const int32_t r = rem / p.Hq;
+    return pre2_item(p, t.seq[r], t.q_first[r], t.len_q[r], t.len_k[r], rem - r * p.Hq,
+                     p.n_qtiles - 1 - sc.lev, it);
+}
+
 __global__ void __launch_bounds__(kPre2Threads, 1)
 prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                 const PrefillParams p) {
@@ -582,72 +688,68 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_pairs = (p.n_qtiles + 1) / 2;
-    const int pair = n_pairs - 1 - static_cast<int>(blockIdx.x);   // longest tiles first
-    const int h = blockIdx.y, b = blockIdx.z;
-    const int kvh = h / p.G;
-    const int q_first = p.cu_q[b];
-    const int len_q = p.cu_q[b + 1] - q_first;
-    const int64_t len_k = p.lens_k[b];
-    if (pair * 2 * kTile >= len_q || len_k < len_q) return;
 
-    // per query tile k of the pair: rows, positions and key tiles
-    int n_rows[2];
-    int64_t P0[2], kt_lo[2], kt_hi[2];
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        const int qt = 2 * pair + k;
-        n_rows[k] = max(0, min(kTile, len_q - qt * kTile));
-        P0[k] = len_k - len_q + static_cast<int64_t>(qt) * kTile;
-        const int64_t pos_last = P0[k] + max(n_rows[k], 1) - 1;
-        int64_t key_lo = 0;
-        if (p.window > 0 && P0[k] - p.window + 1 > 0) key_lo = P0[k] - p.window + 1;
-        kt_lo[k] = key_lo / kTile;
-        kt_hi[k] = pos_last / kTile;
-    }
-    const bool act1 = n_rows[1] > 0;
-    const int64_t kt0 = kt_lo[0];
-    const int64_t kt1 = act1 ? kt_hi[1] : kt_hi[0];
-    const int ntiles = static_cast<int>(kt1 - kt0 + 1);
-    // does query tile k use CTA-local key tile j?
-    auto need = [&](int k, int j) -> bool {
-        const int64_t t = kt0 + j;
-        return (k == 0 || act1) && t >= kt_lo[k] && t <= kt_hi[k];
-    };
-
+    // barriers of pipeline k at bars + 16 k
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffMisc);
-    uint64_t *full = bars;              // [kStages]
-    uint64_t *empty = bars + 4;         // [kStages]
-    // per query tile k and key half hh, index 2k + hh
-    uint64_t *s_full = bars + 8;        // S half written by QK
-    uint64_t *s_free = bars + 12;       // S half read into registers
-    uint64_t *p_full = bars + 16;       // P half written
-    uint64_t *o_done = bars + 20;       // PV of the P half complete
-    uint64_t *mma_done = bars + 24;     // [query tile]
-    uint64_t *q_full = bars + 26;       // [query tile] Q8 written
+    auto full = [&](int k, int s) { return bars + 16 * k + s; };         // stage loaded
+    auto empty = [&](int k, int s) { return bars + 16 * k + 2 + s; };    // stage consumed
+    auto s_full = [&](int k, int hh) { return bars + 16 * k + 4 + hh; }; // S half written by QK
+    auto s_free = [&](int k, int hh) { return bars + 16 * k + 6 + hh; }; // S half read
+    auto p_full = [&](int k, int hh) { return bars + 16 * k + 8 + hh; }; // P half written
+    auto o_done = [&](int k, int hh) { return bars + 16 * k + 10 + hh; };// PV of P half done
+    auto q_full = [&](int k) { return bars + 16 * k + 12; };             // Q8 of next item
+    auto mma_done = [&](int k) { return bars + 16 * k + 13; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc + 256);
     CtaFail *fail = reinterpret_cast<CtaFail *>(smem + C::kOffMisc + 260);
+    Pre2Seqs tab;
+    tab.seq = reinterpret_cast<int32_t *>(smem + C::kOffSched);
+    tab.q_first = tab.seq + kPre2SchedSeqs;
+    tab.len_q = tab.q_first + kPre2SchedSeqs;
+    tab.len_k = tab.len_q + kPre2SchedSeqs;
 
+    if (p.persist) {
+        // sort the sequences by query count, most first (ties by index): the
+        // rank of each is the number of sequences ahead of it.  The counts
+        // are staged in the P buffers, unused until the first item.
+        int32_t *eff = reinterpret_cast<int32_t *>(smem + C::kOffP);
+        for (int b = threadIdx.x; b < p.num_seqs; b += blockDim.x) {
+            const int32_t q0 = __ldg(p.cu_q + b), lq = __ldg(p.cu_q + b + 1) - q0;
+            eff[b] = (lq > 0 && __ldg(p.lens_k + b) >= lq) ? lq : 0;
+        }
+        __syncthreads();
+        for (int b = threadIdx.x; b < p.num_seqs; b += blockDim.x) {
+            const int32_t e = eff[b];
+            int r = 0;
+            for (int o = 0; o < p.num_seqs; ++o) {
+                const int32_t eo = eff[o];
+                r += (eo > e || (eo == e && o < b)) ? 1 : 0;
+            }
+            tab.seq[r] = b;
+            tab.q_first[r] = __ldg(p.cu_q + b);
+            tab.len_q[r] = e;
+            tab.len_k[r] = __ldg(p.lens_k + b);
+        }
+    }
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 2);   // one arrival per MMA issuer
-        }
-        for (int i = 0; i < 4; ++i) {
-            mbar_init(&s_full[i], 1);
-            mbar_init(&s_free[i], 4);
-            mbar_init(&p_full[i], 4);
-            mbar_init(&o_done[i], 1);
-        }
         for (int k = 0; k < 2; ++k) {
-            mbar_init(&mma_done[k], 1);
-            mbar_init(&q_full[k], 4);
+            for (int s = 0; s < C::kStages; ++s) {
+                mbar_init(full(k, s), 1);
+                mbar_init(empty(k, s), 1);
+            }
+            for (int hh = 0; hh < 2; ++hh) {
+                mbar_init(s_full(k, hh), 1);
+                mbar_init(s_free(k, hh), 4);
+                mbar_init(p_full(k, hh), 4);
+                mbar_init(o_done(k, hh), 1);
+            }
+            mbar_init(q_full(k), 4);
+            mbar_init(mma_done(k), 1);
         }
         fail->abort = 0;
         fence_mbar_init();
     }
     if (warp == 9) tmem_alloc(tmem_slot, C::kTmemCols);
-    if (warp == 8 && lane == 0) {
+    if ((warp == 8 || warp == 11) && lane == 0) {
         tma_prefetch_map(&kmap);
         tma_prefetch_map(&vmap);
     }
@@ -656,128 +758,154 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
+    // Per pipeline, counters that run across its items give every barrier
+    // phase: stages of its ring (each item's key tiles pass through it once),
+    // 64-key units (two per key tile; unit u uses S and P half u & 1), and
+    // items.
     if (warp >= 8) {
-      // the third warpgroup (producer, MMA, two idle warps) gives registers back
+      // the third warpgroup (producers and MMA issuers) gives registers back
       asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsIo));
-      if (warp == 8) {
+      if (warp == 8 || warp == 11) {
         // ------------------------------------------------------------ producer
+        const int k = warp == 8 ? 0 : 1;
         const uint64_t pol = l2_policy_evict_first();
         const int nb = kTile / p.block_size;
+        uint8_t *ring = smem + C::kOffStages + k * C::kStages * C::kStageBytes;
         int last_issued[C::kStages];
 #pragma unroll
         for (int s = 0; s < C::kStages; ++s) last_issued[s] = -1;
-        for (int i = 0; i < ntiles; ++i) {
-            const int s = i % C::kStages;
-            int32_t phys = static_cast<int32_t>(p.num_blocks);   // out of range: zero fill
-            if (lane < nb) {
-                const int64_t lb = (kt0 + i) * nb + lane;
-                if (lb * p.block_size < len_k && lb < p.max_blocks) {
-                    const int32_t id =
-                        __ldg(p.block_table + static_cast<int64_t>(b) * p.max_blocks + lb);
-                    if (id >= 0 && id < p.num_blocks)
-                        phys = id;
-                    else
-                        atomicOr(p.err, FP8KV_DEVERR_BAD_BLOCK);
+        int g = 0;   // stages filled
+        bool ok = true;
+        Pre2Sched sc;
+        Pre2Item it;
+        while (ok && pre2_next(p, tab, k, sc, it)) {
+            const int kvh = it.h / p.G;
+            for (int32_t t = it.kt_lo; t <= it.kt_hi; ++t, ++g) {
+                const int s = g % C::kStages;
+                int32_t phys = static_cast<int32_t>(p.num_blocks);   // out of range: zero fill
+                if (lane < nb) {
+                    const int64_t lb = static_cast<int64_t>(t) * nb + lane;
+                    if (lb * p.block_size < it.len_k && lb < p.max_blocks) {
+                        const int32_t id =
+                            __ldg(p.block_table + static_cast<int64_t>(it.b) * p.max_blocks + lb);
+                        if (id >= 0 && id < p.num_blocks)
+                            phys = id;
+                        else
+                            atomicOr(p.err, FP8KV_DEVERR_BAD_BLOCK);
+                    }
                 }
+                int w_ok = 1;
+                if (lane == 0)
+                    w_ok = mbar_wait(empty(k, s), ((g / C::kStages) & 1) ^ 1, fail, p.err);
+                if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) mbar_arrive_expect_tx(full(k, s), C::kStageBytes);
+                __syncwarp();
+                if (lane < nb) {
+                    uint8_t *kdst = ring + s * C::kStageBytes + lane * p.block_size * 128;
+                    tma_load_4d(kdst, &kmap, full(k, s), 0, 0, kvh, phys, pol);
+                    tma_load_4d(kdst + C::kTileBytes, &vmap, full(k, s), 0, 0, kvh, phys, pol);
+                }
+                last_issued[s] = g;
             }
-            int ok = 1;
-            if (lane == 0) ok = mbar_wait(&empty[s], ((i / C::kStages) & 1) ^ 1, fail, p.err);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-            if (lane == 0) mbar_arrive_expect_tx(&full[s], C::kStageBytes);
-            __syncwarp();
-            if (lane < nb) {
-                uint8_t *kdst = smem + C::kOffStages + s * C::kStageBytes + lane * p.block_size * 128;
-                tma_load_4d(kdst, &kmap, &full[s], 0, 0, kvh, phys, pol);
-                tma_load_4d(kdst + C::kTileBytes, &vmap, &full[s], 0, 0, kvh, phys, pol);
-            }
-            last_issued[s] = i;
         }
         if (lane == 0 && fail->abort) {
             for (int s = 0; s < C::kStages; ++s)
                 if (last_issued[s] >= 0)
-                    mbar_drain_p(&full[s], (last_issued[s] / C::kStages) & 1, p.err);
+                    mbar_drain_p(full(k, s), (last_issued[s] / C::kStages) & 1, p.err);
         }
-      } else if (warp == 9 || warp == 10) {
-        // ------------------------------------------------------------ MMA issuers
-        // One thread per query tile k (warp 9: tile 0, warp 10: tile 1), so
-        // neither tile's chain waits on the other's.  Work goes in units of
-        // 64 keys: unit u is half u & 1 of a key tile, with its own S half
-        // (TMEM columns k*128 + 64*(u & 1)) and P half (key bytes 64*(u & 1)
-        // of each P row).  After S of unit u the thread issues the PV of
-        // unit u - 1, so the softmax of one half overlaps the QK of the next
-        // and the PV of the last.  A stage is released once both threads
-        // are done with it (empty[] counts two arrivals).
+      } else {
+        // ------------------------------------------------------------ MMA issuer
+        // After the QK of unit u the thread issues the PV of unit u - 1, so
+        // the softmax of one half overlaps the QK of the next and the PV of
+        // the last; an item's last PV is issued before the thread moves on.
+        // The PV of a key tile's second half releases its stage.  The first
+        // PV of an item overwrites O: its P being written means the softmax
+        // warps have read the previous item's O.
         const int k = warp - 9;
         if (lane == 0) {
             const uint32_t idesc_qk = idesc_e4m3_f32(128, C::kHalf, false, false);
             const uint32_t idesc_pv = idesc_e4m3_f32(128, 128, false, true);
             const uint32_t q_addr = smem_u32(smem + C::kOffQ + k * C::kQBytes);
             const uint32_t p_addr = smem_u32(smem + C::kOffP + k * 2 * C::kPBytes);
-            int u = 0, last_j = -1;   // units whose QK was issued; last key tile used
-            bool ok = true, q_ready = false;
-            // O_k += P_k[:, half] . V_jj[half, :] for unit v (half v & 1 of
-            // key tile jj); the second half releases the stage
-            auto issue_pv = [&](int v, int jj) -> bool {
-                const int hv = v & 1;
-                if (!mbar_wait(&p_full[2 * k + hv], (v >> 1) & 1, fail, p.err)) return false;
-                tc_fence_after_sync();
-                const int s = jj % C::kStages;
-                const uint32_t v_addr =
-                    smem_u32(smem + C::kOffStages + s * C::kStageBytes + C::kTileBytes);
-#pragma unroll
-                for (int part = 0; part < 2; ++part) {
-#pragma unroll
-                    for (int kk = 0; kk < 2; ++kk) {
-                        const int ks = 2 * hv + kk;   // 32-key step within the tile
-                        const uint64_t a = sdesc_sw128(p_addr + part * C::kPBytes + ks * 32, 16, 1024);
-                        const uint64_t bd = sdesc_sw128(v_addr + ks * 32 * 128, kTile * 128, 1024);
-                        mma_e4m3(tmem + 256 + k * 128, a, bd, idesc_pv,
-                                 (v > 0 || part > 0 || kk > 0) ? 1u : 0u);
-                    }
-                }
-                tc_commit(&o_done[2 * k + hv]);
-                if (hv == 1) tc_commit(&empty[s]);
-                return true;
-            };
-            for (int j = 0; j < ntiles && ok; ++j) {
-                const int s = j % C::kStages;
-                if (!mbar_wait(&full[s], (j / C::kStages) & 1, fail, p.err)) { ok = false; break; }
-                if (!need(k, j)) {
-                    // not this query tile's key tile: release the stage now
-                    mbar_arrive(&empty[s]);
-                    continue;
-                }
-                const uint32_t k_addr = smem_u32(smem + C::kOffStages + s * C::kStageBytes);
-                for (int hh = 0; hh < 2; ++hh) {
-                    if (!q_ready && !(q_ready = mbar_wait(&q_full[k], 0, fail, p.err))) {
-                        ok = false;
-                        break;
-                    }
-                    if (!mbar_wait(&s_free[2 * k + hh], ((u >> 1) & 1) ^ 1, fail, p.err)) {
-                        ok = false;
-                        break;
-                    }
+            const uint32_t ring = smem_u32(smem + C::kOffStages + k * C::kStages * C::kStageBytes);
+            const uint32_t col_s = k * 256, col_o = k * 256 + 128;
+            int g = 0;   // stages seen
+            int U = 0;   // units whose QK was issued
+            int A = 0;   // items
+            bool ok = true;
+            Pre2Sched sc;
+            Pre2Item it;
+            while (ok && pre2_next(p, tab, k, sc, it)) {
+                const int g0 = g;
+                const int n = it.kt_hi - it.kt_lo + 1;
+                int ui = 0;   // units of this item issued
+                bool q_ready = false;
+                // O += P[:, half] . V_j[half, :] for unit v (half v & 1 of the
+                // item's key tile j); the second half releases the stage
+                auto issue_pv = [&](int v, bool first, int j) -> bool {
+                    const int hv = v & 1;
+                    if (!mbar_wait(p_full(k, hv), (v >> 1) & 1, fail, p.err)) return false;
                     tc_fence_after_sync();
+                    const int s = (g0 + j) % C::kStages;
+                    const uint32_t v_addr = ring + s * C::kStageBytes + C::kTileBytes;
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t a = sdesc_sw128(q_addr + kk * 32, 16, 1024);
-                        const uint64_t bd =
-                            sdesc_sw128(k_addr + hh * C::kHalf * 128 + kk * 32, 16, 1024);
-                        mma_e4m3(tmem + k * 128 + hh * C::kHalf, a, bd, idesc_qk, kk > 0);
+                    for (int part = 0; part < 2; ++part) {
+#pragma unroll
+                        for (int kk = 0; kk < 2; ++kk) {
+                            const int ks = 2 * hv + kk;   // 32-key step within the tile
+                            const uint64_t a =
+                                sdesc_sw128(p_addr + part * C::kPBytes + ks * 32, 16, 1024);
+                            const uint64_t bd = sdesc_sw128(v_addr + ks * 32 * 128, kTile * 128, 1024);
+                            mma_e4m3(tmem + col_o, a, bd, idesc_pv,
+                                     (!first || part > 0 || kk > 0) ? 1u : 0u);
+                        }
                     }
-                    tc_commit(&s_full[2 * k + hh]);
-                    ++u;
-                    if (u >= 2 && !issue_pv(u - 2, hh == 1 ? j : last_j)) {
+                    tc_commit(o_done(k, hv));
+                    if (hv == 1) tc_commit(empty(k, s));
+                    return true;
+                };
+                for (int j = 0; j < n && ok; ++j) {
+                    const int s = (g0 + j) % C::kStages;
+                    if (!mbar_wait(full(k, s), ((g0 + j) / C::kStages) & 1, fail, p.err)) {
                         ok = false;
                         break;
                     }
+                    const uint32_t k_addr = ring + s * C::kStageBytes;
+                    for (int hh = 0; hh < 2; ++hh) {
+                        if (!q_ready && !(q_ready = mbar_wait(q_full(k), A & 1, fail, p.err))) {
+                            ok = false;
+                            break;
+                        }
+                        if (!mbar_wait(s_free(k, hh), ((U >> 1) & 1) ^ 1, fail, p.err)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after_sync();
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t a = sdesc_sw128(q_addr + kk * 32, 16, 1024);
+                            const uint64_t bd =
+                                sdesc_sw128(k_addr + hh * C::kHalf * 128 + kk * 32, 16, 1024);
+                            mma_e4m3(tmem + col_s + hh * C::kHalf, a, bd, idesc_qk, kk > 0);
+                        }
+                        tc_commit(s_full(k, hh));
+                        ++U;
+                        ++ui;
+                        if (ui >= 2 && !issue_pv(U - 2, ui == 2, hh == 1 ? j : j - 1)) {
+                            ok = false;
+                            break;
+                        }
+                    }
                 }
-                last_j = j;
+                if (ok && ui > 0) ok = issue_pv(U - 1, ui == 1, n - 1);
+                g = g0 + n;
+                ++A;
             }
-            if (ok && u > 0) issue_pv(u - 1, last_j);
-            tc_commit(&mma_done[k]);
-            mbar_drain_p(&mma_done[k], 0, p.err);
+            tc_commit(mma_done(k));
+            mbar_drain_p(mma_done(k), 0, p.err);
         }
         __syncwarp();
       }
@@ -787,200 +915,33 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
         const int k = warp >> 2, wq = warp & 3;
         const int r = threadIdx.x & 127;
         const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-        const uint32_t col_s = k * 128, col_o = 256 + k * 128;
-        const int qt = 2 * pair + k;
-        const int my_rows = k == 0 ? n_rows[0] : n_rows[1];
-        const int64_t my_P0 = k == 0 ? P0[0] : P0[1];
-        const int64_t my_lo = k == 0 ? kt_lo[0] : kt_lo[1];
-        const int64_t my_hi = k == 0 ? kt_hi[0] : kt_hi[1];
-        const int64_t pos = my_P0 + r;
-        const bool row_ok = r < my_rows;
-        const int64_t pos_first = my_P0, pos_last = my_P0 + max(my_rows, 1) - 1;
-        const uint16_t *bias_row =
-            (p.rel && row_ok) ? p.rel + (static_cast<int64_t>(q_first) + qt * kTile + r) *
-                                            p.bias_tok_stride + static_cast<int64_t>(h) * p.rel_extent
-                              : nullptr;
+        const uint32_t col_s = k * 256, col_o = k * 256 + 128;
         const int sw = r & 7;
-        {
-            // Q8 of this query tile = e4m3(q / q_scale), rows past the
-            // sequence's queries zero.  Warp wq loads rows 32 wq .. 32 wq + 31,
-            // two rows per load instruction (16 lanes x 16 bytes per row),
-            // with all sixteen loads in flight; meanwhile the producer has
-            // started on the first K/V tiles.
-            uint8_t *q8 = smem + C::kOffQ + k * C::kQBytes;
-            const int row_in_pair = lane >> 4, col = lane & 15;   // 8 bf16 per lane
-            uint4 v[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int row = 32 * wq + 2 * i + row_in_pair;
-                v[i] = make_uint4(0, 0, 0, 0);
-                if (row < my_rows)
-                    v[i] = __ldg(reinterpret_cast<const uint4 *>(
-                        p.q + (static_cast<int64_t>(q_first) + qt * kTile + row) * p.Hq * D +
-                        static_cast<int64_t>(h) * D + col * 8));
-            }
-            // this row's bias is read on the diagonal key tiles: start it
-            // toward L2 now
-            if (bias_row != nullptr) {
-                for (int off = 0; off < p.rel_extent; off += 64) prefetch_l2(bias_row + off);
-                prefetch_l2(bias_row + p.rel_extent - 1);
-            }
-            uint2 q8w[16];
-            if (p.q_scale.pow2)
-                quantize_q16<true>(v, q8w, p.q_scale);
-            else
-                quantize_q16<false>(v, q8w, p.q_scale);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int row = 32 * wq + 2 * i + row_in_pair;
-                *reinterpret_cast<uint2 *>(q8 + row * 128 + (((col >> 1) ^ (row & 7)) << 4) +
-                                           (col & 1) * 8) = q8w[i];
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&q_full[k]);
-        }
-        float m_used = -INFINITY;
-        float2 lsum = make_float2(0.0f, 0.0f);   // two partial row sums
+        uint8_t *p_hi = smem + C::kOffP + k * 2 * C::kPBytes;
+        uint8_t *p_lo = p_hi + C::kPBytes;
+        uint8_t *ring = smem + C::kOffStages + k * C::kStages * C::kStageBytes;
+        int g = 0;   // stages seen
+        int c = 0;   // key tiles processed
         bool ok = true;
-        int c = 0;   // key tiles processed by this query tile
-        for (int j = static_cast<int>(my_lo - kt0); j <= static_cast<int>(my_hi - kt0) &&
-                                                    (k == 0 || act1) && ok;
-             ++j) {
-            const int64_t k0 = (kt0 + j) * kTile;
-            for (int hh = 0; hh < 2; ++hh) {
-                const int u = 2 * c + hh;   // unit: key half hh of this key tile
-                if (!warp_wait_p(&s_full[2 * k + hh], c & 1, fail, p.err)) { ok = false; break; }
-                tc_fence_after_sync();
-                if (hh == 0 && k0 + r >= len_k) {
-                    // keys past the end of the sequence may hold stale bytes
-                    // (NaN codes included): zero their V rows so that 0 * V
-                    // stays 0 in the MMA.  S of this tile being written means
-                    // the stage's TMA copies have landed.
-                    uint4 *q4 = reinterpret_cast<uint4 *>(smem + C::kOffStages +
-                                                          (j % C::kStages) * C::kStageBytes +
-                                                          C::kTileBytes + r * 128);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) q4[e] = make_uint4(0, 0, 0, 0);
-                }
-                const int64_t kh = k0 + hh * C::kHalf;
-                const bool full_half = (kh + C::kHalf - 1 <= pos_first) &&
-                                       (p.window == 0 || pos_last - kh < p.window);
-                const bool bias_half = bias_row != nullptr && pos - kh >= 0 &&
-                                       pos - kh - (C::kHalf - 1) < p.rel_extent;
-                float x[C::kHalf];
-                tmem_ld_x64(tmem + lane_base + col_s + hh * C::kHalf, x);
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&s_free[2 * k + hh]);
+        // the previous item, whose output is still in O
+        bool have_prev = false;
+        int64_t prev_tok = 0;   // token of its first query row
+        int prev_rows = 0, prev_h = 0;
+        float2 prev_l = make_float2(0.0f, 0.0f);
 
-                // Scores to log2 units: z = x * score_log2 (+ bias * log2(e)),
-                // -inf where masked.  Where no row of the warp has bias the
-                // scale stays folded into the FMA of P (mult); masking and the
-                // max do not need it, the scale being positive.
-                float mult = p.score_log2;
-                const bool any_bias = __any_sync(0xffffffffu, bias_half);
-                const int32_t d0 = static_cast<int32_t>(pos - kh);   // positions are int32
-                if (any_bias) {
-                    uint32_t Y[32];
-                    load_bias64(bias_half ? bias_row : nullptr, d0, p.rel_extent, p.bias_vec != 0, Y);
-#pragma unroll
-                    for (int e = 0; e < C::kHalf; ++e) {
-                        const uint32_t wd = Y[(63 - e) >> 1];
-                        const float bv = __uint_as_float(((63 - e) & 1) ? (wd & 0xFFFF0000u) : (wd << 16));
-                        x[e] = fmaf(bv, kLog2eP, x[e] * p.score_log2);
-                    }
-                    mult = 1.0f;
-                }
-                if (!full_half) {
-                    // key e of the half sits at distance d0 - e from this row:
-                    // visible for e in [e_lo, e_hi] (causal, window, sequence end)
-                    const int32_t keys_left =
-                        static_cast<int32_t>(len_k - kh < C::kHalf ? len_k - kh : C::kHalf);
-                    const int32_t e_hi = min(d0, keys_left - 1);
-                    const int32_t e_lo = p.window > 0 ? max(0, d0 - p.window + 1) : 0;
-#pragma unroll
-                    for (int e = 0; e < C::kHalf; ++e)
-                        x[e] = (e >= e_lo && e <= e_hi) ? x[e] : -INFINITY;
-                }
-                float mx = -INFINITY, m2 = -INFINITY;
-#pragma unroll
-                for (int e = 0; e < C::kHalf; e += 4) {
-                    mx = fmax3(mx, x[e], x[e + 1]);
-                    m2 = fmax3(m2, x[e + 2], x[e + 3]);
-                }
-                mx = fmaxf(mx, m2) * mult;
-                // lazy rescale: a row must move its reference max when its
-                // max grew by more than tau (P <= 2^(8 + tau) stays below
-                // 448).  O is rescaled a whole warp at a time, so once any row
-                // of the warp needs it, every row whose max grew moves too.
-                const bool resc = mx > m_used + kRescaleTau;
-                const bool rescale_o = __any_sync(0xffffffffu, resc && m_used != -INFINITY);
-                const bool move = resc || (rescale_o && mx > m_used);
-                const float m_new = move ? mx : m_used;
-                const float alpha = (move && m_used != -INFINITY) ? ex2_fast(m_used - m_new) : 1.0f;
-                // this P half was read by the PV of unit u - 2
-                if (u >= 2) {
-                    if (!warp_wait_p(&o_done[2 * k + hh], ((u - 2) >> 1) & 1, fail, p.err)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after_sync();
-                }
-                lsum = __fmul2_rn(lsum, make_float2(alpha, alpha));
-                m_used = m_new;
-                const float neg_m8 = (m_used == -INFINITY) ? 0.0f : kPOffset - m_used;
-                uint8_t *p_hi = smem + C::kOffP + k * 2 * C::kPBytes;
-                uint8_t *p_lo = p_hi + C::kPBytes;
-#pragma unroll
-                for (int q = 0; q < C::kHalf / 16; ++q) {
-                    uint4 hi, lo;
-                    p_chunk16(x + q * 16, mult, neg_m8, lsum, hi, lo);
-                    const uint32_t off = r * 128 + (((hh * (C::kHalf / 16) + q) ^ sw) << 4);
-                    *reinterpret_cast<uint4 *>(p_hi + off) = hi;
-                    *reinterpret_cast<uint4 *>(p_lo + off) = lo;
-                }
-                if (rescale_o) {
-                    // O holds the products up to unit u - 1 against the old
-                    // reference: scale it by alpha once the PV of unit u - 1
-                    // (the other half) is done, before this unit's PV is
-                    // issued.  Done after P so that the PV has had the whole
-                    // P phase to finish.
-                    if (!warp_wait_p(&o_done[2 * k + (hh ^ 1)], ((u - 1) >> 1) & 1, fail, p.err)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after_sync();
-#pragma unroll 1
-                    for (int q = 0; q < D / 64; ++q) {
-                        float o[64];
-                        tmem_ld_x64(tmem + lane_base + col_o + q * 64, o);
-#pragma unroll
-                        for (int e = 0; e < 64; ++e) o[e] *= alpha;
-                        tmem_st_x64(tmem + lane_base + col_o + q * 64, o);
-                    }
-                }
-                fence_proxy_async_smem();
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&p_full[2 * k + hh]);
-            }
-            if (ok) ++c;
-        }
-        // the last unit is the second half of the last key tile; its PV
-        // completing means every earlier MMA of this thread completed too
-        if (ok && c > 0 && warp_wait_p(&o_done[2 * k + 1], (c - 1) & 1, fail, p.err)) {
+        // out = bf16(v_scale * O / l) of the previous item, once the PV of
+        // its last unit (the second half of its last key tile; its completion
+        // means every earlier MMA of the pipeline completed too) is done.
+        // Staged through this pipeline's P buffers, row r in its own P_hi and
+        // P_lo rows (chunks 0-7 and 8-15), so that each warp stages and
+        // stores its own 32 rows, two rows per coalesced store instruction.
+        auto epilogue = [&]() -> bool {
+            if (!warp_wait_p(o_done(k, 1), (c - 1) & 1, fail, p.err)) return false;
             tc_fence_after_sync();
-            const float l = lsum.x + lsum.y;
+            const float l = prev_l.x + prev_l.y;
             const float f = (l > 0.0f) ? p.v_scale / l : 0.0f;
-            // out = bf16(v_scale * O / l), staged through this query tile's P
-            // buffer (free: its last PV is done; 128 rows x 256 bytes, chunk
-            // c of row r at c ^ (r & 15)) so that the global stores are
-            // coalesced: each warp writes back its own 32 rows, two rows per
-            // store instruction.
             float o[D];
             tmem_ld_x128(tmem + lane_base + col_o, o);
-            uint8_t *stage = smem + C::kOffP + k * 2 * C::kPBytes;
 #pragma unroll
             for (int cch = 0; cch < D / 8; ++cch) {
                 uint32_t w[4];
@@ -990,7 +951,8 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
                         __floats2bfloat162_rn(o[8 * cch + 2 * e] * f, o[8 * cch + 2 * e + 1] * f);
                     w[e] = *reinterpret_cast<const uint32_t *>(&v2);
                 }
-                *reinterpret_cast<uint4 *>(stage + r * 256 + ((cch ^ (r & 15)) << 4)) =
+                *reinterpret_cast<uint4 *>((cch < 8 ? p_hi : p_lo) + r * 128 +
+                                           (((cch & 7) ^ sw) << 4)) =
                     make_uint4(w[0], w[1], w[2], w[3]);
             }
             __syncwarp();
@@ -998,16 +960,226 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const int row = 32 * wq + 2 * i + row_in_pair;
-                if (row < my_rows) {
-                    const uint4 val =
-                        *reinterpret_cast<const uint4 *>(stage + row * 256 + ((col ^ (row & 15)) << 4));
-                    *reinterpret_cast<uint4 *>(p.out +
-                                               (static_cast<int64_t>(q_first) + qt * kTile + row) *
-                                                   p.Hq * D +
-                                               static_cast<int64_t>(h) * D + col * 8) = val;
+                if (row < prev_rows) {
+                    const uint4 val = *reinterpret_cast<const uint4 *>(
+                        (col < 8 ? p_hi : p_lo) + row * 128 + (((col & 7) ^ (row & 7)) << 4));
+                    *reinterpret_cast<uint4 *>(p.out + (prev_tok + row) * p.Hq * D +
+                                               static_cast<int64_t>(prev_h) * D + col * 8) = val;
                 }
             }
+            // the rows are read back before the next item's P overwrites them
+            __syncwarp();
+            return true;
+        };
+
+        Pre2Sched sc;
+        Pre2Item it;
+        while (ok && pre2_next(p, tab, k, sc, it)) {
+            const int g0 = g;
+            const int n = it.kt_hi - it.kt_lo + 1;
+            g += n;
+            const int64_t pos = it.P0 + r;
+            const bool row_ok = r < it.n_rows;
+            const int64_t pos_first = it.P0, pos_last = it.P0 + it.n_rows - 1;
+            const int64_t tok0 = static_cast<int64_t>(it.q_first) + it.qt * kTile;
+            const uint16_t *bias_row =
+                (p.rel && row_ok) ? p.rel + (tok0 + r) * p.bias_tok_stride +
+                                        static_cast<int64_t>(it.h) * p.rel_extent
+                                  : nullptr;
+            {
+                // Q8 of this item = e4m3(q / q_scale), rows past the
+                // sequence's queries zero.  Q8 is free: every QK of the
+                // previous item has completed, its S having been read.  Warp
+                // wq loads rows 32 wq .. 32 wq + 31, two rows per load
+                // instruction (16 lanes x 16 bytes per row), with all sixteen
+                // loads in flight; the producer is already filling the ring.
+                uint8_t *q8 = smem + C::kOffQ + k * C::kQBytes;
+                const int row_in_pair = lane >> 4, col = lane & 15;   // 8 bf16 per lane
+                uint4 v[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int row = 32 * wq + 2 * i + row_in_pair;
+                    v[i] = make_uint4(0, 0, 0, 0);
+                    if (row < it.n_rows)
+                        v[i] = __ldg(reinterpret_cast<const uint4 *>(
+                            p.q + (tok0 + row) * p.Hq * D + static_cast<int64_t>(it.h) * D +
+                            col * 8));
+                }
+                // this row's bias is read on the diagonal key tiles: start it
+                // toward L2 now
+                if (bias_row != nullptr) {
+                    for (int off = 0; off < p.rel_extent; off += 64) prefetch_l2(bias_row + off);
+                    prefetch_l2(bias_row + p.rel_extent - 1);
+                }
+                uint2 q8w[16];
+                if (p.q_scale.pow2)
+                    quantize_q16<true>(v, q8w, p.q_scale);
+                else
+                    quantize_q16<false>(v, q8w, p.q_scale);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int row = 32 * wq + 2 * i + row_in_pair;
+                    *reinterpret_cast<uint2 *>(q8 + row * 128 + (((col >> 1) ^ (row & 7)) << 4) +
+                                               (col & 1) * 8) = q8w[i];
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(q_full(k));
+            }
+            // the pipeline's next item, and its Q rows toward L2
+            {
+                Pre2Sched peek = sc;
+                Pre2Item nx;
+                if (pre2_next(p, tab, k, peek, nx) && r < nx.n_rows) {
+                    const uint16_t *nq =
+                        p.q + (static_cast<int64_t>(nx.q_first) + nx.qt * kTile + r) * p.Hq * D +
+                        static_cast<int64_t>(nx.h) * D;
+                    prefetch_l2(nq);
+                    prefetch_l2(nq + 64);
+                }
+            }
+            // the previous item's output, while the QKs of this one run
+            if (have_prev && !(ok = epilogue())) break;
+
+            float m_used = -INFINITY;
+            float2 lsum = make_float2(0.0f, 0.0f);   // two partial row sums
+            for (int j = 0; j < n && ok; ++j) {
+                const int64_t k0 = static_cast<int64_t>(it.kt_lo + j) * kTile;
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int u = 2 * c + hh;   // unit: key half hh of this key tile
+                    const int64_t kh = k0 + hh * C::kHalf;
+                    const bool full_half = (kh + C::kHalf - 1 <= pos_first) &&
+                                           (p.window == 0 || pos_last - kh < p.window);
+                    const bool bias_half = bias_row != nullptr && pos - kh >= 0 &&
+                                           pos - kh - (C::kHalf - 1) < p.rel_extent;
+                    const int32_t d0 = static_cast<int32_t>(pos - kh);   // positions are int32
+                    if (!warp_wait_p(s_full(k, hh), c & 1, fail, p.err)) { ok = false; break; }
+                    tc_fence_after_sync();
+                    if (hh == 0 && k0 + r >= it.len_k) {
+                        // keys past the end of the sequence may hold stale
+                        // bytes (NaN codes included): zero their V rows so
+                        // that 0 * V stays 0 in the MMA.  S of this tile being
+                        // written means the stage's TMA copies have landed.
+                        uint4 *q4 = reinterpret_cast<uint4 *>(
+                            ring + ((g0 + j) % C::kStages) * C::kStageBytes + C::kTileBytes +
+                            r * 128);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) q4[e] = make_uint4(0, 0, 0, 0);
+                    }
+                    float x[C::kHalf];
+                    tmem_ld_x64(tmem + lane_base + col_s + hh * C::kHalf, x);
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(s_free(k, hh));
+
+                    // Scores to log2 units: z = x * score_log2 (+ bias *
+                    // log2(e)), -inf where masked.  Where no row of the warp
+                    // has bias the scale stays folded into the FMA of P
+                    // (mult); masking and the max do not need it, the scale
+                    // being positive.
+                    float mult = p.score_log2;
+                    const bool any_bias = __any_sync(0xffffffffu, bias_half);
+                    if (any_bias) {
+                        uint32_t Y[32];
+                        load_bias64(bias_half ? bias_row : nullptr, d0, p.rel_extent,
+                                    p.bias_vec != 0, Y);
+#pragma unroll
+                        for (int e = 0; e < C::kHalf; ++e) {
+                            const uint32_t wd = Y[(63 - e) >> 1];
+                            const float bv =
+                                __uint_as_float(((63 - e) & 1) ? (wd & 0xFFFF0000u) : (wd << 16));
+                            x[e] = fmaf(bv, kLog2eP, x[e] * p.score_log2);
+                        }
+                        mult = 1.0f;
+                    }
+                    if (!full_half) {
+                        // key e of the half sits at distance d0 - e from this
+                        // row: visible for e in [e_lo, e_hi] (causal, window,
+                        // sequence end)
+                        const int32_t keys_left = static_cast<int32_t>(
+                            it.len_k - kh < C::kHalf ? it.len_k - kh : C::kHalf);
+                        const int32_t e_hi = min(d0, keys_left - 1);
+                        const int32_t e_lo = p.window > 0 ? max(0, d0 - p.window + 1) : 0;
+#pragma unroll
+                        for (int e = 0; e < C::kHalf; ++e)
+                            x[e] = (e >= e_lo && e <= e_hi) ? x[e] : -INFINITY;
+                    }
+                    float mx = -INFINITY, m2 = -INFINITY;
+#pragma unroll
+                    for (int e = 0; e < C::kHalf; e += 4) {
+                        mx = fmax3(mx, x[e], x[e + 1]);
+                        m2 = fmax3(m2, x[e + 2], x[e + 3]);
+                    }
+                    mx = fmaxf(mx, m2) * mult;
+                    // lazy rescale: a row must move its reference max when
+                    // its max grew by more than tau (P <= 2^(8 + tau) stays
+                    // below 448).  O is rescaled a whole warp at a time, so
+                    // once any row of the warp needs it, every row whose max
+                    // grew moves too.
+                    const bool resc = mx > m_used + kRescaleTau;
+                    const bool rescale_o = __any_sync(0xffffffffu, resc && m_used != -INFINITY);
+                    const bool move = resc || (rescale_o && mx > m_used);
+                    const float m_new = move ? mx : m_used;
+                    const float alpha =
+                        (move && m_used != -INFINITY) ? ex2_fast(m_used - m_new) : 1.0f;
+                    // this P half was read by the PV of unit u - 2
+                    if (u >= 2) {
+                        if (!warp_wait_p(o_done(k, hh), ((u - 2) >> 1) & 1, fail, p.err)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after_sync();
+                    }
+                    lsum = __fmul2_rn(lsum, make_float2(alpha, alpha));
+                    m_used = m_new;
+                    const float neg_m8 = (m_used == -INFINITY) ? 0.0f : kPOffset - m_used;
+#pragma unroll
+                    for (int q = 0; q < C::kHalf / 16; ++q) {
+                        uint4 hi, lo;
+                        p_chunk16(x + q * 16, mult, neg_m8, lsum, hi, lo);
+                        const uint32_t off = r * 128 + (((hh * (C::kHalf / 16) + q) ^ sw) << 4);
+                        *reinterpret_cast<uint4 *>(p_hi + off) = hi;
+                        *reinterpret_cast<uint4 *>(p_lo + off) = lo;
+                    }
+                    if (rescale_o) {
+                        // O holds the products up to unit u - 1 against the
+                        // old reference: scale it by alpha once the PV of unit
+                        // u - 1 (the other half) is done, before this unit's
+                        // PV is issued.  Done after P so that the PV has had
+                        // the whole P phase to finish.
+                        if (!warp_wait_p(o_done(k, hh ^ 1), ((u - 1) >> 1) & 1, fail, p.err)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after_sync();
+                        const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll 1
+                        for (int q = 0; q < D / 64; ++q) {
+                            float o[64];
+                            tmem_ld_x64(tmem + lane_base + col_o + q * 64, o);
+#pragma unroll
+                            for (int e = 0; e < 64; e += 2) {
+                                const float2 s2 = __fmul2_rn(make_float2(o[e], o[e + 1]), a2);
+                                o[e] = s2.x;
+                                o[e + 1] = s2.y;
+                            }
+                            tmem_st_x64(tmem + lane_base + col_o + q * 64, o);
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(p_full(k, hh));
+                }
+                if (ok) ++c;
+            }
+            have_prev = ok;
+            prev_tok = tok0;
+            prev_rows = it.n_rows;
+            prev_h = it.h;
+            prev_l = lsum;
         }
+        if (ok && have_prev) epilogue();
     }
 
     tc_fence_before_sync();
@@ -1034,15 +1206,24 @@ bool prefill2_registers_ok() {
     return ok == 1;
 }
 
+// CTAs of a persistent launch at most (0: one per SM).
+std::atomic<int> g_prefill_max_ctas{0};
+
 fp8kv_status launch_prefill2(const CUtensorMap &km, const CUtensorMap &vm, const PrefillParams &p,
-                             int num_seqs, cudaStream_t stream) {
+                             int num_seqs, int sms, cudaStream_t stream) {
+    const int cap = g_prefill_max_ctas.load(std::memory_order_relaxed);
+    if (cap > 0 && cap < sms) sms = cap;
     if (!prefill2_registers_ok()) return FP8KV_ERR_UNSUPPORTED;
     if (cudaFuncSetAttribute(prefill2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Pre2Cfg::kSmemBytes) != cudaSuccess) {
         cudaGetLastError();
         return FP8KV_ERR_LAUNCH;
     }
-    dim3 grid((p.n_qtiles + 1) / 2, p.Hq, num_seqs);
+    // persistent: two pipelines per CTA, at most one CTA per SM
+    const int64_t n_pairs = (p.n_qtiles + 1) / 2;
+    const int64_t n_items = n_pairs * p.Hq * num_seqs;
+    const dim3 grid = p.persist ? dim3(static_cast<unsigned>(n_items < sms ? n_items : sms))
+                                : dim3(static_cast<unsigned>(n_pairs), p.Hq, num_seqs);
     prefill2_kernel<<<grid, kPre2Threads, Pre2Cfg::kSmemBytes, stream>>>(km, vm, p);
     if (cudaGetLastError() != cudaSuccess) return FP8KV_ERR_LAUNCH;
     return FP8KV_OK;
@@ -1120,12 +1301,22 @@ extern "C" fp8kv_status attn_fp8_varlen_prefill(
     p.bias_vec = rel_bias && (reinterpret_cast<uintptr_t>(rel_bias) & 15) == 0 &&
                  bias_tok_stride % 8 == 0 && rel_extent % 8 == 0;
     p.window = window;
+    p.num_seqs = num_seqs;
     p.n_qtiles = (max_seqlen_q + kTile - 1) / kTile;
+    // the persistent schedule counts list positions in int32
+    p.persist = D == 128 && num_seqs <= kPre2SchedSeqs && sms > 0 &&
+                static_cast<int64_t>(p.n_qtiles) * num_seqs * num_q_heads < (1ll << 30);
     p.q_scale = make_qscale(q_scale);
     p.score_log2 = static_cast<float>(static_cast<double>(softmax_scale) * q_scale * k_scale *
                                       1.4426950408889634);
     p.v_scale = v_scale;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return D == 128 ? launch_prefill2(km, vm, p, num_seqs, s)
+    return D == 128 ? launch_prefill2(km, vm, p, num_seqs, sms, s)
                     : launch_prefill<256>(km, vm, p, num_seqs, s);
+}
+
+extern "C" fp8kv_status fp8kv_set_prefill_max_ctas(int32_t max_ctas) {
+    if (max_ctas < 0) return FP8KV_ERR_ARG;
+    g_prefill_max_ctas.store(max_ctas, std::memory_order_relaxed);
+    return FP8KV_OK;
 }

@@ -252,6 +252,19 @@ fp8kv_status attn_fp8_varlen_prefill(const fp8kv_cache *cache, const fp8kv_bf16 
                                      void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * fp8kv_set_prefill_max_ctas -- caps the grid of attn_fp8_varlen_prefill at
+ * head_dim 128.  For batches of up to 64 sequences that prefill is
+ * persistent: one CTA per SM, each running two pipelines that work through
+ * the (query tile, head, sequence) items, so that one item's Q load and
+ * output overlap the MMAs of the next item and of the other pipeline.  A cap
+ * below the SM count leaves SMs to work on other streams; 0 (the default)
+ * restores one CTA per SM.  The results do not depend on the cap.
+ * Process-wide, read at each launch.
+ * Returns FP8KV_ERR_ARG for a negative cap.
+ */
+fp8kv_status fp8kv_set_prefill_max_ctas(int32_t max_ctas);
+
+/*
  * kv_store_e4m3_per_token -- quant-on-store with a dynamic scale per token
  * and KV head, kept beside the cache (local-inference-lab/vllm PR 189: a
  * per-token scale stored with each cached token, so that no calibrated

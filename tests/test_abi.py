@@ -37,7 +37,7 @@ def test_header_declares_the_entry_points():
     for n in ("kv_store_e4m3", "paged_attn_fp8_decode", "attn_fp8_varlen_prefill",
               "kv_amax_calibrate", "fp8kv_scale_from_amax", "fp8kv_decode_workspace_size",
               "fp8kv_status_string", "fp8kv_device_error", "fp8kv_cache_bytes",
-              "paged_attn_fp8_decode_ex", "kv_band_counts"):
+              "paged_attn_fp8_decode_ex", "kv_band_counts", "fp8kv_set_prefill_max_ctas"):
         assert n in names, n
 
 
@@ -49,6 +49,14 @@ def test_library_exports_every_declared_symbol(lib):
         assert n in exported, n
     for n in lib.EXPORTED:
         assert n in exported, n
+
+
+def test_prefill_cta_cap_is_host_only(lib):
+    with pytest.raises(lib.Fp8KVError) as e:
+        lib.set_prefill_max_ctas(-1)
+    assert e.value.status == 1
+    lib.set_prefill_max_ctas(5)
+    lib.set_prefill_max_ctas(0)
 
 
 def test_status_strings(lib):

@@ -92,6 +92,64 @@ def test_heavy_bias(fk):
     run_case(fk, [400], E=512, bias_std=3.0, seed=8)
 
 
+def _prefill_at_caps(fk, q_lens, k_lens, caps, window=0, E=128, Hq=8, Hkv=2, seed=0):
+    """The same prefill once per CTA cap (0: one CTA per SM)."""
+    spec = workloads.PrefillSpec("case", q_lens=q_lens, q_lo=0, q_hi=0, n_seqs=len(q_lens),
+                                 Hq=Hq, Hkv=Hkv, D=128, block_size=16, rel_extent=E)
+    inp = workloads.make_prefill(spec, device="cpu", seed=seed, q_lens=q_lens, k_lens=k_lens)
+    kv = inp["kv"]
+    kd = to_device(kv, DEV)
+    cache = fk.KVCache.empty(kv.num_blocks, 16, Hkv, 128, device=DEV, fill=0x7F)
+    fk.kv_store_e4m3(cache, kd.k, kd.v, kd.slot_mapping, 1.0, 1.0)
+    q, cu = inp["q"].to(DEV), inp["cu_seqlens_q"].to(DEV)
+    rel = None if inp["rel"] is None else inp["rel"].to(DEV)
+    outs = []
+    try:
+        for cap in caps:
+            fk.set_prefill_max_ctas(cap)
+            outs.append(fk.attn_fp8_varlen_prefill(cache, q, cu, kd.seq_lens, kd.block_table,
+                                                   max(q_lens), 1.0, 1.0, 1.0, rel_bias=rel,
+                                                   window=window))
+            torch.cuda.synchronize()
+            assert fk.device_error() == 0
+    finally:
+        fk.set_prefill_max_ctas(0)
+    return inp, outs
+
+
+@pytest.mark.parametrize("window", [0, 200])
+def test_persistent_schedule_does_not_change_results(fk, window):
+    """With one, two or seven CTAs each CTA works through dozens of items
+    (query tile pairs of different sequences and heads, second tiles past a
+    sequence's queries, cached prefixes, windows) back to back: the output
+    must be bit-identical to one CTA per SM's, and match the oracle."""
+    q_lens = [1, 129, 256, 300, 700, 1000]
+    k_lens = [1, 193, 256, 600, 700, 1001]   # cached prefixes of 0 .. 300 keys
+    inp, outs = _prefill_at_caps(fk, q_lens, k_lens, [0, 1, 2, 7], window=window, seed=11)
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+    rng = np.random.default_rng(window)
+    cu = inp["cu_seqlens_q"].tolist()
+    rows = []
+    for b, n in enumerate(q_lens):
+        picks = {0, n - 1, 127, 128, 255, 256} | set(int(x) for x in rng.integers(0, n, 10))
+        rows += [(cu[b] + i, int(rng.integers(8))) for i in sorted(picks) if 0 <= i < n]
+    ref = oracle_prefill_rows(inp, rows, 1.0, 1.0, 1.0, window=window, rel=inp["rel"])
+    got = outs[0].float().cpu().numpy()
+    assert_close(np.stack([got[t, h] for t, h in rows]), ref, "persistent prefill")
+
+
+def test_many_sequences_one_cta_per_item(fk):
+    """More sequences than the persistent schedule sorts (64): one CTA per two
+    query tiles, on sampled rows."""
+    rng = np.random.default_rng(12)
+    q_lens = [int(x) for x in rng.integers(1, 300, 100)]
+    k_lens = [q + int(p) for q, p in zip(q_lens, rng.integers(0, 100, 100))]
+    cu = np.concatenate([[0], np.cumsum(q_lens)])
+    rows = [(int(cu[b] + rng.integers(q_lens[b])), int(rng.integers(4))) for b in range(0, 100, 3)]
+    run_case(fk, q_lens, k_lens=k_lens, Hq=4, Hkv=1, E=128, seed=12, rows=rows)
+
+
 def _full_group(fk, which):
     spec = workloads.PREFILL_16K
     inp = workloads.make_prefill(spec, device=DEV, seed=0)
@@ -110,6 +168,18 @@ def _full_group(fk, which):
                                      1.0, 1.0, 1.0, rel_bias=rel_g, window=window)
     torch.cuda.synchronize()
     assert fk.device_error() == 0
+    # a third of the SMs: each CTA takes about three times the items
+    try:
+        fk.set_prefill_max_ctas(50)
+        out2 = fk.attn_fp8_varlen_prefill(cache, q_g, cu_g, kv.seq_lens[lo:hi].contiguous(),
+                                          kv.block_table[lo:hi].contiguous(),
+                                          max(inp["q_lens"][lo:hi]), 1.0, 1.0, 1.0,
+                                          rel_bias=rel_g, window=window)
+        torch.cuda.synchronize()
+    finally:
+        fk.set_prefill_max_ctas(0)
+    assert fk.device_error() == 0
+    assert torch.equal(out, out2)
     got = out.float().cpu().numpy()
     assert np.isfinite(got).all()
     rng = np.random.default_rng(which)
