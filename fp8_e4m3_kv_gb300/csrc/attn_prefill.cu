@@ -74,6 +74,7 @@ struct PrefillParams {
     QScale q_scale;
     float score_log2;   // softmax_scale * q_scale * k_scale * log2(e)
     float v_scale;
+    float bias_fold;    // log2(e) / score_log2, or 0 where that is not a safe finite factor
 };
 
 __device__ __forceinline__ void mbar_drain_p(uint64_t *bar, uint32_t parity, uint32_t *err) {
@@ -1073,24 +1074,41 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
                     if (lane == 0) mbar_arrive(s_free(k, hh));
 
                     // Scores to log2 units: z = x * score_log2 (+ bias *
-                    // log2(e)), -inf where masked.  Where no row of the warp
-                    // has bias the scale stays folded into the FMA of P
-                    // (mult); masking and the max do not need it, the scale
-                    // being positive.
+                    // log2(e)), -inf where masked.  The scale stays folded
+                    // into the FMA of P (mult): the bias is added as bias *
+                    // log2(e) / score_log2; masking and the max do not need
+                    // the scale, it being positive.
                     float mult = p.score_log2;
                     const bool any_bias = __any_sync(0xffffffffu, bias_half);
                     if (any_bias) {
                         uint32_t Y[32];
                         load_bias64(bias_half ? bias_row : nullptr, d0, p.rel_extent,
                                     p.bias_vec != 0, Y);
+                        if (p.bias_fold > 0.0f) {
+                            // x + bias * log2(e) / score_log2: the score scale
+                            // stays folded into the FMA of P (packed pairs;
+                            // key e takes the upper half of its word for even e)
+                            const float2 c2 = make_float2(p.bias_fold, p.bias_fold);
 #pragma unroll
-                        for (int e = 0; e < C::kHalf; ++e) {
-                            const uint32_t wd = Y[(63 - e) >> 1];
-                            const float bv =
-                                __uint_as_float(((63 - e) & 1) ? (wd & 0xFFFF0000u) : (wd << 16));
-                            x[e] = fmaf(bv, kLog2eP, x[e] * p.score_log2);
+                            for (int e = 0; e < C::kHalf; e += 2) {
+                                const uint32_t wd = Y[(63 - e) >> 1];
+                                const float2 r2 = __ffma2_rn(
+                                    make_float2(__uint_as_float(wd & 0xFFFF0000u), __uint_as_float(wd << 16)),
+                                    c2, make_float2(x[e], x[e + 1]));
+                                x[e] = r2.x;
+                                x[e + 1] = r2.y;
+                            }
+                        } else {
+                            // scales too extreme for the factor: unfold
+#pragma unroll
+                            for (int e = 0; e < C::kHalf; ++e) {
+                                const uint32_t wd = Y[(63 - e) >> 1];
+                                const float bv = __uint_as_float(((63 - e) & 1) ? (wd & 0xFFFF0000u)
+                                                                                 : (wd << 16));
+                                x[e] = fmaf(bv, kLog2eP, x[e] * p.score_log2);
+                            }
+                            mult = 1.0f;
                         }
-                        mult = 1.0f;
                     }
                     if (!full_half) {
                         // key e of the half sits at distance d0 - e from this
@@ -1310,6 +1328,10 @@ extern "C" fp8kv_status attn_fp8_varlen_prefill(
     p.score_log2 = static_cast<float>(static_cast<double>(softmax_scale) * q_scale * k_scale *
                                       1.4426950408889634);
     p.v_scale = v_scale;
+    {
+        const double c = 1.0 / (static_cast<double>(softmax_scale) * q_scale * k_scale);
+        p.bias_fold = (c < 0x1p60 && c > 0x1p-60) ? static_cast<float>(c) : 0.0f;
+    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return D == 128 ? launch_prefill2(km, vm, p, num_seqs, sms, s)
                     : launch_prefill<256>(km, vm, p, num_seqs, s);
