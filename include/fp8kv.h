@@ -197,7 +197,7 @@ fp8kv_status paged_attn_fp8_decode_store(const fp8kv_cache *cache, const fp8kv_b
  *     16 MiB buffer (fp8kv_decode_workspace_size(..., split_tokens = 0)
  *     larger than 16 MiB).
  *   - The first call on a device looks up the buffer's device address (a
- *     CUDA runtime query); make that first call before any stream capture.
+ *     CUDA runtime query) and keeps it for later calls.
  *   - Every call on a device shares the one buffer and may overwrite what
  *     the previous call left there; nothing in it needs clearing between
  *     calls.  Calls that can overlap on the GPU (on different streams, or
