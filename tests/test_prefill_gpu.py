@@ -99,15 +99,17 @@ def test_heavy_bias(fk):
     run_case(fk, [400], E=512, bias_std=3.0, seed=8)
 
 
-def _prefill_at_caps(fk, q_lens, k_lens, caps, window=0, E=128, Hq=8, Hkv=2, seed=0):
+def _prefill_at_caps(fk, q_lens, k_lens, caps, window=0, E=128, Hq=8, Hkv=2, seed=0, bs=16,
+                     scales=(1.0, 1.0, 1.0)):
     """The same prefill once per CTA cap (0: one CTA per SM)."""
     spec = workloads.PrefillSpec("case", q_lens=q_lens, q_lo=0, q_hi=0, n_seqs=len(q_lens),
-                                 Hq=Hq, Hkv=Hkv, D=128, block_size=16, rel_extent=E)
+                                 Hq=Hq, Hkv=Hkv, D=128, block_size=bs, rel_extent=E)
     inp = workloads.make_prefill(spec, device="cpu", seed=seed, q_lens=q_lens, k_lens=k_lens)
     kv = inp["kv"]
     kd = to_device(kv, DEV)
-    cache = fk.KVCache.empty(kv.num_blocks, 16, Hkv, 128, device=DEV, fill=0x7F)
-    fk.kv_store_e4m3(cache, kd.k, kd.v, kd.slot_mapping, 1.0, 1.0)
+    sq, sk, sv = scales
+    cache = fk.KVCache.empty(kv.num_blocks, bs, Hkv, 128, device=DEV, fill=0x7F)
+    fk.kv_store_e4m3(cache, kd.k, kd.v, kd.slot_mapping, sk, sv)
     q, cu = inp["q"].to(DEV), inp["cu_seqlens_q"].to(DEV)
     rel = None if inp["rel"] is None else inp["rel"].to(DEV)
     outs = []
@@ -115,7 +117,7 @@ def _prefill_at_caps(fk, q_lens, k_lens, caps, window=0, E=128, Hq=8, Hkv=2, see
         for cap in caps:
             fk.set_prefill_max_ctas(cap)
             outs.append(fk.attn_fp8_varlen_prefill(cache, q, cu, kd.seq_lens, kd.block_table,
-                                                   max(q_lens), 1.0, 1.0, 1.0, rel_bias=rel,
+                                                   max(q_lens), sq, sk, sv, rel_bias=rel,
                                                    window=window))
             torch.cuda.synchronize()
             assert fk.device_error() == 0
@@ -144,6 +146,41 @@ def test_persistent_schedule_does_not_change_results(fk, window):
     ref = oracle_prefill_rows(inp, rows, 1.0, 1.0, 1.0, window=window, rel=inp["rel"])
     got = outs[0].float().cpu().numpy()
     assert_close(np.stack([got[t, h] for t, h in rows]), ref, "persistent prefill")
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_batches_at_several_grids(fk, seed):
+    """Random small batches (empty query runs, cached prefixes, windows, GQA
+    ratios, block sizes, bias extents, non-power-of-two scales): output
+    bit-identical at 0 (one CTA per SM), 1 and 3 CTAs, sampled rows against
+    the oracle."""
+    rng = np.random.default_rng(100 + seed)
+    B = int(rng.integers(1, 7))
+    q_lens = [int(x) for x in rng.choice([0, 1, 5, 127, 128, 129, 200, 256, 300, 513], B)]
+    if max(q_lens) == 0:
+        q_lens[0] = 70
+    k_lens = [q + int(rng.choice([0, 0, 1, 64, 250])) for q in q_lens]
+    Hkv = int(rng.choice([1, 2]))
+    Hq = Hkv * int(rng.choice([1, 3, 8]))
+    bs = int(rng.choice([16, 32, 64]))
+    window = int(rng.choice([0, 0, 100, 512]))
+    E = int(rng.choice([0, 128, 1024]))
+    scales = (float(rng.choice([1.0, 0.75])), float(rng.choice([1.0, 0.3])),
+              float(rng.choice([1.0, 2.5])))
+    inp, outs = _prefill_at_caps(fk, q_lens, k_lens, [0, 1, 3], window=window, E=E, Hq=Hq,
+                                 Hkv=Hkv, seed=seed, bs=bs, scales=scales)
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+    cu = inp["cu_seqlens_q"].tolist()
+    rows = []
+    for b, n in enumerate(q_lens):
+        if n == 0:
+            continue
+        picks = {0, n - 1, 127, 128} | set(int(x) for x in rng.integers(0, n, 4))
+        rows += [(cu[b] + i, int(rng.integers(Hq))) for i in sorted(picks) if 0 <= i < n]
+    ref = oracle_prefill_rows(inp, rows, *scales, window=window, rel=inp["rel"])
+    got = outs[0].float().cpu().numpy()
+    assert_close(np.stack([got[t, h] for t, h in rows]), ref, "random prefill %d" % seed)
 
 
 def test_many_sequences_one_cta_per_item(fk):
