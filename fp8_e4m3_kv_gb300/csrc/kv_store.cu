@@ -125,16 +125,56 @@ int grid_for(int64_t work_items, int num_sms) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Band counters of one stream at one scale: the quotient and code of
-// quantize16, then per element the finite / non-zero / clipped / flushed
-// counts and the relative round-trip error (summed in fp32 over a thread's
-// 16 elements, then in fp64).  A flushed element decodes to 0, so its error
-// term is exactly 1; any other non-zero element's term uses the fast
-// division (a few ulp).  One 64-bit atomic per counter and block.
+// Band counts of two elements (one bf16 word, a = low half): their quotients
+// and codes as quantize16 makes them, the finite / non-zero / clipped /
+// flushed counts, and the relative round-trip errors added to e.  The error
+// |s dec(c) - x| / |x| is taken in the quotient's domain, |dec(c) - q| / |q|
+// (q = x / s; the two are equal in exact arithmetic and q carries one
+// rounding), which keeps the fast division in range without rescaling:
+// |q| >= 2^-10 for an element that is not flushed, and a quotient beyond
+// 2^100 (an overflowed one included) counts as 2^100.  A flushed element
+// decodes to 0, so its term is exactly 1.
+template <bool kPow2>
+__device__ __forceinline__ void band_pair(uint32_t wd, const QScale &s, uint32_t &n_fin,
+                                          uint32_t &n_nz, uint32_t &n_clip, uint32_t &n_flush,
+                                          float &e) {
+    const float xa = __uint_as_float(wd << 16), xb = __uint_as_float(wd & 0xFFFF0000u);
+    const bool fa = (wd & 0x7F80u) != 0x7F80u;             // not NaN or +-Inf
+    const bool fb = (wd & 0x7F800000u) != 0x7F800000u;
+    const bool za = fa && (wd & 0x7FFFu) != 0u;
+    const bool zb = fb && (wd & 0x7FFF0000u) != 0u;
+    float qa, qb;
+    if (kPow2) {
+        const float2 q = __fmul2_rn(make_float2(xa, xb), make_float2(s.inv, s.inv));
+        qa = q.x;
+        qb = q.y;
+    } else {
+        qa = __fdiv_rn(xa, s.scale);
+        qb = __fdiv_rn(xb, s.scale);
+    }
+    const uint32_t code = f32x2_to_e4m3x2(qa, qb);
+    const float2 d = __half22float2(e4m3x2_to_half2(static_cast<uint16_t>(code)));
+    const bool la = za && (code & 0x7Fu) == 0u;
+    const bool lb = zb && (code & 0x7F00u) == 0u;
+    const float aa = fabsf(qa), ab = fabsf(qb);
+    n_fin += static_cast<uint32_t>(fa) + static_cast<uint32_t>(fb);
+    n_nz += static_cast<uint32_t>(za) + static_cast<uint32_t>(zb);
+    n_clip += static_cast<uint32_t>(za && aa > kE4M3Max) + static_cast<uint32_t>(zb && ab > kE4M3Max);
+    n_flush += static_cast<uint32_t>(la) + static_cast<uint32_t>(lb);
+    const float ca = fminf(aa, 0x1p100f), cb = fminf(ab, 0x1p100f);
+    e += la ? 1.0f : (za ? __fdividef(fabsf(fabsf(d.x) - ca), ca) : 0.0f);
+    e += lb ? 1.0f : (zb ? __fdividef(fabsf(fabsf(d.y) - cb), cb) : 0.0f);
+}
+
+// Band counters of one stream at one scale (band_pair over every stored
+// element); the error terms are summed in fp32 over a thread's 16 elements,
+// then in fp64.  chunk_shift is log2 of the chunks per row when that is a
+// power of two, else -1.  One 64-bit atomic per counter and block.
 template <bool kPow2>
 __global__ void __launch_bounds__(kStoreThreads)
 kv_band_kernel(const uint16_t *__restrict__ x, int64_t stride, const int64_t *__restrict__ slots,
-               int64_t num_tokens, int32_t row_elems, const QScale s, fp8kv_band_counts *out) {
+               int64_t num_tokens, int32_t row_elems, int32_t chunk_shift, const QScale s,
+               fp8kv_band_counts *out) {
     __shared__ unsigned long long red_n[4][kStoreThreads / 32];
     __shared__ double red_e[kStoreThreads / 32];
     const int32_t chunks = row_elems / kChunk;
@@ -143,7 +183,7 @@ kv_band_kernel(const uint16_t *__restrict__ x, int64_t stride, const int64_t *__
     double err = 0.0;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t t = i / chunks;
+        const int64_t t = chunk_shift >= 0 ? (i >> chunk_shift) : i / chunks;
         const int32_t c = static_cast<int32_t>(i - t * chunks);
         if (slots && __ldg(slots + t) < 0) continue;
         const uint4 *p = reinterpret_cast<const uint4 *>(x + t * stride + c * kChunk);
@@ -151,25 +191,7 @@ kv_band_kernel(const uint16_t *__restrict__ x, int64_t stride, const int64_t *__
         const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
         float e16 = 0.0f;
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            const uint32_t bits = (w[k >> 1] >> (16 * (k & 1))) & 0xFFFFu;
-            const bool fin = (bits & 0x7F80u) != 0x7F80u;       // not NaN or +-Inf
-            const bool nz = fin && (bits & 0x7FFFu) != 0;
-            const float xf = __uint_as_float(bits << 16);
-            const float q = kPow2 ? xf * s.inv : __fdiv_rn(xf, s.scale);
-            const uint16_t code = f32x2_to_e4m3x2(q, 0.0f) & 0xFFu;
-            const bool flushed = nz && (code & 0x7Fu) == 0;
-            const float back = __low2float(e4m3x2_to_half2(code)) * s.scale;
-            c_fin += fin;
-            c_nz += nz;
-            c_clip += nz && fabsf(q) > kE4M3Max;
-            c_flush += flushed;
-            // the fast division wants its divisor within 2^-126 .. 2^126:
-            // move both operands by the same power of two first
-            const float ax = fabsf(xf);
-            const float f = ax > 0x1p64f ? 0x1p-64f : (ax < 0x1p-64f ? 0x1p64f : 1.0f);
-            e16 += flushed ? 1.0f : (nz ? __fdividef(fabsf(back - xf) * f, ax * f) : 0.0f);
-        }
+        for (int k = 0; k < 8; ++k) band_pair<kPow2>(w[k], s, c_fin, c_nz, c_clip, c_flush, e16);
         err += static_cast<double>(e16);
     }
     unsigned long long n_fin = c_fin, n_nz = c_nz, n_clip = c_clip, n_flush = c_flush;
@@ -357,11 +379,16 @@ extern "C" fp8kv_status kv_band_counts(const fp8kv_bf16 *x, int64_t tok_stride,
     int sms = 0;
     fp8kv_status st = check_device(&sms);
     if (st != FP8KV_OK) return st;
-    const int grid = grid_for(num_tokens * (row_elems / kChunk), sms);
+    const int32_t chunks = row_elems / kChunk;
+    int32_t chunk_shift = -1;
+    if ((chunks & (chunks - 1)) == 0)
+        for (chunk_shift = 0; (1 << chunk_shift) < chunks; ++chunk_shift) {
+        }
+    const int grid = grid_for(num_tokens * chunks, sms);
     const QScale qs = make_qscale(scale);
     auto kernel = qs.pow2 ? kv_band_kernel<true> : kv_band_kernel<false>;
     kernel<<<grid, kStoreThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        x, tok_stride, slot_mapping, num_tokens, row_elems, qs, counts);
+        x, tok_stride, slot_mapping, num_tokens, row_elems, chunk_shift, qs, counts);
     if (cudaGetLastError() != cudaSuccess) return FP8KV_ERR_LAUNCH;
     return FP8KV_OK;
 }
