@@ -504,8 +504,16 @@ def main():
     ap.add_argument("--profile-prefill", type=int, default=0, metavar="GROUP",
                     help="profiling case: only the prefill call of group GROUP-1 (1 = the "
                          "causal sequences, 2 = the 512-window ones) of the prefill chunk")
+    ap.add_argument("--profile-store", action="store_true",
+                    help="profiling case: only the quant-on-store of the 64-sequence pool and the "
+                         "band counters over its V, no JSON contract line")
     args = ap.parse_args()
     rank, world = dist_setup(args.gpus)
+    if args.profile_store:
+        import fp8_e4m3_kv_gb300 as fk
+        dev = torch.device("cuda", torch.cuda.current_device())
+        print(json.dumps(bench_store_and_bands(fk, dev, args.steps, args.warmup, world)))
+        return
     if args.profile_prefill:
         import fp8_e4m3_kv_gb300 as fk
         dev = torch.device("cuda", torch.cuda.current_device())
