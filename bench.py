@@ -421,7 +421,7 @@ def bench_chunked_prefill(fk, dev, steps, warmup, world):
 
 
 def bench_store_and_bands(fk, dev, steps, warmup, world):
-    """Quant-on-store of the whole 64-sequence pool (1.08M tokens) and the band
+    """Quant-on-store of the whole 64-sequence pool (~1.05-1.1M tokens) and the band
     counters over its V, each against the measured HBM bandwidth."""
     spec = workloads.DECODE_32K
     inp = workloads.make_decode(spec, device=dev, seed=0)

@@ -121,7 +121,7 @@ def test_amax_exact_with_skips_nan_and_running_max(fk):
 
 
 def test_store_at_decode_pool_size(fk):
-    """The cache fill of the 64-sequence decode workload (~1.08M tokens, the
+    """The cache fill of the 64-sequence decode workload (~1.05M tokens, the
     store launch the bench makes before timing), sampled tokens checked."""
     spec = workloads.DECODE_32K
     inp = workloads.make_decode(spec, device=DEV, seed=0)
