@@ -165,3 +165,97 @@ def test_band_counts_rejects_bad_arguments_on_host(lib):
     assert f(8, 128, None, 4, 128, 1.0, 16, None) == lib.ERR_ARG             # x not 16-byte aligned
     assert f(16, 128, None, 4, 128, 1.0, 12, None) == lib.ERR_ARG            # counts not 8-byte aligned
     assert f(16, 128, None, 4, 128, 1.0, None, None) == lib.ERR_ARG
+
+
+def _prefill(lib, cache, **kw):
+    a = dict(q=16, Hq=8, cu=16, lk=16, bt=16, mb=4, B=1, maxq=16, qs=1.0, ks=1.0, vs=1.0, sm=0.1,
+             rel=None, bstride=0, E=0, window=0, out=16, ws=None, wsb=0)
+    a.update(kw)
+    return _c(lib).attn_fp8_varlen_prefill(
+        ctypes.byref(cache) if cache is not None else None, a["q"], a["Hq"], a["cu"], a["lk"],
+        a["bt"], a["mb"], a["B"], a["maxq"], a["qs"], a["ks"], a["vs"], a["sm"], a["rel"],
+        a["bstride"], a["E"], a["window"], a["out"], a["ws"], a["wsb"], None)
+
+
+def test_prefill_rejects_bad_arguments_on_host(lib):
+    cache = lib.CacheStruct(16, 16, 4, 16, 2, 128)   # fake pointers, never dereferenced
+    assert _prefill(lib, None) == lib.ERR_ARG
+    for k in ("qs", "ks", "vs", "sm"):
+        for bad in (float("nan"), 0.0, -1.0, float("inf")):
+            assert _prefill(lib, cache, **{k: bad}) == lib.ERR_SCALE
+    assert _prefill(lib, cache, B=-1) == lib.ERR_ARG
+    assert _prefill(lib, cache, Hq=0) == lib.ERR_ARG
+    assert _prefill(lib, cache, Hq=7) == lib.ERR_ARG                 # not a multiple of Hkv
+    assert _prefill(lib, cache, mb=0) == lib.ERR_ARG
+    assert _prefill(lib, cache, window=-1) == lib.ERR_ARG
+    assert _prefill(lib, cache, maxq=-1) == lib.ERR_ARG
+    assert _prefill(lib, lib.CacheStruct(16, 16, 4, 16, 2, 64)) == lib.ERR_UNSUPPORTED   # D 64
+    assert _prefill(lib, lib.CacheStruct(16, 16, 4, 8, 2, 128)) == lib.ERR_UNSUPPORTED   # bs 8
+    assert _prefill(lib, cache, rel=16, E=0) == lib.ERR_ARG
+    assert _prefill(lib, cache, rel=16, E=128, bstride=-1) == lib.ERR_ARG
+    assert _prefill(lib, cache, B=0) == lib.OK                       # nothing to do
+    assert _prefill(lib, cache, maxq=0) == lib.OK
+    assert _prefill(lib, cache, q=None) == lib.ERR_ARG
+    assert _prefill(lib, cache, cu=None) == lib.ERR_ARG
+    assert _prefill(lib, cache, q=8) == lib.ERR_ARG                  # q not 16-byte aligned
+    assert _prefill(lib, cache, out=8) == lib.ERR_ARG
+
+
+def _decode_store(lib, cache, **kw):
+    a = dict(q=16, Hq=8, kn=16, vn=16, bt=16, mb=4, lens=16, B=1, qs=1.0, ks=1.0, vs=1.0, sm=0.1,
+             rel=None, bstride=0, E=0, window=0, ak=None, av=None, out=16, ws=16, wsb=1 << 20)
+    a.update(kw)
+    return _c(lib).paged_attn_fp8_decode_store(
+        ctypes.byref(cache), a["q"], a["Hq"], a["kn"], a["vn"], a["bt"], a["mb"], a["lens"],
+        a["B"], a["qs"], a["ks"], a["vs"], a["sm"], a["rel"], a["bstride"], a["E"], a["window"],
+        a["ak"], a["av"], a["out"], a["ws"], a["wsb"], None)
+
+
+def test_decode_store_rejects_bad_arguments_on_host(lib):
+    cache = lib.CacheStruct(16, 16, 4, 16, 2, 128)
+    assert _decode_store(lib, cache, kn=None) == lib.ERR_ARG
+    assert _decode_store(lib, cache, vn=None) == lib.ERR_ARG
+    assert _decode_store(lib, cache, kn=8) == lib.ERR_ARG            # not 16-byte aligned
+    assert _decode_store(lib, cache, ak=2) == lib.ERR_ARG            # amax not 4-byte aligned
+    assert _decode_store(lib, cache, ks=float("nan")) == lib.ERR_SCALE
+    assert _decode_store(lib, cache, B=0, kn=None, vn=None) == lib.OK
+
+
+def test_per_token_calls_reject_bad_arguments_on_host(lib):
+    L = _c(lib)
+    cache = lib.CacheStruct(16, 16, 4, 16, 2, 128)                   # row = Hkv * D = 256
+    st = L.kv_store_e4m3_per_token   # (cache, k, v, k_stride, v_stride, slots, T, k_sc, v_sc, s)
+    assert st(None, 16, 16, 256, 256, 16, 1, 16, 16, None) == lib.ERR_ARG
+    assert st(ctypes.byref(cache), 16, 16, 256, 256, 16, -1, 16, 16, None) == lib.ERR_ARG
+    d64 = lib.CacheStruct(16, 16, 4, 16, 2, 64)
+    assert st(ctypes.byref(d64), 16, 16, 128, 128, 16, 1, 16, 16, None) == lib.ERR_UNSUPPORTED
+    assert st(ctypes.byref(cache), 16, 16, 256, 256, 16, 0, 16, 16, None) == lib.OK
+    assert st(ctypes.byref(cache), 16, 16, 256, 256, 16, 1, None, 16, None) == lib.ERR_ARG
+    assert st(ctypes.byref(cache), 16, 16, 256, 256, None, 1, 16, 16, None) == lib.ERR_ARG
+    assert st(ctypes.byref(cache), 16, 16, 256, 256, 16, 1, 18, 16, None) == lib.ERR_ARG  # align 4
+    assert st(ctypes.byref(cache), 16, 16, 128, 256, 16, 1, 16, 16, None) == lib.ERR_ARG  # stride
+    assert st(ctypes.byref(cache), 8, 16, 256, 256, 16, 1, 16, 16, None) == lib.ERR_ARG   # align 16
+    dec = L.paged_attn_fp8_decode_per_token
+    # (cache, q, Hq, bt, mb, lens, B, q_scale, softmax_scale, k_sc, v_sc, rel, bstride, E,
+    #  window, out, ws, ws_bytes, stream)
+    args = [ctypes.byref(cache), 16, 8, 16, 4, 16, 1, 1.0, 0.1, 16, 16, None, 0, 0, 0, 16, 16,
+            1 << 20, None]
+    for i, bad in ((9, None), (10, None), (9, 18), (7, float("nan")), (8, 0.0)):
+        a = list(args)
+        a[i] = bad
+        assert dec(*a) == (lib.ERR_SCALE if i in (7, 8) else lib.ERR_ARG), (i, bad)
+    a = list(args)
+    a[6], a[9], a[10] = 0, None, None
+    assert dec(*a) == lib.OK                                           # nothing to do
+
+
+def test_amax_rejects_bad_arguments_on_host(lib):
+    f = _c(lib).kv_amax_calibrate   # (k, v, k_stride, v_stride, slots, T, Hkv, D, amax_k, amax_v, s)
+    assert f(16, 16, 256, 256, None, -1, 2, 128, 16, 16, None) == lib.ERR_ARG
+    assert f(16, 16, 256, 256, None, 1, 0, 128, 16, 16, None) == lib.ERR_ARG
+    assert f(16, 16, 256, 256, None, 1, 2, 100, 16, 16, None) == lib.ERR_UNSUPPORTED  # row % 16
+    assert f(16, None, 256, 256, None, 1, 2, 128, None, None, None) == lib.ERR_ARG    # no amax_k
+    assert f(16, None, 128, 256, None, 1, 2, 128, 16, None, None) == lib.ERR_ARG      # stride < row
+    assert f(8, None, 256, 256, None, 1, 2, 128, 16, None, None) == lib.ERR_ARG       # align 16
+    assert f(None, None, 256, 256, None, 1, 2, 128, None, None, None) == lib.OK       # nothing to do
+    assert f(16, 16, 256, 256, None, 0, 2, 128, 16, 16, None) == lib.OK
