@@ -95,6 +95,34 @@ def test_bias_with_extreme_scales(fk):
              seed=9)
 
 
+def test_bias_broadcast_over_tokens(fk):
+    """One bias table per head for every query token (token stride 0), the
+    form a learned per-head relative-position table takes; every row against
+    the oracle."""
+    q_lens, k_lens, Hq, Hkv, E = [300, 129], [300, 400], 8, 2, 128
+    spec = workloads.PrefillSpec("case", q_lens=q_lens, q_lo=0, q_hi=0, n_seqs=2, Hq=Hq, Hkv=Hkv,
+                                 D=128, block_size=16, rel_extent=E)
+    inp = workloads.make_prefill(spec, device="cpu", seed=13, q_lens=q_lens, k_lens=k_lens)
+    T = sum(q_lens)
+    table = inp["rel"][:1]
+    inp["rel"] = table.expand(T, Hq, E)
+    kv = inp["kv"]
+    kd = to_device(kv, DEV)
+    cache = fk.KVCache.empty(kv.num_blocks, 16, Hkv, 128, device=DEV, fill=0x7F)
+    fk.kv_store_e4m3(cache, kd.k, kd.v, kd.slot_mapping, 1.0, 1.0)
+    rel_d = table.to(DEV).expand(T, Hq, E)
+    assert rel_d.stride(0) == 0
+    out = fk.attn_fp8_varlen_prefill(cache, inp["q"].to(DEV), inp["cu_seqlens_q"].to(DEV),
+                                     kd.seq_lens, kd.block_table, max(q_lens), 1.0, 1.0, 1.0,
+                                     rel_bias=rel_d)
+    torch.cuda.synchronize()
+    assert fk.device_error() == 0
+    rows = [(t, h) for t in range(T) for h in range(Hq)]
+    ref = oracle_prefill_rows(inp, rows, 1.0, 1.0, 1.0, rel=inp["rel"])
+    got = out.float().cpu().numpy()
+    assert_close(np.stack([got[t, h] for t, h in rows]), ref, "broadcast bias")
+
+
 def test_heavy_bias(fk):
     run_case(fk, [400], E=512, bias_std=3.0, seed=8)
 
