@@ -301,10 +301,13 @@ def e2e_decode(run, steps, warmup, world):
 # ---------------------------------------------------------------------------
 # CPU oracle baseline (bounded sample)
 # ---------------------------------------------------------------------------
-def oracle_decode_sample(spec, inp, scales, budget_s=15.0):
+def oracle_decode_sample(spec, inp, scales, budget_s=15.0, max_keys=None):
     """Time the oracle on whole sequences of the workload (all heads), one
     after another, until about budget_s of CPU work; returns GB/s over the
-    sample's KV bytes and a description."""
+    sample's KV bytes and a description.  With max_keys, a longer sequence is
+    cut to its first max_keys keys (a decode of that shorter sequence: same
+    heads, bias and window, the query at its last kept key); the oracle's
+    cost is linear in the keys, so GB/s carries over to the full lengths."""
     import oracle
     bits = workloads.bf16_bits
     kv = inp["kv"]
@@ -315,9 +318,8 @@ def oracle_decode_sample(spec, inp, scales, budget_s=15.0):
     lens = inp["lens"]
     starts = kv.tok_start.cpu().tolist()
     done_bytes, t_total, seqs = 0, 0.0, 0
-    order = list(range(B))
-    for b in order:
-        L = lens[b]
+    for b in range(B):
+        L = lens[b] if max_keys is None else min(lens[b], max_keys)
         L_used = min(L, spec.window) if spec.window else L
         kb = bits(kv.k[starts[b]:starts[b] + L])
         vb = bits(kv.v[starts[b]:starts[b] + L])
@@ -342,10 +344,78 @@ def oracle_decode_sample(spec, inp, scales, budget_s=15.0):
     return done_bytes / t_total / 1e9, seqs, t_total, oracle.num_threads()
 
 
+def cpu_line(value, unit, cores, sample):
+    return {"value": value, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample}
+
+
+def oracle_decode_baseline(spec, inp, scales, budget_s, max_keys=None):
+    gbs, seqs, t, cores = oracle_decode_sample(spec, inp, scales, budget_s, max_keys)
+    cut = "" if max_keys is None else ", each cut to its first %d keys" % max_keys
+    return cpu_line(gbs, "GB/s", cores, "%d sequence(s) of the workload (all %d q heads, float64)%s,"
+                    " %.1f s of CPU time; GB/s over the sample's KV bytes" % (seqs, spec.Hq, cut, t))
+
+
+def oracle_prefill_baseline(spec, inp, groups, budget_s, seed=0):
+    """The oracle on the prefill chunk: the quantization of every sequence's K
+    and V (timed in full), then query rows drawn from every sequence and head
+    (each quantized and attended over all its visible keys) until about
+    budget_s of CPU time.  The time of the whole chunk is extrapolated as
+    quantization + (row time) x (all rows / rows done); TFLOP/s is the
+    chunk's visible-pair FLOPs over that time."""
+    import oracle
+    bits = workloads.bf16_bits
+    kv = inp["kv"]
+    D, Hq, Hkv = spec.D, spec.Hq, spec.Hkv
+    G = Hq // Hkv
+    rng = np.random.default_rng(seed)
+    cu = inp["cu_seqlens_q"].tolist()
+    starts = kv.tok_start.cpu().tolist()
+    t_quant, codes = 0.0, {}
+    for b, _ in groups:
+        kn = inp["k_lens"][b]
+        kb = bits(kv.k[starts[b]:starts[b] + kn])
+        vb = bits(kv.v[starts[b]:starts[b] + kn])
+        t0 = time.perf_counter()
+        codes[b] = (oracle.quantize(kb, 1.0), oracle.quantize(vb, 1.0))
+        t_quant += time.perf_counter() - t0
+    t_rows, rows_done, rows_all, flops_all = 0.0, 0, 0, 0
+    for b, w in groups:
+        qn, kn = inp["q_lens"][b], inp["k_lens"][b]
+        rows_all += qn * Hq
+        flops_all += Hq * sum(4 * D * (min(kn - qn + i + 1, w) if w else kn - qn + i + 1)
+                              for i in range(qn))
+    while t_rows < budget_s:
+        for b, w in groups:
+            qn, kn = inp["q_lens"][b], inp["k_lens"][b]
+            ts = rng.integers(0, qn, 8)
+            hs = rng.integers(0, Hq, 8)
+            qb = np.stack([bits(inp["q"][cu[b] + int(t), int(h)]) for t, h in zip(ts, hs)])
+            relb = None if inp["rel"] is None else np.stack(
+                [bits(inp["rel"][cu[b] + int(t), int(h)]) for t, h in zip(ts, hs)])
+            E = 0 if relb is None else relb.shape[-1]
+            n = len(ts)
+            k8, v8 = codes[b]
+            t0 = time.perf_counter()
+            q8 = oracle.quantize(qb, 1.0)
+            oracle.attend_rows(D, q8, np.arange(n, dtype=np.int64) * D, k8, v8,
+                               (hs // G).astype(np.int64) * D, Hkv * D, [kn] * n,
+                               [kn - qn + int(t) for t in ts], 1 / math.sqrt(D), 1.0, 1.0, 1.0,
+                               relb, None if relb is None else np.arange(n, dtype=np.int64) * E,
+                               E, w)
+            t_rows += time.perf_counter() - t0
+            rows_done += n
+    t_est = t_quant + t_rows * rows_all / rows_done
+    return cpu_line(flops_all / t_est / 1e12, "TFLOP/s", oracle.num_threads(),
+                    "K/V quantization of every sequence (%.1f s) plus %d of the chunk's %d query "
+                    "rows drawn from every sequence and head (%.1f s, float64, each over all its "
+                    "visible keys); whole-chunk time extrapolated linearly in rows: %.0f s"
+                    % (t_quant, rows_done, rows_all, t_rows, t_est))
+
+
 # ---------------------------------------------------------------------------
 # secondary workloads
 # ---------------------------------------------------------------------------
-def bench_prefill(fk, dev, steps, warmup, world, only_group=None):
+def bench_prefill(fk, dev, steps, warmup, world, only_group=None, cpu_budget=0.0):
     spec = workloads.PREFILL_16K
     inp = workloads.make_prefill(spec, device=dev, seed=0)
     kv = inp["kv"]
@@ -387,16 +457,40 @@ def bench_prefill(fk, dev, steps, warmup, world, only_group=None):
     except Exception as e:  # noqa: BLE001
         return {"workload": spec.name, "unavailable": str(e)}
     ms = time_steps(step, steps, warmup, world)
+    # each group alone (causal, 512-window), the store of the chunk included
+    # in neither
+    per_group = []
+    if only_group is None:
+        fk.kv_store_e4m3(cache, kv.k, kv.v, kv.slot_mapping, 1.0, 1.0)
+        for gi, (lo, hi) in enumerate([(0, half), (half, spec.n_seqs)]):
+            w = spec.windows[gi]
+            g = groups[gi]
+            gf = 4 * spec.Hq * spec.D * sum(
+                sum(min(i + 1, w) if w else i + 1 for i in range(L)) for L in q_lens[lo:hi])
+
+            def one(g=g):
+                fk.attn_fp8_varlen_prefill(cache, g["q"], g["cu"], g["lens"], g["bt"], g["maxq"],
+                                           1.0, 1.0, 1.0, rel_bias=g["rel"], window=g["window"],
+                                           out=g["out"])
+            gms = time_steps(one, steps, warmup, world)
+            per_group.append({"window": w, "ms": gms, "tflops": gf / gms / 1e9})
     pk = peaks()
     fp8_peak = 2.0 * pk["bf16_tflops"]      # nominal fp8 : bf16 dense ratio of 2
-    return {"workload": spec.name, "ms_per_step": ms, "tflops": flops / ms / 1e9,
-            "roofline": {"bound": "tensor", "achieved": flops / ms / 1e9, "peak": fp8_peak,
-                         "unit": "TFLOP/s", "frac": flops / ms / 1e9 / fp8_peak,
-                         "peak_source": "2 x %s bf16 burst" % pk["source"]},
-            "flops_per_step": flops, "tokens": sum(q_lens)}
+    res = {"workload": spec.name, "ms_per_step": ms, "tflops": flops / ms / 1e9,
+           "roofline": {"bound": "tensor", "achieved": flops / ms / 1e9, "peak": fp8_peak,
+                        "unit": "TFLOP/s", "frac": flops / ms / 1e9 / fp8_peak,
+                        "peak_source": "2 x %s bf16 burst" % pk["source"]},
+           "flops_per_step": flops, "tokens": sum(q_lens),
+           "step": "kv_store_e4m3 of the chunk, then one prefill call per group",
+           "groups": per_group}
+    if cpu_budget > 0:
+        res["cpu_baseline"] = oracle_prefill_baseline(
+            spec, inp, [(b, spec.windows[0 if b < half else 1]) for b in range(spec.n_seqs)],
+            cpu_budget)
+    return res
 
 
-def bench_chunked_prefill(fk, dev, steps, warmup, world):
+def bench_chunked_prefill(fk, dev, steps, warmup, world, cpu_budget=0.0):
     """One 4,096-query chunk attending over 65,536 keys (a cached prefix)."""
     spec = workloads.PREFILL_CHUNK_64K
     inp = workloads.make_prefill(spec, device=dev, seed=0)
@@ -415,12 +509,15 @@ def bench_chunked_prefill(fk, dev, steps, warmup, world):
                                    window=0, out=out)
     ms = time_steps(step, steps, warmup, world)
     fp8_peak = 2.0 * peaks()["bf16_tflops"]
-    return {"workload": spec.name, "ms_per_step": ms, "tflops": flops / ms / 1e9,
-            "roofline": {"bound": "tensor", "achieved": flops / ms / 1e9, "peak": fp8_peak,
-                         "unit": "TFLOP/s", "frac": flops / ms / 1e9 / fp8_peak}}
+    res = {"workload": spec.name, "ms_per_step": ms, "tflops": flops / ms / 1e9,
+           "roofline": {"bound": "tensor", "achieved": flops / ms / 1e9, "peak": fp8_peak,
+                        "unit": "TFLOP/s", "frac": flops / ms / 1e9 / fp8_peak}}
+    if cpu_budget > 0:
+        res["cpu_baseline"] = oracle_prefill_baseline(spec, inp, [(0, 0)], cpu_budget)
+    return res
 
 
-def bench_store_and_bands(fk, dev, steps, warmup, world):
+def bench_store_and_bands(fk, dev, steps, warmup, world, cpu_budget=0.0):
     """Quant-on-store of the whole 64-sequence pool (~1.05-1.1M tokens) and the band
     counters over its V, each against the measured HBM bandwidth."""
     spec = workloads.DECODE_32K
@@ -442,10 +539,48 @@ def bench_store_and_bands(fk, dev, steps, warmup, world):
         res.append({"workload": name, "ms_per_step": ms, "gbs": gbs,
                     "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
                                  "frac": gbs / hbm}})
+    if cpu_budget > 0:
+        res[0]["cpu_baseline"], res[1]["cpu_baseline"] = oracle_store_band_baselines(
+            kv, spec, cpu_budget)
     return res
 
 
-def bench_decode_per_token(fk, dev, steps, warmup, world):
+def oracle_store_band_baselines(kv, spec, budget_s):
+    """The oracle's store (quantize and scatter, K and V) and band counters
+    (over V at scale 3) on the pool's first tokens, in chunks of 4,096 tokens
+    until about budget_s of CPU time each; GB/s over the same algorithmic
+    bytes as the GPU lines (3 bytes per stored element, 2 per counted one)."""
+    import oracle
+    bits = workloads.bf16_bits
+    cores = oracle.num_threads()
+    row = spec.Hkv * spec.D
+    ck = np.zeros((kv.num_blocks, spec.Hkv, kv.block_size, spec.D), dtype=np.uint8)
+    cv = np.zeros_like(ck)
+    out = []
+    for what in ("store", "bands"):
+        t_total, tokens, c0 = 0.0, 0, 0
+        while t_total < budget_s and c0 < kv.k.shape[0]:
+            c1 = min(c0 + 4096, kv.k.shape[0])
+            vb = bits(kv.v[c0:c1])
+            if what == "store":
+                kb = bits(kv.k[c0:c1])
+                sm = kv.slot_mapping[c0:c1].cpu().numpy()
+                t0 = time.perf_counter()
+                oracle.kv_store(ck, cv, kb, vb, sm, 1.0, 3.0, kv.block_size)
+            else:
+                t0 = time.perf_counter()
+                oracle.band_counts(vb, 3.0)
+            t_total += time.perf_counter() - t0
+            tokens += c1 - c0
+            c0 = c1
+        nbytes = tokens * row * (2 * 3 if what == "store" else 2)
+        out.append(cpu_line(nbytes / t_total / 1e9, "GB/s", 1,
+                            "the pool's first %d tokens (%s), %.1f s of CPU time, one thread" %
+                            (tokens, "K and V" if what == "store" else "V", t_total)))
+    return out
+
+
+def bench_decode_per_token(fk, dev, steps, warmup, world, cpu_budget=0.0):
     """The 64-sequence decode over a cache with per-token scales (written by
     kv_store_e4m3_per_token): KV bytes plus 4 bytes of K and V scale per key
     and KV head."""
@@ -470,18 +605,64 @@ def bench_decode_per_token(fk, dev, steps, warmup, world):
     ms = time_steps(step, steps, warmup, world)
     gbs = nbytes / ms / 1e6
     hbm = peaks()["hbm_gbs"]
-    return {"workload": spec.name + "_per_token_scales", "ms_per_step": ms, "gbs": gbs,
-            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
-                         "frac": gbs / hbm}}
+    res = {"workload": spec.name + "_per_token_scales", "ms_per_step": ms, "gbs": gbs,
+           "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                        "frac": gbs / hbm}}
+    if cpu_budget > 0:
+        res["cpu_baseline"] = oracle_per_token_baseline(spec, inp, cpu_budget)
+    return res
 
 
-def bench_decode_extra(fk, spec, dev, steps, warmup, world, calibrate=False):
-    run = DecodeRun(fk, spec, dev, calibrate=calibrate)
+def oracle_per_token_baseline(spec, inp, budget_s):
+    """The oracle's per-token store and attention (or_quantize_per_token,
+    or_attend_row_pt) on whole sequences, one KV head at a time with its
+    query heads, until about budget_s of CPU time; GB/s over the sample's KV
+    and scale bytes."""
+    import oracle
+    bits = workloads.bf16_bits
+    kv = inp["kv"]
+    D, G = spec.D, spec.Hq // spec.Hkv
+    starts = kv.tok_start.cpu().tolist()
+    t_total, nbytes, units = 0.0, 0, 0
+    for b, L in enumerate(inp["lens"]):
+        for kvh in range(spec.Hkv):
+            kb = bits(kv.k[starts[b]:starts[b] + L, kvh])
+            vb = bits(kv.v[starts[b]:starts[b] + L, kvh])
+            qb = [bits(inp["q"][b, kvh * G + g]) for g in range(G)]
+            rb = [bits(inp["rel"][b, kvh * G + g]) for g in range(G)]
+            t0 = time.perf_counter()
+            k8, sk = oracle.quantize_per_token(kb, D)
+            v8, sv = oracle.quantize_per_token(vb, D)
+            for g in range(G):
+                oracle.attend_row_pt(oracle.quantize(qb[g], 1.0), k8, v8, sk, sv, L - 1,
+                                     1 / math.sqrt(D), 1.0, bias=rb[g])
+            t_total += time.perf_counter() - t0
+            nbytes += L * (2 * D + 8)
+            units += 1
+            if t_total >= budget_s:
+                return cpu_line(nbytes / t_total / 1e9, "GB/s", 1,
+                                "%d (sequence, KV head) pairs with their %d query heads, %.1f s of"
+                                " CPU time, one thread" % (units, G, t_total))
+    return cpu_line(nbytes / t_total / 1e9, "GB/s", 1, "%d (sequence, KV head) pairs, %.1f s" %
+                    (units, t_total))
+
+
+def bench_decode_extra(fk, spec, dev, steps, warmup, world, calibrate=False,
+                       scales=(1.0, 1.0, 1.0), label=None, cpu_budget=0.0, cpu_max_keys=None):
+    run = DecodeRun(fk, spec, dev, calibrate=calibrate, scales=scales)
     ms = time_steps(run.step, steps, warmup, world)
     dms = time_steps(run.decode, steps, warmup, world)
-    res = {"workload": spec.name, "ms_per_step": ms, "gbs": run.step_bytes / ms / 1e6,
-           "decode_ms": dms, "decode_gbs": run.decode_bytes / dms / 1e6,
-           "scales": list(run.scales)}
+    hbm = peaks()["hbm_gbs"]
+    dgbs = run.decode_bytes / dms / 1e6
+    res = {"workload": label or spec.name, "ms_per_step": ms, "gbs": run.step_bytes / ms / 1e6,
+           "decode_ms": dms, "decode_gbs": dgbs, "scales": list(run.scales),
+           "window": spec.window,
+           "roofline": {"bound": "hbm", "achieved": dgbs, "peak": hbm, "unit": "GB/s",
+                        "frac": dgbs / hbm, "frac_of_nominal_8tbs": dgbs / 8000.0,
+                        "kernel": "paged_attn_fp8_decode (decode + split merge)"}}
+    if cpu_budget > 0:
+        res["cpu_baseline"] = oracle_decode_baseline(spec, run.inp, run.scales, cpu_budget,
+                                                     cpu_max_keys)
     del run
     torch.cuda.empty_cache()
     return res
@@ -593,6 +774,7 @@ def main():
             "data": "synthetic", "config": cfg,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
                          "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
+                         "frac_of_nominal_8tbs": achieved / 8000.0,
                          "traffic": decode_traffic_bytes(),
                          "kernel": "paged_attn_fp8_decode (decode + split merge)",
                          "peak_source": pk["source"]},
@@ -610,16 +792,28 @@ def main():
     del run
     torch.cuda.empty_cache()
     if not args.no_extra:
+        import dataclasses
         extra = []
-        for fn in (lambda: bench_prefill(fk, dev, args.steps, args.warmup, world),
+        cb = 5.0 if (rank == 0 and not args.no_cpu) else 0.0   # CPU seconds per extra
+        for fn in (lambda: bench_prefill(fk, dev, args.steps, args.warmup, world, cpu_budget=cb),
                    lambda: bench_chunked_prefill(fk, dev, max(3, args.steps // 4), args.warmup,
-                                                 world),
-                   lambda: bench_store_and_bands(fk, dev, args.steps, args.warmup, world),
-                   lambda: bench_decode_per_token(fk, dev, args.steps, args.warmup, world),
+                                                 world, cpu_budget=cb),
+                   lambda: bench_store_and_bands(fk, dev, args.steps, args.warmup, world,
+                                                 cpu_budget=cb),
+                   lambda: bench_decode_per_token(fk, dev, args.steps, args.warmup, world,
+                                                  cpu_budget=cb),
+                   lambda: bench_decode_extra(fk, dataclasses.replace(spec, window=512), dev,
+                                              args.steps, args.warmup, world,
+                                              label=spec.name + "_window512", cpu_budget=cb),
+                   lambda: bench_decode_extra(fk, spec, dev, args.steps, args.warmup, world,
+                                              scales=(1.0, 1.0, 3.0),
+                                              label=spec.name + "_vscale3", cpu_budget=cb),
                    lambda: bench_decode_extra(fk, workloads.DECODE_128K_CAL, dev, args.steps,
-                                              args.warmup, world, calibrate=True),
+                                              args.warmup, world, calibrate=True, cpu_budget=cb,
+                                              cpu_max_keys=8192),
                    lambda: bench_decode_extra(fk, workloads.DECODE_1M, dev, args.steps,
-                                              args.warmup, world)):
+                                              args.warmup, world, cpu_budget=cb,
+                                              cpu_max_keys=65536)):
             try:
                 r = fn()
                 extra.extend(r if isinstance(r, list) else [r])

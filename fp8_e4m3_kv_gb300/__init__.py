@@ -243,6 +243,17 @@ def decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blo
                         block_size, window, split_tokens))
 
 
+def _table_and_lens(block_table: torch.Tensor, seq_lens: torch.Tensor, B: int, device):
+    """block_table int32 [B][max_blocks] and seq_lens int32 [B], contiguous, on
+    the cache's device: the kernels read them through raw device pointers."""
+    _need(block_table, torch.int32, "block_table", device)
+    _need(seq_lens, torch.int32, "seq_lens", device)
+    if block_table.dim() != 2 or block_table.shape[0] != B or not block_table.is_contiguous():
+        raise ValueError("block_table must be contiguous [B][max_blocks]")
+    if seq_lens.numel() != B or not seq_lens.is_contiguous():
+        raise ValueError("seq_lens must be contiguous [B]")
+
+
 def _bias_args(rel_bias, Hq):
     if rel_bias is None:
         return None, 0, 0
@@ -266,10 +277,7 @@ def paged_attn_fp8_decode(cache: KVCache, q: torch.Tensor, block_table: torch.Te
     if q.dim() != 3 or not q.is_contiguous() or q.shape[2] != cache.head_dim:
         raise ValueError("q must be contiguous [B][Hq][D]")
     B, Hq, D = q.shape
-    _need(block_table, torch.int32, "block_table", cache.device)
-    _need(seq_lens, torch.int32, "seq_lens", cache.device)
-    if block_table.dim() != 2 or block_table.shape[0] != B or not block_table.is_contiguous():
-        raise ValueError("block_table must be contiguous [B][max_blocks]")
+    _table_and_lens(block_table, seq_lens, B, cache.device)
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(D)
     rel, bstride, E = _bias_args(rel_bias, Hq)
@@ -324,10 +332,7 @@ def paged_attn_fp8_decode_per_token(cache: KVCache, q: torch.Tensor, block_table
         _need(t, torch.float32, name, cache.device)
         if tuple(t.shape) != shape or not t.is_contiguous():
             raise ValueError("%s must be contiguous float32 %s" % (name, shape))
-    _need(block_table, torch.int32, "block_table", cache.device)
-    _need(seq_lens, torch.int32, "seq_lens", cache.device)
-    if block_table.dim() != 2 or block_table.shape[0] != B or not block_table.is_contiguous():
-        raise ValueError("block_table must be contiguous [B][max_blocks]")
+    _table_and_lens(block_table, seq_lens, B, cache.device)
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(D)
     rel, bstride, E = _bias_args(rel_bias, Hq)
@@ -368,10 +373,7 @@ def paged_attn_fp8_decode_store(cache: KVCache, q: torch.Tensor, k_new: torch.Te
     for a in (amax_k, amax_v):
         if a is not None:
             _need(a, torch.float32, "amax", cache.device)
-    _need(block_table, torch.int32, "block_table", cache.device)
-    _need(seq_lens, torch.int32, "seq_lens", cache.device)
-    if block_table.dim() != 2 or block_table.shape[0] != B or not block_table.is_contiguous():
-        raise ValueError("block_table must be contiguous [B][max_blocks]")
+    _table_and_lens(block_table, seq_lens, B, cache.device)
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(D)
     rel, bstride, E = _bias_args(rel_bias, Hq)
@@ -396,11 +398,13 @@ def paged_attn_fp8_decode_noalloc(cache: KVCache, q: torch.Tensor, block_table: 
                                   out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """paged_attn_fp8_decode for callers that cannot supply a workspace: the
     split partials go to the library's fixed 16 MiB device buffer (see
-    include/fp8kv.h).  Calls that may overlap on the GPU race on that buffer."""
+    include/fp8kv.h).  Calls that may overlap on the GPU race on that buffer.
+    The arguments are checked like paged_attn_fp8_decode's before the call."""
     _need(q, torch.bfloat16, "q", cache.device)
     if q.dim() != 3 or not q.is_contiguous() or q.shape[2] != cache.head_dim:
         raise ValueError("q must be contiguous [B][Hq][D]")
     B, Hq, D = q.shape
+    _table_and_lens(block_table, seq_lens, B, cache.device)
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(D)
     rel, bstride, E = _bias_args(rel_bias, Hq)

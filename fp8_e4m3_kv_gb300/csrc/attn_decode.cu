@@ -355,8 +355,12 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
             int32_t phys = static_cast<int32_t>(p.num_blocks);   // out of range: zero fill
             if (lane < nb) {
                 const int64_t lb = (t0 + i) * nb + lane;
-                if (lb * p.block_size < len && lb < p.max_blocks) {
-                    const int32_t id = __ldg(p.block_table + static_cast<int64_t>(b) * p.max_blocks + lb);
+                if (lb * p.block_size < len) {
+                    // a length past the block table is flagged like a bad id
+                    const int32_t id =
+                        lb < p.max_blocks
+                            ? __ldg(p.block_table + static_cast<int64_t>(b) * p.max_blocks + lb)
+                            : -1;
                     if (id >= 0 && id < p.num_blocks)
                         phys = id;
                     else

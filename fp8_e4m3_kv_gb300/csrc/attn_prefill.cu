@@ -30,8 +30,30 @@ namespace {
 
 constexpr int kPreThreads = 192;
 constexpr float kLog2eP = 1.4426950408889634f;
-constexpr float kRescaleTau = 0.75f;   // lazy-rescale threshold (log2 units)
-constexpr float kPOffset = 8.0f;       // P pre-scale 2^8
+// P = 2^(z - m + kPOffset) with a lazy reference m: the row's reference max
+// moves only when its max grew by more than kRescaleTau, so P stays below
+// 2^(kPOffset + kRescaleTau) < 448 (the pages' rule tau < log2(448) -
+// max_offset).  The pages' kernel uses max_offset 8 with tau 0.75; here the
+// head_dim-128 kernel takes max_offset 6 with tau 2.75, the same rule: a
+// rescale of O in tensor memory is warp-wide (any of its 32 rows), and at
+// tau 0.75 about half of all 64-key halves paid one.  The e4m3 weights keep
+// their 3-bit precision down to 2^-12 of the row max (2^-14 at offset 8).
+constexpr float kRescaleTau = 0.75f;   // one-query-tile kernel (head_dim 256)
+constexpr float kPOffset = 8.0f;
+constexpr float kRescaleTau2 = 2.75f;  // two-pipeline kernel (head_dim 128)
+constexpr float kPOffset2 = 6.0f;
+static_assert(kPOffset + kRescaleTau < 8.807f && kPOffset2 + kRescaleTau2 < 8.807f,
+              "P must stay below 448");
+// One-term P budget.  Rounding P to one e4m3 term moves each weight by at
+// most 2^-4 of itself, independently per key, so the output error it causes
+// has a variance proportional to (sum of p^2 over the one-term keys) / l^2.
+// A row keeps P in one term for a 64-key half while the running sum of
+// p_max * l_half (>= sum of p^2) over its one-term halves stays within
+// kPBudget * l^2, l being the row sum so far (it only grows, relative to the
+// reference max, so the bound holds for the final l as well); otherwise the
+// half gets the second term e4m3(P - P_hi) as well.  Rows with few visible
+// keys or a few dominant weights take two terms, long flat rows one.
+constexpr float kPBudget = 0.01f;
 
 template <int D>
 struct PreCfg {
@@ -210,9 +232,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
             int32_t phys = static_cast<int32_t>(p.num_blocks);   // out of range: zero fill
             if (lane < nb) {
                 const int64_t lb = (kt0 + i) * nb + lane;
-                if (lb * p.block_size < len_k && lb < p.max_blocks) {
+                if (lb * p.block_size < len_k) {
+                    // a length past the block table is flagged like a bad id
                     const int32_t id =
-                        __ldg(p.block_table + static_cast<int64_t>(b) * p.max_blocks + lb);
+                        lb < p.max_blocks
+                            ? __ldg(p.block_table + static_cast<int64_t>(b) * p.max_blocks + lb)
+                            : -1;
                     if (id >= 0 && id < p.num_blocks)
                         phys = id;
                     else
@@ -482,7 +507,9 @@ struct Pre2Cfg {
     static constexpr int kPBytes = kTile * kTile;           // one P term, 16 KB
     static constexpr int kOffQ = 0;                         // [pipeline] Q8
     static constexpr int kOffStages = 2 * kQBytes;          // [pipeline][stage]
-    static constexpr int kOffP = kOffStages + 2 * kStages * kStageBytes;   // [pipeline][hi, lo]
+    // [pipeline] 32 KB: the output staging of the epilogue (and the sort's
+    // scratch at the start); P itself lives in tensor memory
+    static constexpr int kOffP = kOffStages + 2 * kStages * kStageBytes;
     static constexpr int kOffMisc = kOffP + 2 * 2 * kPBytes;
     static constexpr int kOffSched = kOffMisc + 512;        // sorted sequence tables
     static constexpr int kSmemBytes = kOffSched + 4 * 4 * kPre2SchedSeqs + 1024;
@@ -512,35 +539,35 @@ __device__ __forceinline__ float ex2_fast(float x) {
     return y;
 }
 
-// P for 16 consecutive keys: p = 2^(x*mult - m8); adds them to the two
-// partial row sums l and writes the P_hi and P_lo bytes (16 each) for this
-// row.  The scale and the sums use the packed two-lane fp32 instructions.
-__device__ __forceinline__ void p_chunk16(const float *x, float mult, float neg_m8, float2 &l,
-                                          uint4 &hi, uint4 &lo) {
-    const float2 mult2 = make_float2(mult, mult), off2 = make_float2(neg_m8, neg_m8);
-    uint32_t hw[4], lw[4];
+// 16 consecutive P values of one row -> their 16 e4m3 bytes, nearest even,
+// straight from fp32 (P <= 2^(8 + tau) never reaches the saturation bound).
+__device__ __forceinline__ uint4 p_hi16(const float *pv) {
+    uint32_t w[4];
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
-        uint32_t h2w[2], l2w[2];
+    for (int i = 0; i < 4; ++i)
+        w[i] = static_cast<uint32_t>(f32x2_to_e4m3x2(pv[4 * i], pv[4 * i + 1])) |
+               (static_cast<uint32_t>(f32x2_to_e4m3x2(pv[4 * i + 2], pv[4 * i + 3])) << 16);
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// The second terms e4m3(P - P_hi) of the same 16 values, given their P_hi
+// bytes; the difference is taken in fp16, where it is exact.
+__device__ __forceinline__ uint4 p_lo16(const float *pv, const uint4 hi) {
+    const uint32_t hw[4] = {hi.x, hi.y, hi.z, hi.w};
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t half_words[2];
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
-            const float2 z =
-                __ffma2_rn(make_float2(x[4 * w + 2 * k], x[4 * w + 2 * k + 1]), mult2, off2);
-            const float p0 = ex2_fast(z.x);
-            const float p1 = ex2_fast(z.y);
-            l = __fadd2_rn(l, make_float2(p0, p1));
-            const __half2 ph = __floats2half2_rn(p0, p1);
-            const uint32_t h8 = __nv_cvt_halfraw2_to_fp8x2(ph, __NV_SATFINITE, __NV_E4M3);
-            const __half2 hh = e4m3x2_to_half2(static_cast<uint16_t>(h8));
-            const uint32_t l8 = __nv_cvt_halfraw2_to_fp8x2(__hsub2(ph, hh), __NV_SATFINITE, __NV_E4M3);
-            h2w[k] = h8 & 0xFFFFu;
-            l2w[k] = l8 & 0xFFFFu;
+            const __half2 ph = __floats2half2_rn(pv[4 * i + 2 * k], pv[4 * i + 2 * k + 1]);
+            const __half2 hh = e4m3x2_to_half2(static_cast<uint16_t>(hw[i] >> (16 * k)));
+            half_words[k] =
+                __nv_cvt_halfraw2_to_fp8x2(__hsub2(ph, hh), __NV_SATFINITE, __NV_E4M3) & 0xFFFFu;
         }
-        hw[w] = h2w[0] | (h2w[1] << 16);
-        lw[w] = l2w[0] | (l2w[1] << 16);
+        w[i] = half_words[0] | (half_words[1] << 16);
     }
-    hi = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-    lo = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 // The bias of 64 consecutive keys of one row, fetched before any of it is
@@ -695,13 +722,18 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     auto full = [&](int k, int s) { return bars + 16 * k + s; };         // stage loaded
     auto empty = [&](int k, int s) { return bars + 16 * k + 2 + s; };    // stage consumed
     auto s_full = [&](int k, int hh) { return bars + 16 * k + 4 + hh; }; // S half written by QK
-    auto s_free = [&](int k, int hh) { return bars + 16 * k + 6 + hh; }; // S half read
     auto p_full = [&](int k, int hh) { return bars + 16 * k + 8 + hh; }; // P half written
     auto o_done = [&](int k, int hh) { return bars + 16 * k + 10 + hh; };// PV of P half done
     auto q_full = [&](int k) { return bars + 16 * k + 12; };             // Q8 of next item
     auto mma_done = [&](int k) { return bars + 16 * k + 13; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc + 256);
     CtaFail *fail = reinterpret_cast<CtaFail *>(smem + C::kOffMisc + 260);
+    // byte wq of lo_flag(k, hh): softmax warp wq of pipeline k wrote a second
+    // P term for its rows of the current unit of half hh (written before the
+    // warp arrives on p_full, read by the MMA thread after it waits there)
+    auto lo_flag = [&](int k, int hh) {
+        return reinterpret_cast<volatile uint8_t *>(smem + C::kOffMisc + 264 + 8 * k + 4 * hh);
+    };
     Pre2Seqs tab;
     tab.seq = reinterpret_cast<int32_t *>(smem + C::kOffSched);
     tab.q_first = tab.seq + kPre2SchedSeqs;
@@ -739,7 +771,6 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
             }
             for (int hh = 0; hh < 2; ++hh) {
                 mbar_init(s_full(k, hh), 1);
-                mbar_init(s_free(k, hh), 4);
                 mbar_init(p_full(k, hh), 4);
                 mbar_init(o_done(k, hh), 1);
             }
@@ -786,9 +817,12 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
                 int32_t phys = static_cast<int32_t>(p.num_blocks);   // out of range: zero fill
                 if (lane < nb) {
                     const int64_t lb = static_cast<int64_t>(t) * nb + lane;
-                    if (lb * p.block_size < it.len_k && lb < p.max_blocks) {
+                    if (lb * p.block_size < it.len_k) {
+                        // a length past the block table is flagged like a bad id
                         const int32_t id =
-                            __ldg(p.block_table + static_cast<int64_t>(it.b) * p.max_blocks + lb);
+                            lb < p.max_blocks
+                                ? __ldg(p.block_table + static_cast<int64_t>(it.b) * p.max_blocks + lb)
+                                : -1;
                         if (id >= 0 && id < p.num_blocks)
                             phys = id;
                         else
@@ -830,7 +864,6 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
             const uint32_t idesc_qk = idesc_e4m3_f32(128, C::kHalf, false, false);
             const uint32_t idesc_pv = idesc_e4m3_f32(128, 128, false, true);
             const uint32_t q_addr = smem_u32(smem + C::kOffQ + k * C::kQBytes);
-            const uint32_t p_addr = smem_u32(smem + C::kOffP + k * 2 * C::kPBytes);
             const uint32_t ring = smem_u32(smem + C::kOffStages + k * C::kStages * C::kStageBytes);
             const uint32_t col_s = k * 256, col_o = k * 256 + 128;
             int g = 0;   // stages seen
@@ -845,23 +878,26 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
                 int ui = 0;   // units of this item issued
                 bool q_ready = false;
                 // O += P[:, half] . V_j[half, :] for unit v (half v & 1 of the
-                // item's key tile j); the second half releases the stage
+                // item's key tile j), P read from tensor memory, where the
+                // softmax wrote it over the half's S columns (P_hi in the
+                // first 16, P_lo in the next 16); the second half releases
+                // the stage
                 auto issue_pv = [&](int v, bool first, int j) -> bool {
                     const int hv = v & 1;
                     if (!mbar_wait(p_full(k, hv), (v >> 1) & 1, fail, p.err)) return false;
                     tc_fence_after_sync();
                     const int s = (g0 + j) % C::kStages;
                     const uint32_t v_addr = ring + s * C::kStageBytes + C::kTileBytes;
-#pragma unroll
-                    for (int part = 0; part < 2; ++part) {
+                    // the P_lo product only when a softmax warp wrote a second term
+                    const int parts = *reinterpret_cast<volatile uint32_t *>(lo_flag(k, hv)) ? 2 : 1;
+#pragma unroll 1
+                    for (int part = 0; part < parts; ++part) {
 #pragma unroll
                         for (int kk = 0; kk < 2; ++kk) {
                             const int ks = 2 * hv + kk;   // 32-key step within the tile
-                            const uint64_t a =
-                                sdesc_sw128(p_addr + part * C::kPBytes + ks * 32, 16, 1024);
                             const uint64_t bd = sdesc_sw128(v_addr + ks * 32 * 128, kTile * 128, 1024);
-                            mma_e4m3(tmem + col_o, a, bd, idesc_pv,
-                                     (!first || part > 0 || kk > 0) ? 1u : 0u);
+                            mma_e4m3_tmem_a(tmem + col_o, tmem + col_s + hv * C::kHalf + part * 16 + kk * 8,
+                                            bd, idesc_pv, (!first || part > 0 || kk > 0) ? 1u : 0u);
                         }
                     }
                     tc_commit(o_done(k, hv));
@@ -880,10 +916,9 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
                             ok = false;
                             break;
                         }
-                        if (!mbar_wait(s_free(k, hh), ((U >> 1) & 1) ^ 1, fail, p.err)) {
-                            ok = false;
-                            break;
-                        }
+                        // S half hh last held P of unit U - 2, whose PV was
+                        // issued before this QK: MMAs of this thread run in
+                        // issue order, so the PV reads P before the QK writes
                         tc_fence_after_sync();
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {
@@ -1044,6 +1079,7 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
 
             float m_used = -INFINITY;
             float2 lsum = make_float2(0.0f, 0.0f);   // two partial row sums
+            float err_bound = 0.0f;   // sum of p_max * l_half over single-term halves
             for (int j = 0; j < n && ok; ++j) {
                 const int64_t k0 = static_cast<int64_t>(it.kt_lo + j) * kTile;
                 for (int hh = 0; hh < 2; ++hh) {
@@ -1066,12 +1102,10 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
                             r * 128);
 #pragma unroll
                         for (int e = 0; e < 8; ++e) q4[e] = make_uint4(0, 0, 0, 0);
+                        fence_proxy_async_smem();   // before the PV reads the rows
                     }
                     float x[C::kHalf];
                     tmem_ld_x64(tmem + lane_base + col_s + hh * C::kHalf, x);
-                    tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(s_free(k, hh));
 
                     // Scores to log2 units: z = x * score_log2 (+ bias *
                     // log2(e)), -inf where masked.  The scale stays folded
@@ -1134,31 +1168,69 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
                     // below 448).  O is rescaled a whole warp at a time, so
                     // once any row of the warp needs it, every row whose max
                     // grew moves too.
-                    const bool resc = mx > m_used + kRescaleTau;
+                    const bool resc = mx > m_used + kRescaleTau2;
                     const bool rescale_o = __any_sync(0xffffffffu, resc && m_used != -INFINITY);
                     const bool move = resc || (rescale_o && mx > m_used);
                     const float m_new = move ? mx : m_used;
                     const float alpha =
                         (move && m_used != -INFINITY) ? ex2_fast(m_used - m_new) : 1.0f;
-                    // this P half was read by the PV of unit u - 2
-                    if (u >= 2) {
-                        if (!warp_wait_p(o_done(k, hh), ((u - 2) >> 1) & 1, fail, p.err)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after_sync();
-                    }
                     lsum = __fmul2_rn(lsum, make_float2(alpha, alpha));
+                    err_bound *= alpha * alpha;
                     m_used = m_new;
-                    const float neg_m8 = (m_used == -INFINITY) ? 0.0f : kPOffset - m_used;
+                    const float neg_m8 = (m_used == -INFINITY) ? 0.0f : kPOffset2 - m_used;
+                    // P = 2^(x * mult - m8) of the half, kept in x
+                    float2 lu = make_float2(0.0f, 0.0f);
+                    {
+                        const float2 mult2 = make_float2(mult, mult), off2 = make_float2(neg_m8, neg_m8);
 #pragma unroll
-                    for (int q = 0; q < C::kHalf / 16; ++q) {
-                        uint4 hi, lo;
-                        p_chunk16(x + q * 16, mult, neg_m8, lsum, hi, lo);
-                        const uint32_t off = r * 128 + (((hh * (C::kHalf / 16) + q) ^ sw) << 4);
-                        *reinterpret_cast<uint4 *>(p_hi + off) = hi;
-                        *reinterpret_cast<uint4 *>(p_lo + off) = lo;
+                        for (int e = 0; e < C::kHalf; e += 2) {
+                            const float2 z = __ffma2_rn(make_float2(x[e], x[e + 1]), mult2, off2);
+                            x[e] = ex2_fast(z.x);
+                            x[e + 1] = ex2_fast(z.y);
+                            lu = __fadd2_rn(lu, make_float2(x[e], x[e + 1]));
+                        }
                     }
+                    lsum = __fadd2_rn(lsum, lu);
+                    // One e4m3 term for this half's P when the row's bound
+                    // stays within the budget; the warp takes two terms if
+                    // any of its rows needs them (sum p^2 <= p_max * l_half).
+                    const float l_row = lsum.x + lsum.y;
+                    const float s2 = ex2_fast(mx + neg_m8) * (lu.x + lu.y);
+                    const bool two = __any_sync(0xffffffffu, err_bound + s2 > kPBudget * l_row * l_row);
+                    if (!two) err_bound += s2;
+                    // P over the half's own S columns (read above): P_hi in
+                    // the first 16 columns, P_lo (or zeros, when another warp
+                    // makes the PV take the second term) in the next 16
+                    {
+                        uint32_t w[16];
+#pragma unroll
+                        for (int q = 0; q < C::kHalf / 16; ++q) {
+                            const uint4 hi = p_hi16(x + q * 16);
+                            w[4 * q] = hi.x;
+                            w[4 * q + 1] = hi.y;
+                            w[4 * q + 2] = hi.z;
+                            w[4 * q + 3] = hi.w;
+                        }
+                        const uint32_t pcol = tmem + lane_base + col_s + hh * C::kHalf;
+                        tmem_st_x16_nowait(pcol, w);
+                        uint32_t wl[16];
+                        if (two) {
+#pragma unroll
+                            for (int q = 0; q < C::kHalf / 16; ++q) {
+                                const uint4 lo = p_lo16(x + q * 16, make_uint4(w[4 * q], w[4 * q + 1],
+                                                                               w[4 * q + 2], w[4 * q + 3]));
+                                wl[4 * q] = lo.x;
+                                wl[4 * q + 1] = lo.y;
+                                wl[4 * q + 2] = lo.z;
+                                wl[4 * q + 3] = lo.w;
+                            }
+                        } else {
+#pragma unroll
+                            for (int q = 0; q < 16; ++q) wl[q] = 0u;
+                        }
+                        tmem_st_x16_nowait(pcol + 16, wl);
+                    }
+                    if (lane == 0) lo_flag(k, hh)[wq] = two ? 1 : 0;
                     if (rescale_o) {
                         // O holds the products up to unit u - 1 against the
                         // old reference: scale it by alpha once the PV of unit
@@ -1184,7 +1256,7 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
                             tmem_st_x64(tmem + lane_base + col_o + q * 64, o);
                         }
                     }
-                    fence_proxy_async_smem();
+                    tmem_wait_st();
                     tc_fence_before_sync();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(p_full(k, hh));

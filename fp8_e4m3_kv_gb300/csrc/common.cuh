@@ -169,6 +169,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait with a suspend-time hint: a thread whose phase has not completed
+// sleeps until it completes or `hint_ns` elapses, instead of spinning on the
+// issue slots that the other warps of its scheduler need.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t addr, uint32_t parity,
+                                                    uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(addr), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Longest sleep of one try_wait in a bounded wait: the abort flag and the
+// time limit are checked after each.
+constexpr uint32_t kWaitSleepNs = 100000;   // 0.1 ms
+
 // Shared state of one CTA's failure handling: the first wait that runs out
 // sets `abort`; every later wait in the CTA then gives up at once, so all
 // roles reach the teardown without waiting out the limit again.
@@ -185,9 +205,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, CtaFai
     if (mbar_try_wait(addr, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
-#pragma unroll 1
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(addr, parity)) return true;
+        if (mbar_try_wait_sleep(addr, parity, kWaitSleepNs)) return true;
         if (fail->abort) return false;
         if (global_timer_ns() - t0 > kWaitLimitNs) {
             fail->abort = 1;
@@ -275,6 +293,20 @@ __device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint6
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem desc], e4m3 x e4m3 -> fp32, with A read from
+// tensor memory: row i of A in lane i, each 32-bit column holding four
+// consecutive K elements (lowest byte first); one MMA of K = 32 reads eight
+// columns from a_tmem.
+__device__ __forceinline__ void mma_e4m3_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -392,6 +424,22 @@ __device__ __forceinline__ void tmem_st_x128(uint32_t taddr, const float *v) {
         "tcgen05.st.sync.aligned.32x32b.x128.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127,%128};\n\t"
         "tcgen05.wait::st.sync.aligned;" ::"r"(taddr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])), "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])), "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])), "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])), "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])), "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31])), "r"(__float_as_uint(v[32])), "r"(__float_as_uint(v[33])), "r"(__float_as_uint(v[34])), "r"(__float_as_uint(v[35])), "r"(__float_as_uint(v[36])), "r"(__float_as_uint(v[37])), "r"(__float_as_uint(v[38])), "r"(__float_as_uint(v[39])), "r"(__float_as_uint(v[40])), "r"(__float_as_uint(v[41])), "r"(__float_as_uint(v[42])), "r"(__float_as_uint(v[43])), "r"(__float_as_uint(v[44])), "r"(__float_as_uint(v[45])), "r"(__float_as_uint(v[46])), "r"(__float_as_uint(v[47])), "r"(__float_as_uint(v[48])), "r"(__float_as_uint(v[49])), "r"(__float_as_uint(v[50])), "r"(__float_as_uint(v[51])), "r"(__float_as_uint(v[52])), "r"(__float_as_uint(v[53])), "r"(__float_as_uint(v[54])), "r"(__float_as_uint(v[55])), "r"(__float_as_uint(v[56])), "r"(__float_as_uint(v[57])), "r"(__float_as_uint(v[58])), "r"(__float_as_uint(v[59])), "r"(__float_as_uint(v[60])), "r"(__float_as_uint(v[61])), "r"(__float_as_uint(v[62])), "r"(__float_as_uint(v[63])), "r"(__float_as_uint(v[64])), "r"(__float_as_uint(v[65])), "r"(__float_as_uint(v[66])), "r"(__float_as_uint(v[67])), "r"(__float_as_uint(v[68])), "r"(__float_as_uint(v[69])), "r"(__float_as_uint(v[70])), "r"(__float_as_uint(v[71])), "r"(__float_as_uint(v[72])), "r"(__float_as_uint(v[73])), "r"(__float_as_uint(v[74])), "r"(__float_as_uint(v[75])), "r"(__float_as_uint(v[76])), "r"(__float_as_uint(v[77])), "r"(__float_as_uint(v[78])), "r"(__float_as_uint(v[79])), "r"(__float_as_uint(v[80])), "r"(__float_as_uint(v[81])), "r"(__float_as_uint(v[82])), "r"(__float_as_uint(v[83])), "r"(__float_as_uint(v[84])), "r"(__float_as_uint(v[85])), "r"(__float_as_uint(v[86])), "r"(__float_as_uint(v[87])), "r"(__float_as_uint(v[88])), "r"(__float_as_uint(v[89])), "r"(__float_as_uint(v[90])), "r"(__float_as_uint(v[91])), "r"(__float_as_uint(v[92])), "r"(__float_as_uint(v[93])), "r"(__float_as_uint(v[94])), "r"(__float_as_uint(v[95])), "r"(__float_as_uint(v[96])), "r"(__float_as_uint(v[97])), "r"(__float_as_uint(v[98])), "r"(__float_as_uint(v[99])), "r"(__float_as_uint(v[100])), "r"(__float_as_uint(v[101])), "r"(__float_as_uint(v[102])), "r"(__float_as_uint(v[103])), "r"(__float_as_uint(v[104])), "r"(__float_as_uint(v[105])), "r"(__float_as_uint(v[106])), "r"(__float_as_uint(v[107])), "r"(__float_as_uint(v[108])), "r"(__float_as_uint(v[109])), "r"(__float_as_uint(v[110])), "r"(__float_as_uint(v[111])), "r"(__float_as_uint(v[112])), "r"(__float_as_uint(v[113])), "r"(__float_as_uint(v[114])), "r"(__float_as_uint(v[115])), "r"(__float_as_uint(v[116])), "r"(__float_as_uint(v[117])), "r"(__float_as_uint(v[118])), "r"(__float_as_uint(v[119])), "r"(__float_as_uint(v[120])), "r"(__float_as_uint(v[121])), "r"(__float_as_uint(v[122])), "r"(__float_as_uint(v[123])), "r"(__float_as_uint(v[124])), "r"(__float_as_uint(v[125])), "r"(__float_as_uint(v[126])), "r"(__float_as_uint(v[127]))
         : "memory");
+}
+
+// Store 16 consecutive 32-bit TMEM columns of this thread's lane without
+// waiting; tmem_wait_st() waits for every store the thread issued.
+__device__ __forceinline__ void tmem_st_x16_nowait(uint32_t taddr, const uint32_t *w) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]),
+        "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]),
+        "r"(w[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void tmem_st_x32(uint32_t taddr, const float *v) {

@@ -68,7 +68,8 @@ typedef uint16_t fp8kv_bf16;    /* raw bfloat16 bit pattern */
 
 /* Device error word bits (fp8kv_device_error). */
 #define FP8KV_DEVERR_WAIT_TIMEOUT 0x1u   /* a bounded pipeline wait ran out       */
-#define FP8KV_DEVERR_BAD_BLOCK    0x2u   /* a block id outside [0, num_blocks)     */
+#define FP8KV_DEVERR_BAD_BLOCK    0x2u   /* a block id outside [0, num_blocks), or a
+                                            sequence length past its block-table row  */
 #define FP8KV_DEVERR_BAD_SLOT     0x4u   /* a slot outside the pool                */
 
 typedef struct {
@@ -113,7 +114,9 @@ fp8kv_status kv_store_e4m3(const fp8kv_cache *cache, const fp8kv_bf16 *k,
  * seq_lens:     device int32 [num_seqs], keys per sequence,
  *               0 <= len <= max_blocks_per_seq*block_size.  The query sits at
  *               position len-1 (it is the newest stored token).  len = 0
- *               yields zeros.
+ *               yields zeros.  Keys whose block lies past the table row (a
+ *               longer len) or whose table entry is outside [0, num_blocks)
+ *               are read as zeros and set FP8KV_DEVERR_BAD_BLOCK.
  * rel_bias:     NULL, or device bf16; the bias of sequence b, query head h,
  *               distance d = (len-1) - j is rel_bias[b*bias_tok_stride +
  *               h*rel_extent + d] for 0 <= d < rel_extent, else 0.  It is
@@ -135,7 +138,7 @@ fp8kv_status paged_attn_fp8_decode(const fp8kv_cache *cache, const fp8kv_bf16 *q
 /*
  * paged_attn_fp8_decode_ex -- paged_attn_fp8_decode with an explicit split
  * length: split_tokens > 0 makes every split cover that many keys and must be
- * a multiple of the kernel's key tile (256 keys at head_dim 128, 128 at 256);
+ * a multiple of the kernel's key tile (128 keys);
  * 0 chooses it from the device's SM count (the plain call).
  */
 fp8kv_status paged_attn_fp8_decode_ex(const fp8kv_cache *cache, const fp8kv_bf16 *q,
@@ -224,7 +227,10 @@ size_t fp8kv_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads,
  * a chunk of query tokens per sequence over the cached keys, on FP8 tensor
  * cores (vLLM PR 54705 "Purpose" descale handling; evidence document Tier 0:
  * P is formed in e4m3 pre-scaled by 2^8 with a lazy-rescale threshold of
- * 0.75 < log2(448) - 8).
+ * 0.75 < log2(448) - 8).  P of a 64-key half of a row is one e4m3 term
+ * while a bound on the rounding error it adds to the row stays within a
+ * fixed budget; rows with few visible keys or a few dominant weights get a
+ * second term e4m3(P - P_hi) as well.
  * q:             device bf16 [total_q][num_q_heads][head_dim], contiguous;
  *                sequence b's queries are rows cu_seqlens_q[b] ..
  *                cu_seqlens_q[b+1]-1.
@@ -232,6 +238,9 @@ size_t fp8kv_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads,
  * seq_lens_k:    device int32 [num_seqs]; keys per sequence, >= the
  *                sequence's query count.  The queries are the last ones:
  *                query i of a chunk of n sits at position seq_len_k - n + i.
+ *                Keys past the block-table row, or with a table entry outside
+ *                [0, num_blocks), are read as zeros and set
+ *                FP8KV_DEVERR_BAD_BLOCK.
  * max_seqlen_q:  an upper bound of the per-sequence query counts (sizes the
  *                grid; rows beyond a sequence's count do nothing).
  * rel_bias:      NULL, or device bf16; bias of query row t (global index),

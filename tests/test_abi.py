@@ -259,3 +259,38 @@ def test_amax_rejects_bad_arguments_on_host(lib):
     assert f(8, None, 256, 256, None, 1, 2, 128, 16, None, None) == lib.ERR_ARG       # align 16
     assert f(None, None, 256, 256, None, 1, 2, 128, None, None, None) == lib.OK       # nothing to do
     assert f(16, 16, 256, 256, None, 0, 2, 128, 16, 16, None) == lib.OK
+
+
+def test_decode_bindings_check_table_and_lengths(lib):
+    """Every decode binding checks block_table and seq_lens (dtype, device,
+    shape, contiguity) before the call: the kernels read them through raw
+    device pointers.  The cache here is a host tensor, so a "device" mismatch
+    is a meta tensor; nothing reaches CUDA."""
+    import torch
+    cache = lib.KVCache.empty(4, 16, 1, 128, device="cpu")
+    q = torch.zeros(2, 4, 128, dtype=torch.bfloat16)
+    bt = torch.zeros(2, 3, dtype=torch.int32)
+    lens = torch.ones(2, dtype=torch.int32)
+    calls = {
+        "decode": lambda t, n: lib.paged_attn_fp8_decode(cache, q, t, n, 1.0, 1.0, 1.0),
+        "noalloc": lambda t, n: lib.paged_attn_fp8_decode_noalloc(cache, q, t, n, 1.0, 1.0, 1.0),
+        "store": lambda t, n: lib.paged_attn_fp8_decode_store(
+            cache, q, torch.zeros(2, 1, 128, dtype=torch.bfloat16),
+            torch.zeros(2, 1, 128, dtype=torch.bfloat16), t, n, 1.0, 1.0, 1.0),
+        "per_token": lambda t, n: lib.paged_attn_fp8_decode_per_token(
+            cache, q, t, n, 1.0, torch.ones(4, 1, 16), torch.ones(4, 1, 16)),
+    }
+    bad = [
+        (bt.to(torch.int64), lens, TypeError),                  # int64 table
+        (bt, lens.to(torch.int64), TypeError),                  # int64 lengths
+        (torch.zeros(1, 3, dtype=torch.int32), lens, ValueError),   # fewer rows than B
+        (torch.zeros(2, dtype=torch.int32), lens, ValueError),      # not 2-D
+        (torch.zeros(3, 2, dtype=torch.int32).t(), lens, ValueError),   # not contiguous
+        (bt, torch.ones(3, dtype=torch.int32), ValueError),     # lengths of another batch
+        (torch.zeros(2, 3, dtype=torch.int32, device="meta"), lens, ValueError),  # other device
+        (bt, torch.ones(2, dtype=torch.int32, device="meta"), ValueError),
+    ]
+    for name, call in calls.items():
+        for t, n, exc in bad:
+            with pytest.raises(exc):
+                call(t, n)

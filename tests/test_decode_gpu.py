@@ -114,7 +114,8 @@ def test_empty_and_single_key(fk):
     assert (got[0] == 0).all()
 
 
-def _full(fk, spec, rows_per_check, seed=0, scales=(1.0, 1.0, 1.0), calibrate=False):
+def _full(fk, spec, rows_per_check, seed=0, scales=(1.0, 1.0, 1.0), calibrate=False,
+          longest_all_heads=False):
     inp = workloads.make_decode(spec, device=DEV, seed=seed)
     kv = inp["kv"]
     sq, sk, sv = scales
@@ -142,6 +143,9 @@ def _full(fk, spec, rows_per_check, seed=0, scales=(1.0, 1.0, 1.0), calibrate=Fa
     for b in bsel:
         kvh = int(rng.integers(spec.Hkv))
         rows += [(b, kvh * G + g) for g in range(G)][: rows_per_check[1]]
+    if longest_all_heads:   # every query head of the longest sequence
+        b = int(order[-1])
+        rows += [(b, h) for h in range(spec.Hq) if (b, h) not in rows]
     host = dict(inp)
     host["kv"] = kv
     ref = oracle_decode_rows(host, rows, sq, sk, sv, window=spec.window, rel=inp["rel"])
@@ -154,6 +158,39 @@ def test_full_decode_64seq_32k(fk):
 
 def test_full_decode_64seq_32k_vscale3(fk):
     _full(fk, workloads.DECODE_32K, (2, 8), scales=(1.0, 1.0, 3.0))
+
+
+def test_full_decode_64seq_32k_vscale3_longest_all_heads(fk):
+    """v_scale 3.0 on the full workload: every head of its longest sequence."""
+    _full(fk, workloads.DECODE_32K, (0, 0), scales=(1.0, 1.0, 3.0), longest_all_heads=True)
+
+
+def test_full_decode_64seq_32k_window512(fk):
+    """The full workload as a 512-token sliding-window layer."""
+    import dataclasses
+    _full(fk, dataclasses.replace(workloads.DECODE_32K, window=512), (4, 8))
+
+
+def test_length_past_block_table_is_flagged(fk):
+    """A length past the sequence's block-table row: the keys beyond the row
+    read as zeros, FP8KV_DEVERR_BAD_BLOCK is set, and the call completes."""
+    spec = workloads.DecodeSpec("case", B=2, Hq=8, Hkv=2, D=128, block_size=16, ctx_lo=1,
+                                ctx_hi=1)
+    inp = workloads.make_decode(spec, device="cpu", seed=30, lens=[40, 48])
+    kv = to_device(inp["kv"], DEV)
+    cache = fk.KVCache.empty(kv.num_blocks, 16, 2, 128, device=DEV)
+    fk.kv_store_e4m3(cache, kv.k, kv.v, kv.slot_mapping, 1.0, 1.0)
+    assert kv.block_table.shape[1] == 3
+    q = inp["q"].to(DEV)
+    fk.paged_attn_fp8_decode(cache, q, kv.block_table, kv.seq_lens, 1.0, 1.0, 1.0)
+    torch.cuda.synchronize()
+    assert fk.device_error() == 0
+    too_long = torch.tensor([40, 48 + 37], dtype=torch.int32, device=DEV)
+    out = fk.paged_attn_fp8_decode(cache, q, kv.block_table, too_long, 1.0, 1.0, 1.0)
+    torch.cuda.synchronize()
+    assert fk.device_error() & fk.DEVERR_BAD_BLOCK
+    assert fk.device_error() == 0          # read with clear: the word is clean again
+    assert torch.isfinite(out.float()).all()
 
 
 def test_full_decode_128k_calibrated_d256(fk):

@@ -313,3 +313,22 @@ def test_full_chunk_over_64k_prefix(fk):
     host["rel"] = inp["rel"].cpu()
     ref = oracle_prefill_rows(host, rows, 1.0, 1.0, 1.0, window=0, rel=host["rel"])
     assert_close(np.stack([got[t, h] for t, h in rows]), ref, spec.name)
+
+
+def test_length_past_block_table_is_flagged(fk):
+    """seq_lens_k past the block-table row: the keys beyond it read as zeros,
+    FP8KV_DEVERR_BAD_BLOCK is set, and the call completes."""
+    spec = workloads.PrefillSpec("case", q_lens=[100], q_lo=0, q_hi=0, n_seqs=1, Hq=4, Hkv=1,
+                                 D=128, block_size=16)
+    inp = workloads.make_prefill(spec, device="cpu", seed=31, q_lens=[100], k_lens=[100])
+    kv = to_device(inp["kv"], DEV)
+    cache = fk.KVCache.empty(kv.num_blocks, 16, 1, 128, device=DEV)
+    fk.kv_store_e4m3(cache, kv.k, kv.v, kv.slot_mapping, 1.0, 1.0)
+    assert kv.block_table.shape[1] == 7          # 112 keys of room
+    too_long = torch.tensor([100 + 60], dtype=torch.int32, device=DEV)
+    out = fk.attn_fp8_varlen_prefill(cache, inp["q"].to(DEV), inp["cu_seqlens_q"].to(DEV),
+                                     too_long, kv.block_table, 100, 1.0, 1.0, 1.0)
+    torch.cuda.synchronize()
+    assert fk.device_error() & fk.DEVERR_BAD_BLOCK
+    assert fk.device_error() == 0
+    assert torch.isfinite(out.float()).all()
