@@ -65,6 +65,9 @@ _store_pt = _sig("kv_store_e4m3_per_token", ctypes.c_int,
 _decode_pt = _sig("paged_attn_fp8_decode_per_token", ctypes.c_int,
                   [ctypes.POINTER(CacheStruct), P, i32, P, i32, P, i32, f32, f32, P, P, P, i64,
                    i32, i32, P, P, sz, P])
+_prefill_pt = _sig("attn_fp8_varlen_prefill_per_token", ctypes.c_int,
+                   [ctypes.POINTER(CacheStruct), P, i32, P, P, P, i32, i32, i32, f32, f32, P, P, P,
+                    i64, i32, i32, P, P])
 _ws_size = _sig("fp8kv_decode_workspace_size", sz, [i32, i32, i32, i32, i32, i32, i32, i32])
 _prefill = _sig("attn_fp8_varlen_prefill", ctypes.c_int,
                 [ctypes.POINTER(CacheStruct), P, i32, P, P, P, i32, i32, i32, f32, f32, f32,
@@ -81,6 +84,7 @@ EXPORTED = ("kv_store_e4m3", "paged_attn_fp8_decode", "paged_attn_fp8_decode_ex"
             "paged_attn_fp8_decode_noalloc", "paged_attn_fp8_decode_store",
             "kv_store_e4m3_per_token", "paged_attn_fp8_decode_per_token",
             "fp8kv_decode_workspace_size", "attn_fp8_varlen_prefill",
+            "attn_fp8_varlen_prefill_per_token",
             "fp8kv_set_prefill_max_ctas", "kv_amax_calibrate",
             "kv_band_counts",
             "fp8kv_scale_from_amax", "fp8kv_cache_bytes", "fp8kv_device_error",
@@ -449,6 +453,43 @@ def attn_fp8_varlen_prefill(cache: KVCache, q: torch.Tensor, cu_seqlens_q: torch
     return out
 
 
+def attn_fp8_varlen_prefill_per_token(cache: KVCache, q: torch.Tensor, cu_seqlens_q: torch.Tensor,
+                                      seq_lens_k: torch.Tensor, block_table: torch.Tensor,
+                                      max_seqlen_q: int, q_scale: float, k_scales: torch.Tensor,
+                                      v_scales: torch.Tensor, softmax_scale: Optional[float] = None,
+                                      rel_bias: Optional[torch.Tensor] = None, window: int = 0,
+                                      out: Optional[torch.Tensor] = None,
+                                      stream=None) -> torch.Tensor:
+    """attn_fp8_varlen_prefill over a cache written by kv_store_e4m3_per_token
+    (its scale arrays k_scales, v_scales); returns out [Tq][Hq][D] bf16."""
+    _need(q, torch.bfloat16, "q", cache.device)
+    if q.dim() != 3 or not q.is_contiguous() or q.shape[2] != cache.head_dim:
+        raise ValueError("q must be contiguous [Tq][Hq][D]")
+    Tq, Hq, D = q.shape
+    shape = (cache.num_blocks, cache.num_kv_heads, cache.block_size)
+    for name, t in (("k_scales", k_scales), ("v_scales", v_scales)):
+        _need(t, torch.float32, name, cache.device)
+        if tuple(t.shape) != shape or not t.is_contiguous():
+            raise ValueError("%s must be contiguous float32 %s" % (name, shape))
+    _need(cu_seqlens_q, torch.int32, "cu_seqlens_q", cache.device)
+    _need(seq_lens_k, torch.int32, "seq_lens_k", cache.device)
+    _need(block_table, torch.int32, "block_table", cache.device)
+    B = seq_lens_k.numel()
+    if cu_seqlens_q.numel() != B + 1 or block_table.shape[0] != B or \
+            not block_table.is_contiguous():
+        raise ValueError("cu_seqlens_q [B+1], seq_lens_k [B], block_table [B][max_blocks]")
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    rel, bstride, E = _bias_args(rel_bias, Hq)
+    if out is None:
+        out = torch.empty_like(q)
+    _check(_prefill_pt(cache.c(), _ptr(q), Hq, _ptr(cu_seqlens_q), _ptr(seq_lens_k),
+                       _ptr(block_table), block_table.shape[1], B, int(max_seqlen_q), q_scale,
+                       softmax_scale, _ptr(k_scales), _ptr(v_scales), _ptr(rel), bstride, E, window,
+                       _ptr(out), _stream(stream)), "attn_fp8_varlen_prefill_per_token")
+    return out
+
+
 def set_prefill_max_ctas(max_ctas: int) -> None:
     """Caps the CTAs of the persistent head_dim-128 prefill (0: one per SM)."""
     _check(_prefill_max_ctas(int(max_ctas)), "fp8kv_set_prefill_max_ctas")
@@ -465,6 +506,6 @@ __all__ = ["KVCache", "Fp8KVError", "kv_store_e4m3", "kv_amax_calibrate", "kv_ba
            "band_counts_dict", "BAND_COUNTS_BYTES", "scale_from_amax",
            "paged_attn_fp8_decode", "paged_attn_fp8_decode_noalloc", "paged_attn_fp8_decode_store",
            "kv_store_e4m3_per_token", "paged_attn_fp8_decode_per_token",
-           "attn_fp8_varlen_prefill", "set_prefill_max_ctas",
+           "attn_fp8_varlen_prefill", "attn_fp8_varlen_prefill_per_token", "set_prefill_max_ctas",
            "decode_workspace_size",
            "cache_bytes", "device_error", "status_string", "LIB_PATH", "EXPORTED"]

@@ -97,6 +97,11 @@ struct PrefillParams {
     float score_log2;   // softmax_scale * q_scale * k_scale * log2(e)
     float v_scale;
     float bias_fold;    // log2(e) / score_log2, or 0 where that is not a safe finite factor
+    // per-token scales (the per-token variant only):
+    // float[num_blocks][num_kv_heads][block_size], one per cached token and head
+    const float *k_tok_scale;
+    const float *v_tok_scale;
+    int32_t num_kv_heads;
 };
 
 __device__ __forceinline__ void mbar_drain_p(uint64_t *bar, uint32_t parity, uint32_t *err) {
@@ -515,7 +520,12 @@ struct Pre2Cfg {
     static constexpr int kSmemBytes = kOffSched + 4 * 4 * kPre2SchedSeqs + 1024;
     static constexpr uint32_t kTmemCols = 512;              // S0 O0 | S1 O1
     static constexpr int kHalf = kTile / 2;                 // keys per unit
+    // per-token variant: per pipeline and ring stage, three float[128] key
+    // tables (score factor, log2 of the V scale, its reciprocal) in the
+    // staging area, which that variant's epilogue does not use
+    static constexpr int kOffTab = kOffP;
 };
+static_assert(2 * Pre2Cfg::kStages * 2048 <= 2 * 2 * Pre2Cfg::kPBytes, "per-token tables");
 static_assert(Pre2Cfg::kSmemBytes <= 227 * 1024, "shared memory");
 
 // 16 x 8 bf16 -> 16 x 8 e4m3 bytes, the scale's form fixed at compile time.
@@ -706,6 +716,12 @@ __device__ __forceinline__ bool pre2_next(const PrefillParams &p, const Pre2Seqs
                      p.n_qtiles - 1 - sc.lev, it);
 }
 
+// kPT: per-token scales.  Key j's score is x_j * score_log2 * k_scale_j; its
+// V scale is folded into the exponent, P_j = 2^(z_j + log2 v_scale_j - m +
+// offset), so that the MMA weights are p_j * v_scale_j, and the row sum adds
+// P_j / v_scale_j.  The producer writes the three per-key factors of each
+// key tile into its stage's table.
+template <bool kPT>
 __global__ void __launch_bounds__(kPre2Threads, 1)
 prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                 const PrefillParams p) {
@@ -733,6 +749,10 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     // warp arrives on p_full, read by the MMA thread after it waits there)
     auto lo_flag = [&](int k, int hh) {
         return reinterpret_cast<volatile uint8_t *>(smem + C::kOffMisc + 264 + 8 * k + 4 * hh);
+    };
+    // per-token key tables of pipeline k's ring stage s: [factor | log2 sv | 1 / sv]
+    auto key_tab = [&](int k, int s) {
+        return reinterpret_cast<float *>(smem + C::kOffTab + (2 * k + s) * 2048);
     };
     Pre2Seqs tab;
     tab.seq = reinterpret_cast<int32_t *>(smem + C::kOffSched);
@@ -835,6 +855,38 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
                 if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
                     ok = false;
                     break;
+                }
+                if constexpr (kPT) {
+                    // the stage's key table (its previous tile's softmax is
+                    // done with it: the stage is empty); four keys per lane.
+                    // Keys outside the sequence get factors that keep their
+                    // masked -inf scores -inf and add nothing to the sum.
+                    float4 fk = make_float4(1.0f, 1.0f, 1.0f, 1.0f);
+                    float4 lv = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                    float4 iv = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                    float *fkp = &fk.x, *lvp = &lv.x, *ivp = &iv.x;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int32_t key = t * kTile + 4 * lane + i;
+                        const int32_t lb = key / p.block_size;
+                        if (key < it.len_k && lb < p.max_blocks) {
+                            const int32_t id =
+                                __ldg(p.block_table + static_cast<int64_t>(it.b) * p.max_blocks + lb);
+                            if (id >= 0 && id < p.num_blocks) {
+                                const int64_t si = (static_cast<int64_t>(id) * p.num_kv_heads + kvh) *
+                                                       p.block_size + key % p.block_size;
+                                const float sv = __ldg(p.v_tok_scale + si);
+                                fkp[i] = p.score_log2 * __ldg(p.k_tok_scale + si);
+                                lvp[i] = log2f(sv);
+                                ivp[i] = __frcp_rn(sv);
+                            }
+                        }
+                    }
+                    float *tb = key_tab(k, s);
+                    reinterpret_cast<float4 *>(tb)[lane] = fk;
+                    reinterpret_cast<float4 *>(tb + kTile)[lane] = lv;
+                    reinterpret_cast<float4 *>(tb + 2 * kTile)[lane] = iv;
+                    __syncwarp();   // the table before lane 0's arrive releases it
                 }
                 if (lane == 0) mbar_arrive_expect_tx(full(k, s), C::kStageBytes);
                 __syncwarp();
@@ -978,6 +1030,25 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
             const float f = (l > 0.0f) ? p.v_scale / l : 0.0f;
             float o[D];
             tmem_ld_x128(tmem + lane_base + col_o, o);
+            if constexpr (kPT) {
+                // the staging area holds the key tables: each thread stores
+                // its own row
+                if (r < prev_rows) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.out + (prev_tok + r) * p.Hq * D +
+                                                           static_cast<int64_t>(prev_h) * D);
+#pragma unroll
+                    for (int cch = 0; cch < D / 8; ++cch) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const __nv_bfloat162 v2 = __floats2bfloat162_rn(
+                                o[8 * cch + 2 * e] * f, o[8 * cch + 2 * e + 1] * f);
+                            w[e] = *reinterpret_cast<const uint32_t *>(&v2);
+                        }
+                        dst[cch] = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                }
+            } else {
 #pragma unroll
             for (int cch = 0; cch < D / 8; ++cch) {
                 uint32_t w[4];
@@ -1005,6 +1076,7 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
             }
             // the rows are read back before the next item's P overwrites them
             __syncwarp();
+            }
             return true;
         };
 
@@ -1106,19 +1178,52 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
                     }
                     float x[C::kHalf];
                     tmem_ld_x64(tmem + lane_base + col_s + hh * C::kHalf, x);
+                    const float *ktab = key_tab(k, (g0 + j) % C::kStages) + hh * C::kHalf;
+                    if constexpr (kPT) {
+                        // the producer's table of this stage: its full barrier
+                        // (complete, since S of the tile exists) orders it
+                        if (hh == 0 && !warp_wait_p(full(k, (g0 + j) % C::kStages),
+                                                    ((g0 + j) / C::kStages) & 1, fail, p.err)) {
+                            ok = false;
+                            break;
+                        }
+                        // z = x * score_log2 * k_scale + log2(v_scale)
+#pragma unroll
+                        for (int e = 0; e < C::kHalf; e += 4) {
+                            const float4 f4 = *reinterpret_cast<const float4 *>(ktab + e);
+                            const float4 l4 = *reinterpret_cast<const float4 *>(ktab + kTile + e);
+                            const float2 za = __ffma2_rn(make_float2(x[e], x[e + 1]),
+                                                         make_float2(f4.x, f4.y), make_float2(l4.x, l4.y));
+                            const float2 zb = __ffma2_rn(make_float2(x[e + 2], x[e + 3]),
+                                                         make_float2(f4.z, f4.w), make_float2(l4.z, l4.w));
+                            x[e] = za.x;
+                            x[e + 1] = za.y;
+                            x[e + 2] = zb.x;
+                            x[e + 3] = zb.y;
+                        }
+                    }
 
                     // Scores to log2 units: z = x * score_log2 (+ bias *
                     // log2(e)), -inf where masked.  The scale stays folded
                     // into the FMA of P (mult): the bias is added as bias *
                     // log2(e) / score_log2; masking and the max do not need
                     // the scale, it being positive.
-                    float mult = p.score_log2;
+                    float mult = kPT ? 1.0f : p.score_log2;
                     const bool any_bias = __any_sync(0xffffffffu, bias_half);
                     if (any_bias) {
                         uint32_t Y[32];
                         load_bias64(bias_half ? bias_row : nullptr, d0, p.rel_extent,
                                     p.bias_vec != 0, Y);
-                        if (p.bias_fold > 0.0f) {
+                        if (kPT) {
+                            // the scores are already in log2 units
+#pragma unroll
+                            for (int e = 0; e < C::kHalf; ++e) {
+                                const uint32_t wd = Y[(63 - e) >> 1];
+                                const float bv = __uint_as_float(((63 - e) & 1) ? (wd & 0xFFFF0000u)
+                                                                                 : (wd << 16));
+                                x[e] = fmaf(bv, kLog2eP, x[e]);
+                            }
+                        } else if (p.bias_fold > 0.0f) {
                             // x + bias * log2(e) / score_log2: the score scale
                             // stays folded into the FMA of P (packed pairs;
                             // key e takes the upper half of its word for even e)
@@ -1187,7 +1292,11 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
                             const float2 z = __ffma2_rn(make_float2(x[e], x[e + 1]), mult2, off2);
                             x[e] = ex2_fast(z.x);
                             x[e + 1] = ex2_fast(z.y);
-                            lu = __fadd2_rn(lu, make_float2(x[e], x[e + 1]));
+                            if constexpr (kPT)   // the row sum takes P / v_scale
+                                lu = __ffma2_rn(make_float2(x[e], x[e + 1]),
+                                                make_float2(ktab[2 * kTile + e], ktab[2 * kTile + e + 1]), lu);
+                            else
+                                lu = __fadd2_rn(lu, make_float2(x[e], x[e + 1]));
                         }
                     }
                     lsum = __fadd2_rn(lsum, lu);
@@ -1196,7 +1305,9 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
                     // any of its rows needs them (sum p^2 <= p_max * l_half).
                     const float l_row = lsum.x + lsum.y;
                     const float s2 = ex2_fast(mx + neg_m8) * (lu.x + lu.y);
-                    const bool two = __any_sync(0xffffffffu, err_bound + s2 > kPBudget * l_row * l_row);
+                    // (the per-token variant always takes two terms)
+                    const bool two =
+                        kPT || __any_sync(0xffffffffu, err_bound + s2 > kPBudget * l_row * l_row);
                     if (!two) err_bound += s2;
                     // P over the half's own S columns (read above): P_hi in
                     // the first 16 columns, P_lo (or zeros, when another warp
@@ -1283,11 +1394,12 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
 // The register split relies on the kernel being launched with kRegsLaunch
 // registers per thread: with fewer, setmaxnreg.inc would wait for registers
 // that do not exist.  Checked once per process against the built kernel.
+template <bool kPT>
 bool prefill2_registers_ok() {
     static int ok = -1;
     if (ok < 0) {
         cudaFuncAttributes attr;
-        ok = (cudaFuncGetAttributes(&attr, prefill2_kernel) == cudaSuccess &&
+        ok = (cudaFuncGetAttributes(&attr, prefill2_kernel<kPT>) == cudaSuccess &&
               attr.numRegs >= kRegsLaunch && attr.maxThreadsPerBlock >= kPre2Threads)
                  ? 1
                  : 0;
@@ -1299,12 +1411,13 @@ bool prefill2_registers_ok() {
 // CTAs of a persistent launch at most (0: one per SM).
 std::atomic<int> g_prefill_max_ctas{0};
 
+template <bool kPT>
 fp8kv_status launch_prefill2(const CUtensorMap &km, const CUtensorMap &vm, const PrefillParams &p,
                              int num_seqs, int sms, cudaStream_t stream) {
     const int cap = g_prefill_max_ctas.load(std::memory_order_relaxed);
     if (cap > 0 && cap < sms) sms = cap;
-    if (!prefill2_registers_ok()) return FP8KV_ERR_UNSUPPORTED;
-    if (cudaFuncSetAttribute(prefill2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (!prefill2_registers_ok<kPT>()) return FP8KV_ERR_UNSUPPORTED;
+    if (cudaFuncSetAttribute(prefill2_kernel<kPT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Pre2Cfg::kSmemBytes) != cudaSuccess) {
         cudaGetLastError();
         return FP8KV_ERR_LAUNCH;
@@ -1314,7 +1427,7 @@ fp8kv_status launch_prefill2(const CUtensorMap &km, const CUtensorMap &vm, const
     const int64_t n_items = n_pairs * p.Hq * num_seqs;
     const dim3 grid = p.persist ? dim3(static_cast<unsigned>(n_items < sms ? n_items : sms))
                                 : dim3(static_cast<unsigned>(n_pairs), p.Hq, num_seqs);
-    prefill2_kernel<<<grid, kPre2Threads, Pre2Cfg::kSmemBytes, stream>>>(km, vm, p);
+    prefill2_kernel<kPT><<<grid, kPre2Threads, Pre2Cfg::kSmemBytes, stream>>>(km, vm, p);
     if (cudaGetLastError() != cudaSuccess) return FP8KV_ERR_LAUNCH;
     return FP8KV_OK;
 }
@@ -1340,15 +1453,16 @@ fp8kv_status launch_prefill(const CUtensorMap &km, const CUtensorMap &vm, const 
 
 using namespace fp8kv;
 
-extern "C" fp8kv_status attn_fp8_varlen_prefill(
-    const fp8kv_cache *cache, const fp8kv_bf16 *q, int32_t num_q_heads,
-    const int32_t *cu_seqlens_q, const int32_t *seq_lens_k, const int32_t *block_table,
-    int32_t max_blocks_per_seq, int32_t num_seqs, int32_t max_seqlen_q, float q_scale,
-    float k_scale, float v_scale, float softmax_scale, const fp8kv_bf16 *rel_bias,
-    int64_t bias_tok_stride, int32_t rel_extent, int32_t window, fp8kv_bf16 *out, void *workspace,
-    size_t workspace_bytes, void *stream) {
-    (void)workspace;
-    (void)workspace_bytes;
+namespace {
+// k_scales / v_scales non-null: the per-token variant (k_scale = v_scale = 1).
+fp8kv_status prefill_impl(const fp8kv_cache *cache, const fp8kv_bf16 *q, int32_t num_q_heads,
+                          const int32_t *cu_seqlens_q, const int32_t *seq_lens_k,
+                          const int32_t *block_table, int32_t max_blocks_per_seq, int32_t num_seqs,
+                          int32_t max_seqlen_q, float q_scale, float k_scale, float v_scale,
+                          float softmax_scale, const float *k_scales, const float *v_scales,
+                          const fp8kv_bf16 *rel_bias, int64_t bias_tok_stride, int32_t rel_extent,
+                          int32_t window, fp8kv_bf16 *out, void *stream) {
+    const bool per_token = k_scales != nullptr;
     if (!cache || num_seqs < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || window < 0 ||
         max_seqlen_q < 0)
         return FP8KV_ERR_ARG;
@@ -1363,6 +1477,9 @@ extern "C" fp8kv_status attn_fp8_varlen_prefill(
     if (num_seqs == 0 || max_seqlen_q == 0) return FP8KV_OK;
     if (!q || !cu_seqlens_q || !seq_lens_k || !block_table || !out || !cache->k || !cache->v)
         return FP8KV_ERR_ARG;
+    if (per_token && (D != 128 || !v_scales || (reinterpret_cast<uintptr_t>(k_scales) & 3) ||
+                      (reinterpret_cast<uintptr_t>(v_scales) & 3)))
+        return D != 128 ? FP8KV_ERR_UNSUPPORTED : FP8KV_ERR_ARG;
     if ((reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(out) & 15) ||
         (reinterpret_cast<uintptr_t>(cache->k) & 15) || (reinterpret_cast<uintptr_t>(cache->v) & 15))
         return FP8KV_ERR_ARG;
@@ -1404,10 +1521,45 @@ extern "C" fp8kv_status attn_fp8_varlen_prefill(
         const double c = 1.0 / (static_cast<double>(softmax_scale) * q_scale * k_scale);
         p.bias_fold = (c < 0x1p60 && c > 0x1p-60) ? static_cast<float>(c) : 0.0f;
     }
+    p.k_tok_scale = k_scales;
+    p.v_tok_scale = v_scales;
+    p.num_kv_heads = Hkv;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return D == 128 ? launch_prefill2(km, vm, p, num_seqs, sms, s)
+    if (per_token) return launch_prefill2<true>(km, vm, p, num_seqs, sms, s);
+    return D == 128 ? launch_prefill2<false>(km, vm, p, num_seqs, sms, s)
                     : launch_prefill<256>(km, vm, p, num_seqs, s);
 }
+}  // namespace
+
+extern "C" fp8kv_status attn_fp8_varlen_prefill(
+    const fp8kv_cache *cache, const fp8kv_bf16 *q, int32_t num_q_heads,
+    const int32_t *cu_seqlens_q, const int32_t *seq_lens_k, const int32_t *block_table,
+    int32_t max_blocks_per_seq, int32_t num_seqs, int32_t max_seqlen_q, float q_scale,
+    float k_scale, float v_scale, float softmax_scale, const fp8kv_bf16 *rel_bias,
+    int64_t bias_tok_stride, int32_t rel_extent, int32_t window, fp8kv_bf16 *out, void *workspace,
+    size_t workspace_bytes, void *stream) {
+    (void)workspace;
+    (void)workspace_bytes;
+    return prefill_impl(cache, q, num_q_heads, cu_seqlens_q, seq_lens_k, block_table,
+                        max_blocks_per_seq, num_seqs, max_seqlen_q, q_scale, k_scale, v_scale,
+                        softmax_scale, nullptr, nullptr, rel_bias, bias_tok_stride, rel_extent,
+                        window, out, stream);
+}
+
+extern "C" fp8kv_status attn_fp8_varlen_prefill_per_token(
+    const fp8kv_cache *cache, const fp8kv_bf16 *q, int32_t num_q_heads,
+    const int32_t *cu_seqlens_q, const int32_t *seq_lens_k, const int32_t *block_table,
+    int32_t max_blocks_per_seq, int32_t num_seqs, int32_t max_seqlen_q, float q_scale,
+    float softmax_scale, const float *k_scales, const float *v_scales, const fp8kv_bf16 *rel_bias,
+    int64_t bias_tok_stride, int32_t rel_extent, int32_t window, fp8kv_bf16 *out, void *stream) {
+    if (num_seqs > 0 && max_seqlen_q > 0 && (!k_scales || !v_scales)) return FP8KV_ERR_ARG;
+    // the per-token scales replace k_scale and v_scale (1 in the fold and the epilogue)
+    return prefill_impl(cache, q, num_q_heads, cu_seqlens_q, seq_lens_k, block_table,
+                        max_blocks_per_seq, num_seqs, max_seqlen_q, q_scale, 1.0f, 1.0f,
+                        softmax_scale, k_scales ? k_scales : nullptr, v_scales, rel_bias,
+                        bias_tok_stride, rel_extent, window, out, stream);
+}
+
 
 extern "C" fp8kv_status fp8kv_set_prefill_max_ctas(int32_t max_ctas) {
     if (max_ctas < 0) return FP8KV_ERR_ARG;

@@ -318,6 +318,34 @@ fp8kv_status paged_attn_fp8_decode_per_token(const fp8kv_cache *cache, const fp8
                                              void *stream);
 
 /*
+ * attn_fp8_varlen_prefill_per_token -- attn_fp8_varlen_prefill over a cache
+ * written by kv_store_e4m3_per_token (local-inference-lab/vllm PR 189: a
+ * per-token scale stored with each cached token, read by decode and by the
+ * chunked prefill over the cached prefix): key j of a sequence is
+ * k_j = k_scales[j] * dec(k8_j) and v_j = v_scales[j] * dec(v8_j) (its
+ * block's entries of the scale arrays), so the score is
+ * softmax_scale * q_scale * k_scales[j] * (q8 . k8_j) (+ bias) and the
+ * output sum_j softmax_j * v_scales[j] * v8_j.  In the kernel the V scale is
+ * folded into the exponent of P (P_j = p_j * v_scales[j]), the row sum adds
+ * P_j / v_scales[j], and P is always kept in two e4m3 terms.
+ * k_scales, v_scales: device float[num_blocks][num_kv_heads][block_size],
+ *                4-byte aligned, finite and > 0 where the sequences' keys
+ *                are (kv_store_e4m3_per_token writes such values).
+ * Other arguments and the result are those of attn_fp8_varlen_prefill (no
+ * workspace).  head_dim 128 only (FP8KV_ERR_UNSUPPORTED for 256).
+ */
+fp8kv_status attn_fp8_varlen_prefill_per_token(const fp8kv_cache *cache, const fp8kv_bf16 *q,
+                                               int32_t num_q_heads, const int32_t *cu_seqlens_q,
+                                               const int32_t *seq_lens_k,
+                                               const int32_t *block_table,
+                                               int32_t max_blocks_per_seq, int32_t num_seqs,
+                                               int32_t max_seqlen_q, float q_scale,
+                                               float softmax_scale, const float *k_scales,
+                                               const float *v_scales, const fp8kv_bf16 *rel_bias,
+                                               int64_t bias_tok_stride, int32_t rel_extent,
+                                               int32_t window, fp8kv_bf16 *out, void *stream);
+
+/*
  * kv_band_counts -- clip and flush-to-zero counters and the round-trip error
  * of quantizing the stored values at one scale: the KV value-range
  * instrument of vLLM PR 54705 (evidence document, Tier 2: exact e4m3 band

@@ -294,3 +294,24 @@ def test_decode_bindings_check_table_and_lengths(lib):
         for t, n, exc in bad:
             with pytest.raises(exc):
                 call(t, n)
+
+
+def test_per_token_prefill_rejects_bad_arguments_on_host(lib):
+    f = _c(lib).attn_fp8_varlen_prefill_per_token
+    cache = lib.CacheStruct(16, 16, 4, 16, 2, 128)   # fake pointers, never dereferenced
+    # (cache, q, Hq, cu, lens_k, bt, mb, B, maxq, q_scale, softmax_scale, k_sc, v_sc, rel,
+    #  bstride, E, window, out, stream)
+    args = [ctypes.byref(cache), 16, 8, 16, 16, 16, 4, 1, 16, 1.0, 0.1, 16, 16, None, 0, 0, 0, 16,
+            None]
+    for i, bad, want in ((11, None, lib.ERR_ARG), (12, None, lib.ERR_ARG), (11, 18, lib.ERR_ARG),
+                         (9, float("nan"), lib.ERR_SCALE), (10, 0.0, lib.ERR_SCALE)):
+        a = list(args)
+        a[i] = bad
+        assert f(*a) == want, (i, bad)
+    a = list(args)
+    a[7], a[11], a[12] = 0, None, None
+    assert f(*a) == lib.OK                                             # nothing to do
+    d256 = lib.CacheStruct(16, 16, 4, 16, 2, 256)
+    a = list(args)
+    a[0] = ctypes.byref(d256)
+    assert f(*a) == lib.ERR_UNSUPPORTED

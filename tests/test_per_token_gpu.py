@@ -129,3 +129,95 @@ def test_decode_head_dim_256_block_32(fk, oracle_lib):
 
 def test_decode_sixteen_heads_per_kv_head(fk, oracle_lib):
     run_decode(fk, oracle_lib, [77, 400], 32, 2, 128, 16, seed=4)
+
+
+def run_prefill(fk, oracle_lib, q_lens, k_lens, Hq, Hkv, window=0, E=0, v_dist="normal", seed=0,
+                q_scale=1.0, rows_per_seq=None, caps=(0,)):
+    """Per-token prefill (chunks over cached prefixes) against the oracle's
+    per-token attention: all rows, or rows_per_seq sampled rows per sequence;
+    the output must not depend on the CTA cap."""
+    g = torch.Generator().manual_seed(seed)
+    kv = workloads.make_paged_kv(k_lens, Hkv, 128, 16, g=g, device="cpu", v_dist=v_dist)
+    Tq = sum(q_lens)
+    q = workloads.draw_values((Tq, Hq, 128), "normal", g, "cpu")
+    rel = None
+    if E:
+        rel = (0.5 * torch.randn((Tq, Hq, E), generator=g)).to(torch.bfloat16)
+    cu = [0]
+    for n in q_lens:
+        cu.append(cu[-1] + n)
+    cache, ks, vs, kd = store(fk, kv, Hkv, 128, 16)
+    outs = []
+    try:
+        for cap in caps:
+            fk.set_prefill_max_ctas(cap)
+            outs.append(fk.attn_fp8_varlen_prefill_per_token(
+                cache, q.to(DEV), torch.tensor(cu, dtype=torch.int32, device=DEV), kd.seq_lens,
+                kd.block_table, max(q_lens), q_scale, ks, vs,
+                rel_bias=None if rel is None else rel.to(DEV), window=window))
+            torch.cuda.synchronize()
+            assert fk.device_error() == 0
+    finally:
+        fk.set_prefill_max_ctas(0)
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+    got = outs[0].float().cpu().numpy()
+    assert np.isfinite(got).all()
+    G = Hq // Hkv
+    starts = kv.tok_start.tolist()
+    rng = np.random.default_rng(seed)
+    rows, refs = [], []
+    memo = {}
+    for b, n in enumerate(q_lens):
+        picks = range(n) if rows_per_seq is None else sorted(
+            {0, n - 1} | set(int(x) for x in rng.integers(0, n, rows_per_seq)))
+        for i in picks:
+            h = int(rng.integers(Hq))
+            kvh = h // G
+            if (b, kvh) not in memo:
+                s, L = starts[b], k_lens[b]
+                k8, sk = oracle_lib.quantize_per_token(bits(kv.k[s:s + L, kvh]), 128)
+                v8, sv = oracle_lib.quantize_per_token(bits(kv.v[s:s + L, kvh]), 128)
+                memo[(b, kvh)] = (k8, sk, v8, sv)
+            k8, sk, v8, sv = memo[(b, kvh)]
+            t = cu[b] + i
+            q8 = oracle_lib.quantize(bits(q[t, h]), q_scale)
+            bias = None if rel is None else bits(rel[t, h])
+            refs.append(oracle_lib.attend_row_pt(q8, k8, v8, sk, sv, k_lens[b] - n + i,
+                                                 1 / math.sqrt(128), q_scale, bias=bias,
+                                                 window=window))
+            rows.append((t, h))
+    assert_close(np.stack([got[t, h] for t, h in rows]), np.stack(refs), "per-token prefill")
+
+
+def test_prefill_ragged_fresh_chunks(fk, oracle_lib):
+    """Fresh chunks (queries = keys), ragged tiles, heavy-tailed V with a planted
+    1,272, every row."""
+    run_prefill(fk, oracle_lib, [1, 127, 129, 300], [1, 127, 129, 300], 8, 2, E=128,
+                v_dist="v_t3", seed=5, caps=(0, 1, 3))
+
+
+def test_prefill_chunks_over_cached_prefixes(fk, oracle_lib):
+    run_prefill(fk, oracle_lib, [64, 200, 5], [500, 777, 40], 8, 2, E=1024, seed=6, q_scale=0.5)
+
+
+def test_prefill_sliding_window(fk, oracle_lib):
+    run_prefill(fk, oracle_lib, [700, 50], [900, 50], 8, 1, window=512, E=128, seed=7,
+                rows_per_seq=40)
+
+
+def test_prefill_long_chunk_sampled(fk, oracle_lib):
+    """A 2,048-query chunk over 4,000 keys, sampled rows."""
+    run_prefill(fk, oracle_lib, [2048], [4000], 32, 4, E=128, seed=8, rows_per_seq=48)
+
+
+def test_prefill_per_token_rejects_head_dim_256(fk):
+    cache = fk.KVCache.empty(4, 16, 1, 256, device=DEV)
+    ks = torch.ones((4, 1, 16), dtype=torch.float32, device=DEV)
+    q = torch.zeros(4, 2, 256, dtype=torch.bfloat16, device=DEV)
+    cu = torch.tensor([0, 4], dtype=torch.int32, device=DEV)
+    lens = torch.tensor([4], dtype=torch.int32, device=DEV)
+    bt = torch.zeros(1, 4, dtype=torch.int32, device=DEV)
+    with pytest.raises(fk.Fp8KVError) as e:
+        fk.attn_fp8_varlen_prefill_per_token(cache, q, cu, lens, bt, 4, 1.0, ks, ks)
+    assert e.value.status == fk.ERR_UNSUPPORTED
