@@ -490,6 +490,44 @@ def bench_prefill(fk, dev, steps, warmup, world, only_group=None, cpu_budget=0.0
     return res
 
 
+def bench_prefill_per_token(fk, dev, steps, warmup, world):
+    """The prefill chunk's two groups (causal, 512-window) over a cache written
+    by kv_store_e4m3_per_token; the store is outside the timed calls."""
+    spec = workloads.PREFILL_16K
+    inp = workloads.make_prefill(spec, device=dev, seed=0)
+    kv = inp["kv"]
+    cache = fk.KVCache.empty(kv.num_blocks, kv.block_size, spec.Hkv, spec.D, device=dev)
+    ks = torch.empty((kv.num_blocks, spec.Hkv, kv.block_size), dtype=torch.float32, device=dev)
+    vs = torch.empty_like(ks)
+    fk.kv_store_e4m3_per_token(cache, kv.k, kv.v, kv.slot_mapping, ks, vs)
+    q_lens = inp["q_lens"]
+    half = spec.n_seqs // 2
+    cu = inp["cu_seqlens_q"].tolist()
+    groups, flops = [], 0
+    for gi, (lo, hi) in enumerate([(0, half), (half, spec.n_seqs)]):
+        w = spec.windows[gi]
+        groups.append(dict(window=w, q=inp["q"][cu[lo]:cu[hi]],
+                           cu=torch.tensor([c - cu[lo] for c in cu[lo:hi + 1]], dtype=torch.int32,
+                                           device=dev),
+                           lens=kv.seq_lens[lo:hi].contiguous(), bt=kv.block_table[lo:hi].contiguous(),
+                           rel=inp["rel"][cu[lo]:cu[hi]], out=torch.empty_like(inp["q"][cu[lo]:cu[hi]]),
+                           maxq=max(q_lens[lo:hi])))
+        flops += 4 * spec.Hq * spec.D * sum(sum(min(i + 1, w) if w else i + 1 for i in range(L))
+                                            for L in q_lens[lo:hi])
+
+    def step():
+        for g in groups:
+            fk.attn_fp8_varlen_prefill_per_token(cache, g["q"], g["cu"], g["lens"], g["bt"],
+                                                 g["maxq"], 1.0, ks, vs, rel_bias=g["rel"],
+                                                 window=g["window"], out=g["out"])
+    ms = time_steps(step, steps, warmup, world)
+    fp8_peak = 2.0 * peaks()["bf16_tflops"]
+    return {"workload": spec.name + "_per_token_scales", "ms_per_step": ms,
+            "tflops": flops / ms / 1e9,
+            "roofline": {"bound": "tensor", "achieved": flops / ms / 1e9, "peak": fp8_peak,
+                         "unit": "TFLOP/s", "frac": flops / ms / 1e9 / fp8_peak}}
+
+
 def bench_chunked_prefill(fk, dev, steps, warmup, world, cpu_budget=0.0):
     """One 4,096-query chunk attending over 65,536 keys (a cached prefix)."""
     spec = workloads.PREFILL_CHUNK_64K
@@ -685,11 +723,28 @@ def main():
     ap.add_argument("--profile-prefill", type=int, default=0, metavar="GROUP",
                     help="profiling case: only the prefill call of group GROUP-1 (1 = the "
                          "causal sequences, 2 = the 512-window ones) of the prefill chunk")
+    ap.add_argument("--only-extra", default="",
+                    help="run only the named secondary workload (per_token_decode, "
+                         "per_token_prefill, window_decode) and print its JSON")
     ap.add_argument("--profile-store", action="store_true",
                     help="profiling case: only the quant-on-store of the 64-sequence pool and the "
                          "band counters over its V, no JSON contract line")
     args = ap.parse_args()
     rank, world = dist_setup(args.gpus)
+    if args.only_extra:
+        import dataclasses
+        import fp8_e4m3_kv_gb300 as fk
+        dev = torch.device("cuda", torch.cuda.current_device())
+        spec = workloads.DECODE_32K
+        fn = {"per_token_decode": lambda: bench_decode_per_token(fk, dev, args.steps, args.warmup,
+                                                                 world),
+              "per_token_prefill": lambda: bench_prefill_per_token(fk, dev, args.steps,
+                                                                   args.warmup, world),
+              "window_decode": lambda: bench_decode_extra(
+                  fk, dataclasses.replace(spec, window=512), dev, args.steps, args.warmup, world,
+                  label=spec.name + "_window512")}[args.only_extra]
+        print(json.dumps(fn()))
+        return
     if args.profile_store:
         import fp8_e4m3_kv_gb300 as fk
         dev = torch.device("cuda", torch.cuda.current_device())
@@ -798,6 +853,7 @@ def main():
         for fn in (lambda: bench_prefill(fk, dev, args.steps, args.warmup, world, cpu_budget=cb),
                    lambda: bench_chunked_prefill(fk, dev, max(3, args.steps // 4), args.warmup,
                                                  world, cpu_budget=cb),
+                   lambda: bench_prefill_per_token(fk, dev, args.steps, args.warmup, world),
                    lambda: bench_store_and_bands(fk, dev, args.steps, args.warmup, world,
                                                  cpu_budget=cb),
                    lambda: bench_decode_per_token(fk, dev, args.steps, args.warmup, world,

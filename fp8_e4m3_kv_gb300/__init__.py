@@ -77,6 +77,7 @@ _band_counts = _sig("kv_band_counts", ctypes.c_int, [P, i64, P, i64, i32, f32, P
 _scale_from_amax = _sig("fp8kv_scale_from_amax", ctypes.c_int, [f32, i32, ctypes.POINTER(f32)])
 _cache_bytes = _sig("fp8kv_cache_bytes", sz, [i64, i32, i32, i32])
 _prefill_max_ctas = _sig("fp8kv_set_prefill_max_ctas", ctypes.c_int, [i32])
+_drop_first_copy = _sig("fp8kv_test_drop_first_copy", ctypes.c_int, [i32])
 _device_error = _sig("fp8kv_device_error", ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), i32])
 _status_string = _sig("fp8kv_status_string", ctypes.c_char_p, [ctypes.c_int])
 
@@ -88,6 +89,7 @@ EXPORTED = ("kv_store_e4m3", "paged_attn_fp8_decode", "paged_attn_fp8_decode_ex"
             "fp8kv_set_prefill_max_ctas", "kv_amax_calibrate",
             "kv_band_counts",
             "fp8kv_scale_from_amax", "fp8kv_cache_bytes", "fp8kv_device_error",
+            "fp8kv_test_drop_first_copy",
             "fp8kv_status_string")
 
 
@@ -493,6 +495,12 @@ def attn_fp8_varlen_prefill_per_token(cache: KVCache, q: torch.Tensor, cu_seqlen
 def set_prefill_max_ctas(max_ctas: int) -> None:
     """Caps the CTAs of the persistent head_dim-128 prefill (0: one per SM)."""
     _check(_prefill_max_ctas(int(max_ctas)), "fp8kv_set_prefill_max_ctas")
+
+
+def test_drop_first_copy(on: bool = True) -> None:
+    """Test hook: the next decode launch skips each CTA's first key-tile copy,
+    so its bounded wait runs out (see include/fp8kv.h)."""
+    _check(_drop_first_copy(1 if on else 0), "fp8kv_test_drop_first_copy")
 
 
 def device_error(clear: bool = True) -> int:

@@ -28,6 +28,7 @@
 // v_scale * o / l in bf16.
 #include <math.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -36,6 +37,7 @@ namespace fp8kv {
 namespace {
 
 constexpr int kNPad = 16;          // query heads per KV head, padded to the MMA N
+constexpr float kMinLog2VScale = -60.0f;   // per-token V scales folded into exponents
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Consumer warpgroups, pipeline depth, keys per tile and resident CTAs per SM
@@ -132,6 +134,15 @@ struct DecodeParams {
     // float[num_blocks][num_kv_heads][block_size], one per cached token and head
     const float *k_tok_scale;
     const float *v_tok_scale;
+    // test hook (fp8kv_test_drop_first_copy): the producer issues neither
+    // the copy nor the expected-bytes arrival of its first key tile, so the
+    // MMA warp's wait for that tile runs out
+    int32_t drop_first_copy;
+    // one split per (sequence, KV head): the decode kernel writes
+    // out = bf16(v_scale * o / l) itself, the merge's arithmetic for one split
+    uint16_t *out;
+    float out_scale;    // v_scale (1 for per-token scales)
+    int32_t direct_out;
 };
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -215,9 +226,11 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
-// kPT: per-token scales.  Key j's score is multiplied by its K scale; its P
-// by its V scale relative to the tile's largest V scale S (so P stays in the
-// e4m3 range), and the tile's O^T by S when it is accumulated.
+// kPT: per-token scales.  Key j's score is multiplied by its K scale, and
+// its V scale is folded into the exponent: z_j + log2(v_scale_j) takes part
+// in the block-wide max like any score, so P_j = 2^(z_j + log2 v_scale_j -
+// m + 8) <= 2^8 is p_j * v_scale_j (up to the common factor) and the row
+// sum adds P_j / v_scale_j.
 template <int D, int GMAX, bool kPT>
 __global__ void __launch_bounds__(DecCfg<D>::kThreads, DecCfg<D>::kCtasPerSm)
 decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
@@ -226,7 +239,6 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
     constexpr int HS = C::kHS;
     constexpr int GH = GMAX / HS;                      // heads per consumer warpgroup
     static_assert(GH * HS == GMAX && GH % 2 == 0, "head split: an even number of heads per warpgroup");
-    static_assert(!kPT || GH < 16, "the per-token variant keeps the V-scale max in head slot 15");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -246,6 +258,11 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
     const int ntiles = static_cast<int>(t_end - t0 < p.split_tiles ? t_end - t0 : p.split_tiles);
 
     if (ntiles <= 0) {   // nothing to attend in this split: mark it empty
+        if (p.direct_out) {   // the only split: the output is zero
+            for (int e = threadIdx.x; e < p.G * D; e += blockDim.x)
+                p.out[(static_cast<int64_t>(b) * p.Hq + h0 + e / D) * D + e % D] = 0;
+            return;
+        }
         if (threadIdx.x < p.G) {
             float *ml = p.part_ml + ((static_cast<int64_t>(b) * p.Hq + h0 + threadIdx.x) *
                                          p.num_slots + split) * 2;
@@ -371,6 +388,7 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
             if (lane == 0) ok = mbar_wait(&empty[s], ((i / C::kStages) & 1) ^ 1, fail, p.err);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
+            if (i == 0 && p.drop_first_copy) continue;
             if (lane == 0) mbar_arrive_expect_tx(&full[s], C::kStageBytes);
             __syncwarp();
             if (lane < nb) {
@@ -481,7 +499,7 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
         }
         // Accumulate this warpgroup's heads of O^T of tile j (rescaled) into
         // the registers.
-        auto take_o = [&](int j, const float *alpha, float sfac) -> bool {
+        auto take_o = [&](int j, const float *alpha) -> bool {
             const int ob = j % C::kOBuf;
             if (!warp_wait(&o_full[ob], (j / C::kOBuf) & 1, fail, p.err)) return false;
             tc_fence_after_sync();
@@ -491,7 +509,7 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
                 tmem_ld_x16(tmem + lane_base + C::kColO + (ob * C::kCB + mh) * kNPad + gbase, o);
 #pragma unroll
                 for (int g = 0; g < GH; ++g)
-                    o_acc[mh][g] = fmaf(o_acc[mh][g], alpha[g], kPT ? o[g] * sfac : o[g]);
+                    o_acc[mh][g] = fmaf(o_acc[mh][g], alpha[g], o[g]);
             }
             tc_fence_before_sync();
             __syncwarp();
@@ -499,27 +517,47 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
             return true;
         };
 
-        float s_1 = 1.0f, s_2 = 1.0f;   // V-scale factors of tiles j - 1, j - 2 (kPT)
+        // kPT: the raw scales of this thread's keys of tile i (ksc, vsc),
+        // loaded a tile ahead so that their latency stays off the chain
+        float ksc[C::kKB], vsc[C::kKB];
+        auto load_scales = [&](int i) {
+#pragma unroll
+            for (int kb = 0; kb < C::kKB; ++kb) {
+                const int64_t key = (t0 + i) * C::kKeys + kb * 128 + t;
+                const int64_t lb = key / p.block_size;
+                ksc[kb] = 1.0f;
+                vsc[kb] = 0.0f;   // marks a key that is not visible
+                if (i < ntiles && key < len && key >= lo && lb < p.max_blocks) {
+                    const int32_t id =
+                        __ldg(p.block_table + static_cast<int64_t>(b) * p.max_blocks + lb);
+                    if (id >= 0 && id < p.num_blocks) {
+                        const int64_t si = (static_cast<int64_t>(id) * p.num_kv_heads + kvh) *
+                                               p.block_size + key % p.block_size;
+                        ksc[kb] = __ldg(p.k_tok_scale + si);
+                        vsc[kb] = __ldg(p.v_tok_scale + si);
+                    }
+                }
+            }
+        };
+        if constexpr (kPT) load_scales(0);
         for (int i = 0; i < ntiles; ++i) {
-            // per-token scales of this thread's keys (0 where not visible)
-            float tsk[C::kKB], tsv[C::kKB];
+            // per-token factors of this thread's keys: K scale, log2 and
+            // reciprocal of the V scale (1, 0, 0 where not visible; the
+            // score of such a key is -inf anyway)
+            float tsk[C::kKB], tlv[C::kKB], tiv[C::kKB];
             if constexpr (kPT) {
 #pragma unroll
                 for (int kb = 0; kb < C::kKB; ++kb) {
-                    const int64_t key = (t0 + i) * C::kKeys + kb * 128 + t;
-                    const int64_t lb = key / p.block_size;
-                    tsk[kb] = tsv[kb] = 0.0f;
-                    if (key < len && key >= lo && lb < p.max_blocks) {
-                        const int32_t id =
-                            __ldg(p.block_table + static_cast<int64_t>(b) * p.max_blocks + lb);
-                        if (id >= 0 && id < p.num_blocks) {
-                            const int64_t si = (static_cast<int64_t>(id) * p.num_kv_heads + kvh) *
-                                                   p.block_size + key % p.block_size;
-                            tsk[kb] = __ldg(p.k_tok_scale + si);
-                            tsv[kb] = __ldg(p.v_tok_scale + si);
-                        }
-                    }
+                    const float sv = vsc[kb];
+                    const float lv = log2f(sv);
+                    tsk[kb] = ksc[kb];
+                    // below 2^-60 the exponent takes 2^-60 (and the sum its
+                    // reciprocal): P stays far from fp32 underflow, at an
+                    // error below p * 2^-60 * 448
+                    tlv[kb] = sv > 0.0f ? fmaxf(lv, kMinLog2VScale) : 0.0f;
+                    tiv[kb] = sv > 0.0f ? (lv > kMinLog2VScale ? __frcp_rn(sv) : 0x1p60f) : 0.0f;
                 }
+                load_scales(i + 1);   // the next tile's, in flight during this one
             }
             if (!warp_wait(&s_full[i & 1], (i >> 1) & 1, fail, p.err)) { ok = false; break; }
             tc_fence_after_sync();
@@ -545,7 +583,8 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
                 for (int g = 0; g < GH; ++g) {
                     float zz = -INFINITY;
                     if (valid && gbase + g < p.G) {
-                        zz = sc[kb][g] * (kPT ? p.score_log2 * tsk[kb] : p.score_log2);
+                        zz = kPT ? fmaf(sc[kb][g], p.score_log2 * tsk[kb], tlv[kb])
+                                 : sc[kb][g] * p.score_log2;
                         if (has_bias)
                             zz = fmaf(bf16_bits_to_float(__ldg(bias + g * p.rel_extent + dist)),
                                       kLog2e, zz);
@@ -564,24 +603,10 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
                 mx = warp_max(mx);
                 if (lane == 0) rb[wq * 16 + g] = mx;
             }
-            if constexpr (kPT) {
-                float mv = tsv[0];
-#pragma unroll
-                for (int kb = 1; kb < C::kKB; ++kb) mv = fmaxf(mv, tsv[kb]);
-                mv = warp_max(mv);
-                if (lane == 0) rb[wq * 16 + 15] = mv;
-            }
             __syncwarp();
             if (lane == 0) mbar_arrive(&red_bar[i & 1]);
             if (!warp_wait(&red_bar[i & 1], (i >> 1) & 1, fail, p.err)) { ok = false; break; }
             float alpha[GH], neg_m8[GH];
-            // kPT: the tile's largest V scale, and each key's V scale relative to it
-            float s_tile = 1.0f, vr[C::kKB];
-            if constexpr (kPT) {
-                s_tile = fmaxf(fmaxf(rb[15], rb[31]), fmaxf(rb[47], rb[63]));
-#pragma unroll
-                for (int kb = 0; kb < C::kKB; ++kb) vr[kb] = s_tile > 0.0f ? tsv[kb] / s_tile : 0.0f;
-            }
             uint8_t *phi = smem + C::kOffP + (i % C::kOBuf) * 2 * C::kPBytes;
             uint8_t *plo = phi + C::kPBytes;
 #pragma unroll
@@ -605,10 +630,14 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
                 for (int kb = 0; kb < C::kKB; ++kb) {
                     const float p0 = ex2_approx(z[kb][g] + neg_m8[g]);
                     const float p1 = ex2_approx(z[kb][g + 1] + neg_m8[g + 1]);
-                    ls0 += p0;
-                    ls1 += p1;
-                    const __half2 ph =
-                        kPT ? __floats2half2_rn(p0 * vr[kb], p1 * vr[kb]) : __floats2half2_rn(p0, p1);
+                    if constexpr (kPT) {   // the row sum takes P / v_scale
+                        ls0 = fmaf(p0, tiv[kb], ls0);
+                        ls1 = fmaf(p1, tiv[kb], ls1);
+                    } else {
+                        ls0 += p0;
+                        ls1 += p1;
+                    }
+                    const __half2 ph = __floats2half2_rn(p0, p1);
                     const uint32_t h8 = __nv_cvt_halfraw2_to_fp8x2(ph, __NV_SATFINITE, __NV_E4M3);
                     const __half2 hh = e4m3x2_to_half2(static_cast<uint16_t>(h8));
                     const uint32_t l8 =
@@ -643,17 +672,15 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_full[i % C::kOBuf]);
-            if (i >= 2 && !take_o(i - 2, alpha_2, s_2)) { ok = false; break; }
+            if (i >= 2 && !take_o(i - 2, alpha_2)) { ok = false; break; }
 #pragma unroll
             for (int g = 0; g < GH; ++g) {
                 alpha_2[g] = alpha_1[g];
                 alpha_1[g] = alpha[g];
             }
-            s_2 = s_1;
-            s_1 = s_tile;
         }
-        if (ok && ntiles >= 2) ok = take_o(ntiles - 2, alpha_2, s_2);
-        if (ok && ntiles >= 1) ok = take_o(ntiles - 1, alpha_1, s_1);
+        if (ok && ntiles >= 2) ok = take_o(ntiles - 2, alpha_2);
+        if (ok && ntiles >= 1) ok = take_o(ntiles - 1, alpha_1);
 
         // l per head: sum of the thread partials of the warpgroup
 #pragma unroll
@@ -664,8 +691,24 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
         __syncwarp();
         if (lane == 0) mbar_arrive(l_bar);
         if (!warp_wait(l_bar, 0, fail, p.err)) ok = false;
+        if (p.direct_out) {
+            // the only split: out = bf16(v_scale * o / l), as the merge computes it
+#pragma unroll
+            for (int g = 0; g < GH; ++g) {
+                if (gbase + g < p.G) {
+                    const float L = lred[g] + lred[16 + g] + lred[32 + g] + lred[48 + g];
+                    const bool live = ok && m_run[g] != -INFINITY;
+                    const float f = (live && L > 0.0f) ? p.out_scale / L : 0.0f;
+                    uint16_t *o = p.out + (static_cast<int64_t>(b) * p.Hq + h0 + gbase + g) * D;
+#pragma unroll
+                    for (int mh = 0; mh < C::kCB; ++mh)
+                        o[mh * 128 + t] = __bfloat16_as_ushort(
+                            __float2bfloat16_rn((live ? o_acc[mh][g] : 0.0f) * f));
+                }
+            }
+        }
         const int64_t row0 = (static_cast<int64_t>(b) * p.Hq + h0 + gbase) * p.num_slots + split;
-        if (t == 0) {
+        if (!p.direct_out && t == 0) {
 #pragma unroll
             for (int g = 0; g < GH; ++g) {
                 if (gbase + g < p.G) {
@@ -676,7 +719,7 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
             }
         }
 #pragma unroll
-        for (int g = 0; g < GH; ++g) {
+        for (int g = 0; g < GH && !p.direct_out; ++g) {
             if (gbase + g < p.G) {
                 float *po = p.part_o + (row0 + static_cast<int64_t>(g) * p.num_slots) * D;
 #pragma unroll
@@ -848,6 +891,9 @@ extern "C" size_t fp8kv_decode_workspace_size(int32_t num_seqs, int32_t num_q_he
 }
 
 namespace {
+// One-shot request of fp8kv_test_drop_first_copy, taken by the next decode launch.
+std::atomic<int> g_drop_first_copy{0};
+
 // The step's new tokens, stored by the decode launch itself.
 struct FusedStore {
     const fp8kv_bf16 *k_new;
@@ -943,6 +989,10 @@ fp8kv_status decode_impl(const fp8kv_cache *cache, const fp8kv_bf16 *q, int32_t 
     p.v_scale = make_qscale(v_scale);
     p.k_tok_scale = pt ? pt->k_scales : nullptr;
     p.v_tok_scale = pt ? pt->v_scales : nullptr;
+    p.drop_first_copy = g_drop_first_copy.exchange(0, std::memory_order_relaxed);
+    p.out = out;
+    p.out_scale = v_scale;
+    p.direct_out = slots == 1 ? 1 : 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (pt) {
         if (D == 128)
@@ -959,6 +1009,7 @@ fp8kv_status decode_impl(const fp8kv_cache *cache, const fp8kv_bf16 *q, int32_t 
                     : launch_decode<256, 16, false>(km, vm, p, Hkv, num_seqs, s);
     }
     if (st != FP8KV_OK) return st;
+    if (p.direct_out) return FP8KV_OK;   // one split: the decode kernel wrote out
     if (D == 128)
         decode_merge_kernel<128><<<dim3(num_q_heads, num_seqs), kMergeWarps * 32, 0, s>>>(
             p.part_o, p.part_ml, out, num_q_heads, slots, v_scale);
@@ -1009,6 +1060,11 @@ extern "C" fp8kv_status paged_attn_fp8_decode_per_token(
     return decode_impl(cache, q, num_q_heads, block_table, max_blocks_per_seq, seq_lens, num_seqs,
                        q_scale, 1.0f, 1.0f, softmax_scale, rel_bias, bias_tok_stride, rel_extent,
                        window, out, workspace, workspace_bytes, 0, nullptr, &pt, stream);
+}
+
+extern "C" fp8kv_status fp8kv_test_drop_first_copy(int32_t on) {
+    g_drop_first_copy.store(on ? 1 : 0, std::memory_order_relaxed);
+    return FP8KV_OK;
 }
 
 extern "C" fp8kv_status paged_attn_fp8_decode(

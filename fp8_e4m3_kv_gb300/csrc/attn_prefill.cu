@@ -876,9 +876,13 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
                                 const int64_t si = (static_cast<int64_t>(id) * p.num_kv_heads + kvh) *
                                                        p.block_size + key % p.block_size;
                                 const float sv = __ldg(p.v_tok_scale + si);
+                                const float lv = log2f(sv);
                                 fkp[i] = p.score_log2 * __ldg(p.k_tok_scale + si);
-                                lvp[i] = log2f(sv);
-                                ivp[i] = __frcp_rn(sv);
+                                // below 2^-60 the exponent takes 2^-60 (and the
+                                // sum its reciprocal): P stays far from fp32
+                                // underflow, at an error below p * 2^-60 * 448
+                                lvp[i] = fmaxf(lv, -60.0f);
+                                ivp[i] = lv > -60.0f ? __frcp_rn(sv) : 0x1p60f;
                             }
                         }
                     }

@@ -301,9 +301,10 @@ fp8kv_status kv_store_e4m3_per_token(const fp8kv_cache *cache, const fp8kv_bf16 
  * k_j = k_scales[j] * dec(k8_j) and v_j = v_scales[j] * dec(v8_j) (its
  * block's entries of the scale arrays), so the score is
  * softmax_scale * q_scale * k_scales[j] * (q8 . k8_j) (+ bias) and the output
- * sum_j P_j * v_scales[j] * v8_j.  In the kernel P_j is multiplied by
- * v_scales[j] / S, S the largest V scale of its 128-key tile, before the
- * two-term e4m3 split (P stays in range), and the tile's partial O by S.
+ * sum_j P_j * v_scales[j] * v8_j.  In the kernel the V scale is folded into
+ * the exponent of P (z_j + log2 v_scales[j] takes part in the running max,
+ * so P_j = p_j * v_scales[j] up to a common factor stays in the e4m3 range)
+ * and the row sum adds P_j / v_scales[j].
  * Other arguments, the workspace (fp8kv_decode_workspace_size with
  * split_tokens 0) and the result are those of paged_attn_fp8_decode.
  */
@@ -416,6 +417,20 @@ fp8kv_status fp8kv_scale_from_amax(float amax, int32_t rule, float *scale);
 /* Bytes of one cache array (K or V): num_blocks*block_size*num_kv_heads*head_dim. */
 size_t fp8kv_cache_bytes(int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
                          int32_t head_dim);
+
+/*
+ * fp8kv_test_drop_first_copy -- test hook for the failure path of the
+ * kernels' bounded waits.  With on != 0, the next paged_attn_fp8_decode*
+ * launch (one launch only; the request is then cleared) has each CTA's
+ * producer skip the TMA copy of its first key tile and the expected-bytes
+ * arrival that goes with it.  The MMA warp's wait for that tile then runs
+ * out after the wait limit (2 s), the CTA gives up with no copy or MMA in
+ * flight, frees its tensor memory and finishes; the call returns normally,
+ * its output is unspecified, and the device error word gets
+ * FP8KV_DEVERR_WAIT_TIMEOUT.  Nothing faults, traps or hangs, and later
+ * calls are unaffected.  on = 0 withdraws a pending request.
+ */
+fp8kv_status fp8kv_test_drop_first_copy(int32_t on);
 
 /* Reads (and with clear != 0 resets) the current device's error word.
  * Synchronizes the device. */

@@ -199,3 +199,35 @@ def test_full_decode_128k_calibrated_d256(fk):
 
 def test_full_decode_1m(fk):
     _full(fk, workloads.DECODE_1M, (0, 8))
+
+
+def test_bounded_wait_runs_out_and_the_next_call_is_clean(fk):
+    """The failure path of a bounded wait, made to happen: the test hook makes
+    the decode producer skip its first tile's copy (nothing else changes), so
+    the MMA warp's wait for it runs out.  The call returns, the error word
+    says FP8KV_DEVERR_WAIT_TIMEOUT, and the next call in the same process is
+    clean and matches the oracle."""
+    import time
+    lens, Hq, Hkv = [100], 4, 1            # one key tile, one CTA
+    spec = workloads.DecodeSpec("case", B=1, Hq=Hq, Hkv=Hkv, D=128, block_size=16, ctx_lo=1,
+                                ctx_hi=1)
+    inp = workloads.make_decode(spec, device="cpu", seed=40, lens=lens)
+    kd = to_device(inp["kv"], DEV)
+    cache = fk.KVCache.empty(kd.num_blocks, 16, Hkv, 128, device=DEV)
+    fk.kv_store_e4m3(cache, kd.k, kd.v, kd.slot_mapping, 1.0, 1.0)
+    q = inp["q"].to(DEV)
+    torch.cuda.synchronize()
+    assert fk.device_error() == 0
+    fk.test_drop_first_copy(True)
+    t0 = time.time()
+    fk.paged_attn_fp8_decode(cache, q, kd.block_table, kd.seq_lens, 1.0, 1.0, 1.0)
+    torch.cuda.synchronize()
+    waited = time.time() - t0
+    assert fk.device_error() & fk.DEVERR_WAIT_TIMEOUT
+    assert 1.5 < waited < 30.0, waited     # the 2 s limit, then the teardown
+    out = fk.paged_attn_fp8_decode(cache, q, kd.block_table, kd.seq_lens, 1.0, 1.0, 1.0)
+    torch.cuda.synchronize()
+    assert fk.device_error() == 0
+    rows = [(0, h) for h in range(Hq)]
+    ref = oracle_decode_rows(inp, rows, 1.0, 1.0, 1.0)
+    assert_close(out.float().cpu().numpy()[0], ref, "decode after a timed-out call")

@@ -221,3 +221,30 @@ def test_prefill_per_token_rejects_head_dim_256(fk):
     with pytest.raises(fk.Fp8KVError) as e:
         fk.attn_fp8_varlen_prefill_per_token(cache, q, cu, lens, bt, 4, 1.0, ks, ks)
     assert e.value.status == fk.ERR_UNSUPPORTED
+
+
+def test_decode_dominant_keys_with_tiny_v(fk, oracle_lib):
+    """Keys whose V rows are tiny (scale ~1e-33 / 448) but whose scores
+    dominate: the V scale folded into the exponent must not drop them from
+    the row sum (the output is then close to zero, as the oracle's)."""
+    spec = workloads.DecodeSpec("case", B=2, Hq=8, Hkv=2, D=128, block_size=16, ctx_lo=1, ctx_hi=1)
+    inp = workloads.make_decode(spec, device="cpu", seed=9, lens=[300, 77])
+    kv = inp["kv"]
+    q = inp["q"]
+    starts = kv.tok_start.tolist()
+    for b, j in ((0, 5), (0, 299), (1, 40)):
+        t = starts[b] + j
+        kv.v[t] = (kv.v[t].float() * 1e-33).to(torch.bfloat16)
+        # align the key with every query head of its KV head: a dominant score
+        kv.k[t, 0] = (q[b, :4].float().mean(0) * 6.0).to(torch.bfloat16)
+        kv.k[t, 1] = (q[b, 4:].float().mean(0) * 6.0).to(torch.bfloat16)
+    cache, ks, vs, kd = store(fk, kv, 2, 128, 16)
+    out = fk.paged_attn_fp8_decode_per_token(cache, q.to(DEV), kd.block_table, kd.seq_lens, 1.0,
+                                             ks, vs)
+    torch.cuda.synchronize()
+    assert fk.device_error() == 0
+    got = out.float().cpu().numpy()
+    assert np.isfinite(got).all()
+    rows = [(b, h) for b in range(2) for h in range(8)]
+    ref = oracle_rows_pt(oracle_lib, inp, rows, 1.0)
+    assert_close(np.stack([got[b, h] for b, h in rows]), ref, "tiny V scales")
