@@ -52,12 +52,42 @@ def peaks():
             "source": "fallback"}
 
 
+def fp8_mma_probe(dev, shapes=((256, 2, 1), (128, 2, 2), (128, 1, 1), (64, 2, 2))):
+    """FP8 (e4m3) tcgen05 MMA throughput of this GPU measured by the repo's
+    own probe (libfp8kv_probe.so): one CTA per SM, `issuers` threads issuing
+    M=128, K=32 MMAs of N = n back to back over `accs` accumulators each,
+    timed with CUDA events.  Context for the prefill roofline, whose
+    denominator stays 2 x the measured bf16 rate."""
+    import ctypes
+    path = os.path.join(ROOT, "fp8_e4m3_kv_gb300", "libfp8kv_probe.so")
+    if not os.path.exists(path):
+        return None
+    lib = ctypes.CDLL(path)
+    fn = lib.fp8kv_probe_mma_e4m3
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                   ctypes.POINTER(ctypes.c_float), ctypes.c_void_p]
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    res = {}
+    for n, accs, issuers in shapes:
+        iters = 20000 * 256 // n
+        ms = ctypes.c_float()
+        rc = fn(sms, iters, n, accs, issuers, ctypes.byref(ms),
+                ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+        if rc != 0 or ms.value <= 0:
+            return {"error": "probe status %d" % rc}
+        res["n%d_acc%d_thr%d_tflops" % (n, accs, issuers)] = (
+            2.0 * 128 * n * 32 * iters * issuers * sms / (ms.value * 1e-3) / 1e12)
+    return res
+
+
 # DRAM bytes (read + write) of one decode launch of the 64-sequence workload,
-# from the ncu capture summarised in profiles/ (decode launch list), keyed by a
-# hash of the kernel sources it was taken on: once the kernel changes, the
-# number no longer describes it and is reported as null.
+# from the ncu capture summarised in profiles/ (decode launch list: measured
+# on a 16-sequence cut and scaled by the KV bytes), keyed by a hash of the
+# kernel sources it was taken on: once the kernel changes, the number no
+# longer describes it and is reported as null.
 DECODE_TRAFFIC = {
-    "6fad2258069faf63b0626fb2f151663ed96db0dc73f1b3ea11c03387f71a2735": 1084723840,
+    "f7dcb79a504da0bcd07dda19522e39375b79e242f091f5434767e8a4bd7bd62a": 1083428752,
 }
 DECODE_SOURCES = ("fp8_e4m3_kv_gb300/csrc/attn_decode.cu", "fp8_e4m3_kv_gb300/csrc/common.cuh")
 
@@ -476,7 +506,9 @@ def bench_prefill(fk, dev, steps, warmup, world, only_group=None, cpu_budget=0.0
             per_group.append({"window": w, "ms": gms, "tflops": gf / gms / 1e9})
     pk = peaks()
     fp8_peak = 2.0 * pk["bf16_tflops"]      # nominal fp8 : bf16 dense ratio of 2
+    probe = fp8_mma_probe(dev)
     res = {"workload": spec.name, "ms_per_step": ms, "tflops": flops / ms / 1e9,
+           "fp8_mma_probe": probe,
            "roofline": {"bound": "tensor", "achieved": flops / ms / 1e9, "peak": fp8_peak,
                         "unit": "TFLOP/s", "frac": flops / ms / 1e9 / fp8_peak,
                         "peak_source": "2 x %s bf16 burst" % pk["source"]},
