@@ -43,6 +43,8 @@
  * row s % block_size, of every head.  A sequence's keys are listed by its block-table row:
  * logical block i of sequence b is physical block block_table[b][i].
  * Supported: block_size in {16, 32, 64, 128}, head_dim in {128, 256}.
+ * head_dim 64 is not supported (FP8KV_ERR_UNSUPPORTED): the kernels move
+ * K/V rows as 128-byte swizzled TMA boxes and feed the MMAs 128-byte rows.
  */
 #ifndef FP8KV_H
 #define FP8KV_H
