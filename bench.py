@@ -63,21 +63,23 @@ def fp8_mma_probe(dev, shapes=((256, 2, 1), (128, 2, 2), (128, 1, 1), (64, 2, 2)
     if not os.path.exists(path):
         return None
     lib = ctypes.CDLL(path)
-    fn = lib.fp8kv_probe_mma_e4m3
+    fn = lib.fp8kv_probe_mma_e4m3_mode
     fn.restype = ctypes.c_int
     fn.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
-                   ctypes.POINTER(ctypes.c_float), ctypes.c_void_p]
+                   ctypes.c_int32, ctypes.POINTER(ctypes.c_float), ctypes.c_void_p]
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     res = {}
-    for n, accs, issuers in shapes:
+    for shape in shapes:
+        n, accs, issuers = shape[:3]
+        mode = shape[3] if len(shape) > 3 else 0
         iters = 20000 * 256 // n
         ms = ctypes.c_float()
-        rc = fn(sms, iters, n, accs, issuers, ctypes.byref(ms),
+        rc = fn(sms, iters, n, accs, issuers, mode, ctypes.byref(ms),
                 ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
         if rc != 0 or ms.value <= 0:
             return {"error": "probe status %d" % rc}
-        res["n%d_acc%d_thr%d_tflops" % (n, accs, issuers)] = (
-            2.0 * 128 * n * 32 * iters * issuers * sms / (ms.value * 1e-3) / 1e12)
+        key = "n%d_acc%d_thr%d" % (n, accs, issuers) + ("_mode%d" % mode if mode else "")
+        res[key + "_tflops"] = 2.0 * 128 * n * 32 * iters * issuers * sms / (ms.value * 1e-3) / 1e12
     return res
 
 

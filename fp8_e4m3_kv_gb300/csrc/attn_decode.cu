@@ -11,8 +11,11 @@
 //                   column) into a ring of stages;
 //   MMA warp        one thread issues the tcgen05 FP8 MMAs:
 //                     S^T[key][head] = K_tile . Q8^T              (M=128, N=16)
-//                     O^T[d][head]  = V_tile^T . (P_hi + P_lo)^T   (M=128, N=16)
-//                   into TMEM (S^T double-, O^T triple-buffered);
+//                     O^T[d][n]     = V_tile^T . P^T        (M=128, N=2*GMAX)
+//                   into TMEM (S^T double-, O^T triple-buffered), where the
+//                   rows n of P hold both e4m3 terms of every head (P_hi
+//                   and P_lo of a warpgroup's heads side by side), so the
+//                   PV takes as many MMAs as one term of P would;
 //   consumer        thread t owns key row t of S^T and value row d = t of
 //   warpgroups      O^T; warpgroup hs takes its share of the query heads:
 //                   folded descale, bias, mask, block-wide max per head
@@ -23,7 +26,8 @@
 // halves each thread's serial work.  P is exp2(z - m + 8) (at most 256) split
 // into two e4m3 terms, P_hi = e4m3(P) and P_lo = e4m3(P - P_hi), so the PV
 // product runs on the FP8 tensor cores while the weights keep ~8 significant
-// bits.  The partial (o, m, l) of each split goes to the workspace; a second
+// bits (the consumers add the two terms' columns of O^T).  The partial
+// (o, m, l) of each split goes to the workspace; a second
 // kernel merges the splits with the log-sum-exp rule and writes
 // v_scale * o / l in bf16.
 #include <math.h>
@@ -78,22 +82,28 @@ struct DecCfg {
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kQBytes = kNPad * D;         // Q8: 16 rows x D bytes
     static constexpr int kPBytes = kNPad * kKeys;     // one P term: 16 rows x kKeys keys
+    // P of one tile: per 128-key column block, up to 32 rows of 128 bytes
+    // (both terms of up to 16 heads), 128-byte swizzled
+    static constexpr int kPBlock = 2 * kNPad * 128;
     // P and O^T buffers: a tile's O^T is read back two tiles later, so the
     // PV latency stays off the softmax chain
     static constexpr int kOBuf = 3;
     static constexpr int kOffQ = kStages * kStageBytes;
-    static constexpr int kOffP = kOffQ + kQBytes;     // [kOBuf][hi, lo]
+    static constexpr int kOffP = kOffQ + kQBytes;     // [kOBuf][kKB][P rows]
     static constexpr int kOffMisc = kOffP + kOBuf * 2 * kPBytes;
     // misc: barriers, tmem slot, abort flag, then per warpgroup the tile-max
     // exchange [2][4][16] and row-sum exchange [4][16] floats
     static constexpr int kOffRed = 512;
     static constexpr int kMiscBytes = kOffRed + kHS * 768;
     static constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;   // + alignment slack
-    // TMEM: S^T 2 buffers x kKB x 16 columns, then O^T kOBuf buffers x kCB x 16
+    // TMEM: S^T 2 buffers x kKB x 16 columns, then O^T kOBuf buffers x kCB x
+    // np columns (np = rows of P: 16 for up to 8 heads, 32 for 16)
     static constexpr uint32_t kColO = 2 * kKB * kNPad;
-    static constexpr uint32_t kCols = kColO + kOBuf * kCB * kNPad + kNPad;   // + over-read room
-    static constexpr uint32_t kTmemCols = kCols <= 64 ? 64 : kCols <= 128 ? 128 : 256;
-    static_assert(kCols <= 256, "TMEM columns");
+    __host__ __device__ static constexpr uint32_t cols(int np) { return kColO + kOBuf * kCB * np + kNPad; }   // + over-read room
+    __host__ __device__ static constexpr uint32_t tmem_cols(int np) {
+        return cols(np) <= 64 ? 64 : cols(np) <= 128 ? 128 : 256;
+    }
+    static_assert(cols(2 * kNPad) <= 256, "TMEM columns");
     static_assert(kStages >= 2 && kStages <= 8, "stages");
     static_assert(kHS >= 1 && kHS <= 4, "head split");
 };
@@ -143,6 +153,12 @@ struct DecodeParams {
     uint16_t *out;
     float out_scale;    // v_scale (1 for per-token scales)
     int32_t direct_out;
+    // work items: num_kv_heads x num_seqs x num_slots, taken in order from
+    // the counter *sched (zero at launch); sched == nullptr: one CTA per
+    // item, CTA c takes item c
+    uint32_t *sched;
+    int32_t num_items;
+    int32_t num_seqs;
 };
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -226,11 +242,48 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// One work item: a split of one (sequence, KV head); ntiles < 0 ends the
+// list.
+struct DecItem {
+    int32_t b, kvh, split, ntiles;
+};
+constexpr int kItemSlots = 4;   // item records in flight between the roles
+
+// The key range of split `split` of sequence b: keys [lo, len) (the window's
+// keys for a sliding-window layer) in tiles of kKeys, this split's tiles
+// [t0, t0 + ntiles) (ntiles <= 0: none).
+struct ItemGeom {
+    int64_t len, lo, t0, t_end;
+    int ntiles;
+};
+
+template <int kKeys>
+__device__ __forceinline__ ItemGeom item_geom(const DecodeParams &p, int b, int split) {
+    ItemGeom g;
+    g.len = p.seq_lens[b];
+    g.lo = (p.window > 0 && g.len > p.window) ? g.len - p.window : 0;
+    g.t0 = g.lo / kKeys + static_cast<int64_t>(split) * p.split_tiles;
+    g.t_end = (g.len + kKeys - 1) / kKeys;
+    g.ntiles = static_cast<int>(g.t_end - g.t0 < p.split_tiles ? g.t_end - g.t0 : p.split_tiles);
+    return g;
+}
+
 // kPT: per-token scales.  Key j's score is multiplied by its K scale, and
 // its V scale is folded into the exponent: z_j + log2(v_scale_j) takes part
 // in the block-wide max like any score, so P_j = 2^(z_j + log2 v_scale_j -
 // m + 8) <= 2^8 is p_j * v_scale_j (up to the common factor) and the row
 // sum adds P_j / v_scale_j.
+//
+// The launch is persistent: up to kCtasPerSm CTAs per SM, each taking work
+// items from a counter in global memory until none is left.  Items are
+// numbered KV heads fastest, then sequences, then splits in descending
+// order (the first splits, full-length ones, come last and fill the tail).
+// The producer warp takes the items, marks the empty ones itself and hands
+// the others to the MMA thread and the consumers through a ring of item
+// records in shared memory; it loads each item's key tiles right after the
+// previous item's, so the pipeline does not drain between items, and the
+// consumers quantize the next item's Q while the last P of an item is
+// multiplied.
 template <int D, int GMAX, bool kPT>
 __global__ void __launch_bounds__(DecCfg<D>::kThreads, DecCfg<D>::kCtasPerSm)
 decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
@@ -239,38 +292,16 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
     constexpr int HS = C::kHS;
     constexpr int GH = GMAX / HS;                      // heads per consumer warpgroup
     static_assert(GH * HS == GMAX && GH % 2 == 0, "head split: an even number of heads per warpgroup");
+    // rows of P (= the PV's N): warpgroup hs writes P_hi of its head g in row
+    // hs * 2GH + g and P_lo in row hs * 2GH + GH + g
+    constexpr int NP = 2 * GMAX < 16 ? 16 : 2 * GMAX;
+    static_assert(NP % 16 == 0 && NP <= 2 * kNPad && 2 * GH <= 16, "P rows");
+    constexpr uint32_t kTmemCols = C::tmem_cols(NP);
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // KV heads fastest (the CTAs of one split stream neighbouring cache
-    // blocks together), then sequences; splits slowest and in descending
-    // order, so the last CTAs to run are the first splits, which are the
-    // short ones of short sequences
-    const int kvh = blockIdx.x, b = blockIdx.y;
-    const int split = static_cast<int>(gridDim.z) - 1 - static_cast<int>(blockIdx.z);
-    const int h0 = kvh * p.G;
-    const int64_t len = p.seq_lens[b];
-    const int64_t lo = (p.window > 0 && len > p.window) ? len - p.window : 0;
-    const int64_t t0 = lo / C::kKeys + static_cast<int64_t>(split) * p.split_tiles;
-    const int64_t t_end = (len + C::kKeys - 1) / C::kKeys;
-    const int ntiles = static_cast<int>(t_end - t0 < p.split_tiles ? t_end - t0 : p.split_tiles);
-
-    if (ntiles <= 0) {   // nothing to attend in this split: mark it empty
-        if (p.direct_out) {   // the only split: the output is zero
-            for (int e = threadIdx.x; e < p.G * D; e += blockDim.x)
-                p.out[(static_cast<int64_t>(b) * p.Hq + h0 + e / D) * D + e % D] = 0;
-            return;
-        }
-        if (threadIdx.x < p.G) {
-            float *ml = p.part_ml + ((static_cast<int64_t>(b) * p.Hq + h0 + threadIdx.x) *
-                                         p.num_slots + split) * 2;
-            ml[0] = -INFINITY;
-            ml[1] = 0.0f;
-        }
-        return;
-    }
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffMisc);
     uint64_t *full = bars;          // [kStages] TMA landed
@@ -282,9 +313,15 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
     uint64_t *o_free = bars + 26;   // [3] O^T read by all consumer warps
     uint64_t *mma_done = bars + 29; // teardown: all MMAs complete
     // per warpgroup hs: red_bar[2] at bars + 30 + 3*hs, l_bar at + 2
+    uint64_t *q_full = bars + 42;      // Q8 of the next item written by every consumer warp
+    uint64_t *item_full = bars + 43;   // [kItemSlots] item record written
+    uint64_t *item_free = bars + 47;   // [kItemSlots] record read by the MMA thread and every consumer warp
+    DecItem *items = reinterpret_cast<DecItem *>(smem + C::kOffMisc + 416);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc + 480);
     CtaFail *fail = reinterpret_cast<CtaFail *>(smem + C::kOffMisc + 484);
-    static_assert(30 + 3 * 4 <= 60, "barrier area");
+    static_assert(30 + 3 * 4 <= 42 && (47 + kItemSlots) * 8 <= 416 &&
+                      416 + kItemSlots * sizeof(DecItem) <= 480,
+                  "barrier area");
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
@@ -306,45 +343,15 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
             mbar_init(bars + 31 + 3 * hs, 4);
             mbar_init(bars + 32 + 3 * hs, 4);
         }
+        mbar_init(q_full, 4 * HS);
+        for (int i = 0; i < kItemSlots; ++i) {
+            mbar_init(&item_full[i], 1);
+            mbar_init(&item_free[i], 1 + 4 * HS);
+        }
         fail->abort = 0;
         fence_mbar_init();
     }
-    if (warp == C::kMmaWarp) tmem_alloc(tmem_slot, C::kTmemCols);
-    if (p.k_new != nullptr && len > 0 && t0 + ntiles == t_end && threadIdx.x < D / 8) {
-        // Fused store: this CTA reads the sequence's last tile, so it writes
-        // the step's new token (position len - 1) for its KV head first; the
-        // proxy fence orders these generic writes before the tile's TMA copy.
-        const int64_t lb = (len - 1) / p.block_size;
-        const int32_t id = lb < p.max_blocks
-                               ? __ldg(p.block_table + static_cast<int64_t>(b) * p.max_blocks + lb)
-                               : -1;
-        if (id >= 0 && id < p.num_blocks) {
-            const int d = threadIdx.x * 8;
-            const int64_t src = (static_cast<int64_t>(b) * p.num_kv_heads + kvh) * D + d;
-            const int64_t dst = ((static_cast<int64_t>(id) * p.num_kv_heads + kvh) * p.block_size +
-                                 (len - 1) % p.block_size) * D + d;
-            const uint4 kw = *reinterpret_cast<const uint4 *>(p.k_new + src);
-            const uint4 vw = *reinterpret_cast<const uint4 *>(p.v_new + src);
-            *reinterpret_cast<uint2 *>(p.cache_k + dst) = store_quantize8(kw, p.k_scale);
-            *reinterpret_cast<uint2 *>(p.cache_v + dst) = store_quantize8(vw, p.v_scale);
-            // non-negative floats order like their bit patterns
-            if (p.amax_k) atomicMax(reinterpret_cast<unsigned int *>(p.amax_k), __float_as_uint(absmax8(kw)));
-            if (p.amax_v) atomicMax(reinterpret_cast<unsigned int *>(p.amax_v), __float_as_uint(absmax8(vw)));
-            asm volatile("fence.proxy.async.global;" ::: "memory");
-        } else if (threadIdx.x == 0) {
-            atomicOr(p.err, FP8KV_DEVERR_BAD_BLOCK);
-        }
-    }
-    if (warp < 4 * HS) {
-        // Q8 = e4m3(q / q_scale) for the group's heads, rows >= G zero;
-        // 128-byte swizzled, K-major (row = head, D bytes per row).
-        uint8_t *q8 = smem + C::kOffQ;
-        const uint16_t *qb = p.q + (static_cast<int64_t>(b) * p.Hq + h0) * D;
-        if (p.q_scale.pow2)
-            load_q8<true, D, C::kConsumers>(q8, qb, p.G, p.q_scale);
-        else
-            load_q8<false, D, C::kConsumers>(q8, qb, p.G, p.q_scale);
-    }
+    if (warp == C::kMmaWarp) tmem_alloc(tmem_slot, kTmemCols);
     if (warp == C::kProducerWarp) {
         // zero the P buffers: rows past the group are never written
         uint4 *pz = reinterpret_cast<uint4 *>(smem + C::kOffP);
@@ -367,40 +374,120 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
         int last_issued[C::kStages];
 #pragma unroll
         for (int s = 0; s < C::kStages; ++s) last_issued[s] = -1;
-        for (int i = 0; i < ntiles; ++i) {
-            const int s = i % C::kStages;
-            int32_t phys = static_cast<int32_t>(p.num_blocks);   // out of range: zero fill
-            if (lane < nb) {
-                const int64_t lb = (t0 + i) * nb + lane;
-                if (lb * p.block_size < len) {
-                    // a length past the block table is flagged like a bad id
-                    const int32_t id =
-                        lb < p.max_blocks
-                            ? __ldg(p.block_table + static_cast<int64_t>(b) * p.max_blocks + lb)
-                            : -1;
-                    if (id >= 0 && id < p.num_blocks)
-                        phys = id;
-                    else
-                        atomicOr(p.err, FP8KV_DEVERR_BAD_BLOCK);
+        int T = 0;   // key tiles of this CTA so far
+        int J = 0;   // item records written
+        bool ok = true;
+        bool fetched = false;
+        while (ok) {
+            int idx = 0;
+            if (lane == 0)
+                idx = p.sched ? static_cast<int>(atomicAdd(p.sched, 1u))
+                              : (fetched ? p.num_items : static_cast<int>(blockIdx.x));
+            idx = __shfl_sync(0xffffffffu, idx, 0);
+            fetched = true;
+            DecItem it{0, 0, 0, -1};
+            ItemGeom gm{};
+            if (idx < p.num_items) {
+                const int kvh = idx % p.num_kv_heads;
+                const int rest = idx / p.num_kv_heads;
+                const int b = rest % p.num_seqs;
+                const int split = p.num_slots - 1 - rest / p.num_seqs;
+                gm = item_geom<C::kKeys>(p, b, split);
+                if (gm.ntiles <= 0) {   // nothing to attend in this split: mark it empty
+                    const int h0 = kvh * p.G;
+                    if (p.direct_out) {   // the only split: the output is zero
+                        for (int e = lane; e < p.G * D; e += 32)
+                            p.out[(static_cast<int64_t>(b) * p.Hq + h0 + e / D) * D + e % D] = 0;
+                    } else if (lane < p.G) {
+                        float *ml = p.part_ml + ((static_cast<int64_t>(b) * p.Hq + h0 + lane) *
+                                                     p.num_slots + split) * 2;
+                        ml[0] = -INFINITY;
+                        ml[1] = 0.0f;
+                    }
+                    continue;
                 }
+                it = DecItem{b, kvh, split, gm.ntiles};
             }
-            int ok = 1;
-            if (lane == 0) ok = mbar_wait(&empty[s], ((i / C::kStages) & 1) ^ 1, fail, p.err);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-            if (i == 0 && p.drop_first_copy) continue;
-            if (lane == 0) mbar_arrive_expect_tx(&full[s], C::kStageBytes);
-            __syncwarp();
-            if (lane < nb) {
-                uint8_t *kdst = smem + s * C::kStageBytes + lane * p.block_size * 128;
-                uint8_t *vdst = kdst + C::kTileBytes;
+            const int slot = J % kItemSlots;
+            int w = 1;
+            if (lane == 0) w = mbar_wait(&item_free[slot], ((J / kItemSlots) & 1) ^ 1, fail, p.err);
+            if (!__shfl_sync(0xffffffffu, w, 0)) break;
+            if (lane == 0) {
+                items[slot] = it;
+                mbar_arrive(&item_full[slot]);
+            }
+            ++J;
+            if (it.ntiles < 0) break;
+            if (p.k_new != nullptr && gm.len > 0 && gm.t0 + it.ntiles == gm.t_end) {
+                // Fused store: this item holds the sequence's last tile, so the
+                // warp writes the step's new token (position len - 1) for its
+                // KV head before loading the tile; the proxy fence orders these
+                // generic writes before the warp's TMA copies.
+                const int64_t lb = (gm.len - 1) / p.block_size;
+                const int32_t id =
+                    lb < p.max_blocks
+                        ? __ldg(p.block_table + static_cast<int64_t>(it.b) * p.max_blocks + lb)
+                        : -1;
+                if (id >= 0 && id < p.num_blocks) {
+                    if (lane < D / 8) {
+                        const int d = lane * 8;
+                        const int64_t src = (static_cast<int64_t>(it.b) * p.num_kv_heads + it.kvh) * D + d;
+                        const int64_t dst = ((static_cast<int64_t>(id) * p.num_kv_heads + it.kvh) *
+                                                 p.block_size + (gm.len - 1) % p.block_size) * D + d;
+                        const uint4 kw = *reinterpret_cast<const uint4 *>(p.k_new + src);
+                        const uint4 vw = *reinterpret_cast<const uint4 *>(p.v_new + src);
+                        *reinterpret_cast<uint2 *>(p.cache_k + dst) = store_quantize8(kw, p.k_scale);
+                        *reinterpret_cast<uint2 *>(p.cache_v + dst) = store_quantize8(vw, p.v_scale);
+                        // non-negative floats order like their bit patterns
+                        if (p.amax_k)
+                            atomicMax(reinterpret_cast<unsigned int *>(p.amax_k), __float_as_uint(absmax8(kw)));
+                        if (p.amax_v)
+                            atomicMax(reinterpret_cast<unsigned int *>(p.amax_v), __float_as_uint(absmax8(vw)));
+                    }
+                } else if (lane == 0) {
+                    atomicOr(p.err, FP8KV_DEVERR_BAD_BLOCK);
+                }
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                __syncwarp();
+            }
+            for (int i = 0; i < it.ntiles; ++i, ++T) {
+                const int s = T % C::kStages;
+                int32_t phys = static_cast<int32_t>(p.num_blocks);   // out of range: zero fill
+                if (lane < nb) {
+                    const int64_t lb = (gm.t0 + i) * nb + lane;
+                    if (lb * p.block_size < gm.len) {
+                        // a length past the block table is flagged like a bad id
+                        const int32_t id =
+                            lb < p.max_blocks
+                                ? __ldg(p.block_table + static_cast<int64_t>(it.b) * p.max_blocks + lb)
+                                : -1;
+                        if (id >= 0 && id < p.num_blocks)
+                            phys = id;
+                        else
+                            atomicOr(p.err, FP8KV_DEVERR_BAD_BLOCK);
+                    }
+                }
+                int okw = 1;
+                if (lane == 0) okw = mbar_wait(&empty[s], ((T / C::kStages) & 1) ^ 1, fail, p.err);
+                okw = __shfl_sync(0xffffffffu, okw, 0);
+                if (!okw) {
+                    ok = false;
+                    break;
+                }
+                if (T == 0 && p.drop_first_copy) continue;
+                if (lane == 0) mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+                __syncwarp();
+                if (lane < nb) {
+                    uint8_t *kdst = smem + s * C::kStageBytes + lane * p.block_size * 128;
+                    uint8_t *vdst = kdst + C::kTileBytes;
 #pragma unroll
-                for (int cb = 0; cb < C::kCB; ++cb) {
-                    tma_load_4d(kdst + cb * C::kCBBytes, &kmap, &full[s], cb * 128, 0, kvh, phys, pol);
-                    tma_load_4d(vdst + cb * C::kCBBytes, &vmap, &full[s], cb * 128, 0, kvh, phys, pol);
+                    for (int cb = 0; cb < C::kCB; ++cb) {
+                        tma_load_4d(kdst + cb * C::kCBBytes, &kmap, &full[s], cb * 128, 0, it.kvh, phys, pol);
+                        tma_load_4d(vdst + cb * C::kCBBytes, &vmap, &full[s], cb * 128, 0, it.kvh, phys, pol);
+                    }
                 }
+                last_issued[s] = T;
             }
-            last_issued[s] = i;
         }
         if (lane == 0 && fail->abort) {   // let copies already issued land
             for (int s = 0; s < C::kStages; ++s)
@@ -408,65 +495,80 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
         }
     } else if (warp == C::kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        // Step i issues QK of tile i, then PV of tile i - 1 (whose P the
-        // consumers produced while QK of tile i was in flight).
+        // Per item, step i issues QK of tile i, then PV of tile i - 1 (whose P
+        // the consumers produced while QK of tile i was in flight).
         if (lane == 0) {
             const uint32_t idesc_qk = idesc_e4m3_f32(128, kNPad, false, false);
-            const uint32_t idesc_pv = idesc_e4m3_f32(128, kNPad, true, false);
+            const uint32_t idesc_pv = idesc_e4m3_f32(128, NP, true, false);
             const uint32_t q_addr = smem_u32(smem + C::kOffQ);
-            for (int i = 0; i <= ntiles; ++i) {
-                if (i < ntiles) {
-                    const int s = i % C::kStages, sb = i & 1;
-                    if (!mbar_wait(&full[s], (i / C::kStages) & 1, fail, p.err)) break;
-                    if (!mbar_wait(&s_free[sb], ((i >> 1) & 1) ^ 1, fail, p.err)) break;
-                    tc_fence_after_sync();
-                    const uint32_t k_addr = smem_u32(smem + s * C::kStageBytes);
-#pragma unroll
-                    for (int kb = 0; kb < C::kKB; ++kb) {
-                        const uint32_t dcol = tmem + (sb * C::kKB + kb) * kNPad;
-#pragma unroll
-                        for (int kk = 0; kk < D / 32; ++kk) {
-                            const uint32_t cb = kk / 4, ko = (kk % 4) * 32;
-                            const uint64_t a = sdesc_sw128(
-                                k_addr + cb * C::kCBBytes + kb * (128 * 128) + ko, 16, 1024);
-                            const uint64_t bd =
-                                sdesc_sw128(q_addr + cb * (kNPad * 128) + ko, 16, 1024);
-                            mma_e4m3(dcol, a, bd, idesc_qk, kk > 0);
+            int T = 0, J = 0, A = 0;
+            bool ok = true;
+            while (ok) {
+                const int slot = J % kItemSlots;
+                if (!mbar_wait(&item_full[slot], (J / kItemSlots) & 1, fail, p.err)) break;
+                const int ntiles = reinterpret_cast<volatile DecItem *>(items)[slot].ntiles;
+                mbar_arrive(&item_free[slot]);
+                ++J;
+                if (ntiles < 0) break;
+                if (!mbar_wait(q_full, A & 1, fail, p.err)) break;
+                ++A;
+                for (int i = 0; i <= ntiles; ++i) {
+                    if (i < ntiles) {
+                        const int TT = T + i;
+                        const int s = TT % C::kStages, sb = TT & 1;
+                        if (!mbar_wait(&full[s], (TT / C::kStages) & 1, fail, p.err) ||
+                            !mbar_wait(&s_free[sb], ((TT >> 1) & 1) ^ 1, fail, p.err)) {
+                            ok = false;
+                            break;
                         }
+                        tc_fence_after_sync();
+                        const uint32_t k_addr = smem_u32(smem + s * C::kStageBytes);
+#pragma unroll
+                        for (int kb = 0; kb < C::kKB; ++kb) {
+                            const uint32_t dcol = tmem + (sb * C::kKB + kb) * kNPad;
+#pragma unroll
+                            for (int kk = 0; kk < D / 32; ++kk) {
+                                const uint32_t cb = kk / 4, ko = (kk % 4) * 32;
+                                const uint64_t a = sdesc_sw128(
+                                    k_addr + cb * C::kCBBytes + kb * (128 * 128) + ko, 16, 1024);
+                                const uint64_t bd =
+                                    sdesc_sw128(q_addr + cb * (kNPad * 128) + ko, 16, 1024);
+                                mma_e4m3(dcol, a, bd, idesc_qk, kk > 0);
+                            }
+                        }
+                        tc_commit(&s_full[sb]);
                     }
-                    tc_commit(&s_full[sb]);
-                }
-                if (i >= 1) {
-                    const int j = i - 1, s = j % C::kStages;
-                    const int pb = j % C::kOBuf, ph = (j / C::kOBuf) & 1;
-                    if (!mbar_wait(&p_full[pb], ph, fail, p.err)) break;
-                    if (!mbar_wait(&o_free[pb], ph ^ 1, fail, p.err)) break;
-                    tc_fence_after_sync();
-                    const uint32_t v_addr = smem_u32(smem + s * C::kStageBytes + C::kTileBytes);
-                    const uint32_t p_addr = smem_u32(smem + C::kOffP + pb * 2 * C::kPBytes);
+                    if (i >= 1) {
+                        const int j = T + i - 1, s = j % C::kStages;
+                        const int pb = j % C::kOBuf, ph = (j / C::kOBuf) & 1;
+                        if (!mbar_wait(&p_full[pb], ph, fail, p.err) ||
+                            !mbar_wait(&o_free[pb], ph ^ 1, fail, p.err)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after_sync();
+                        const uint32_t v_addr = smem_u32(smem + s * C::kStageBytes + C::kTileBytes);
+                        const uint32_t p_addr = smem_u32(smem + C::kOffP + pb * 2 * C::kPBytes);
 #pragma unroll
-                    for (int mh = 0; mh < C::kCB; ++mh) {
-                        const uint32_t dcol = tmem + C::kColO + (pb * C::kCB + mh) * kNPad;
-#pragma unroll
-                        for (int part = 0; part < 2; ++part) {
+                        for (int mh = 0; mh < C::kCB; ++mh) {
+                            const uint32_t dcol = tmem + C::kColO + (pb * C::kCB + mh) * NP;
 #pragma unroll
                             for (int kk = 0; kk < C::kKeys / 32; ++kk) {
                                 // V tile, MN-major: rows are keys (128 bytes of d
                                 // each), 8-row groups 1024 bytes apart; 32 keys per
-                                // MMA.  P: 16 rows of kKeys bytes in 128-byte
-                                // column blocks of 2 KB.
+                                // MMA.  P: NP rows of 128 keys per column block.
                                 const uint64_t a = sdesc_sw128(
                                     v_addr + mh * C::kCBBytes + kk * 32 * 128, C::kCBBytes, 1024);
                                 const uint64_t bd = sdesc_sw128(
-                                    p_addr + part * C::kPBytes + (kk / 4) * (kNPad * 128) + (kk % 4) * 32,
-                                    16, 1024);
-                                mma_e4m3(dcol, a, bd, idesc_pv, (part | kk) != 0);
+                                    p_addr + (kk / 4) * C::kPBlock + (kk % 4) * 32, 16, 1024);
+                                mma_e4m3(dcol, a, bd, idesc_pv, kk != 0);
                             }
                         }
+                        tc_commit(&o_full[pb]);
+                        tc_commit(&empty[s]);
                     }
-                    tc_commit(&o_full[pb]);
-                    tc_commit(&empty[s]);
                 }
+                T += ntiles;
             }
             tc_commit(mma_done);
             mbar_drain(mma_done, 0, p.err);
@@ -481,250 +583,330 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
         float *red = reinterpret_cast<float *>(smem + C::kOffMisc + C::kOffRed + hs * 768);  // [2][4][16]
         float *lred = red + 128;                                                          // [4][16]
         const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-        const uint16_t *bias = p.rel ? p.rel + static_cast<int64_t>(b) * p.bias_tok_stride +
-                                           static_cast<int64_t>(h0 + gbase) * p.rel_extent
-                                     : nullptr;
+        int T = 0, J = 0, A = 0;
         bool ok = true;
 
-        // rescale factors of the two previous tiles (a tile's O^T is taken two
-        // tiles later): alpha_1 of tile j - 1, alpha_2 of tile j - 2
-        float m_run[GH], l_part[GH], alpha_1[GH], alpha_2[GH], o_acc[C::kCB][GH];
-#pragma unroll
-        for (int g = 0; g < GH; ++g) {
-            m_run[g] = -INFINITY;
-            l_part[g] = 0.0f;
-            alpha_1[g] = alpha_2[g] = 1.0f;
-#pragma unroll
-            for (int mh = 0; mh < C::kCB; ++mh) o_acc[mh][g] = 0.0f;
-        }
-        // Accumulate this warpgroup's heads of O^T of tile j (rescaled) into
-        // the registers.
-        auto take_o = [&](int j, const float *alpha) -> bool {
-            const int ob = j % C::kOBuf;
-            if (!warp_wait(&o_full[ob], (j / C::kOBuf) & 1, fail, p.err)) return false;
-            tc_fence_after_sync();
-#pragma unroll
-            for (int mh = 0; mh < C::kCB; ++mh) {
-                float o[16];
-                tmem_ld_x16(tmem + lane_base + C::kColO + (ob * C::kCB + mh) * kNPad + gbase, o);
-#pragma unroll
-                for (int g = 0; g < GH; ++g)
-                    o_acc[mh][g] = fmaf(o_acc[mh][g], alpha[g], o[g]);
-            }
-            tc_fence_before_sync();
+        // the next item record (every lane reads it; lane 0 releases it)
+        auto pop_item = [&](DecItem &it) -> bool {
+            const int slot = J % kItemSlots;
+            if (!warp_wait(&item_full[slot], (J / kItemSlots) & 1, fail, p.err)) return false;
+            const volatile DecItem *r = reinterpret_cast<volatile DecItem *>(items) + slot;
+            it.b = r->b;
+            it.kvh = r->kvh;
+            it.split = r->split;
+            it.ntiles = r->ntiles;
             __syncwarp();
-            if (lane == 0) mbar_arrive(&o_free[ob]);
+            if (lane == 0) mbar_arrive(&item_free[slot]);
+            ++J;
             return true;
         };
-
-        // kPT: the raw scales of this thread's keys of tile i (ksc, vsc),
-        // loaded a tile ahead so that their latency stays off the chain
-        float ksc[C::kKB], vsc[C::kKB];
-        auto load_scales = [&](int i) {
+        // Q rows of an item's group (8 bf16 per thread and step; rows >= G
+        // zero), then Q8 = e4m3(q / q_scale), 128-byte swizzled, K-major (row =
+        // head, D bytes per row), handed to the MMA thread
+        constexpr int kQV = kNPad * D / 8 / C::kConsumers;
+        static_assert(kQV * 8 * C::kConsumers == kNPad * D, "Q split");
+        uint4 qreg[kQV];
+        auto load_q = [&](const DecItem &it) {
+            const uint16_t *qb = p.q + (static_cast<int64_t>(it.b) * p.Hq + it.kvh * p.G) * D;
 #pragma unroll
-            for (int kb = 0; kb < C::kKB; ++kb) {
-                const int64_t key = (t0 + i) * C::kKeys + kb * 128 + t;
-                const int64_t lb = key / p.block_size;
-                ksc[kb] = 1.0f;
-                vsc[kb] = 0.0f;   // marks a key that is not visible
-                if (i < ntiles && key < len && key >= lo && lb < p.max_blocks) {
-                    const int32_t id =
-                        __ldg(p.block_table + static_cast<int64_t>(b) * p.max_blocks + lb);
-                    if (id >= 0 && id < p.num_blocks) {
-                        const int64_t si = (static_cast<int64_t>(id) * p.num_kv_heads + kvh) *
-                                               p.block_size + key % p.block_size;
-                        ksc[kb] = __ldg(p.k_tok_scale + si);
-                        vsc[kb] = __ldg(p.v_tok_scale + si);
-                    }
-                }
+            for (int v = 0; v < kQV; ++v) {
+                const int e = (threadIdx.x + v * C::kConsumers) * 8;
+                const int g = e / D, d = e % D;
+                qreg[v] = g < p.G ? *reinterpret_cast<const uint4 *>(qb + static_cast<int64_t>(g) * D + d)
+                                  : make_uint4(0u, 0u, 0u, 0u);
             }
         };
-        if constexpr (kPT) load_scales(0);
-        for (int i = 0; i < ntiles; ++i) {
-            // per-token factors of this thread's keys: K scale, log2 and
-            // reciprocal of the V scale (1, 0, 0 where not visible; the
-            // score of such a key is -inf anyway)
-            float tsk[C::kKB], tlv[C::kKB], tiv[C::kKB];
-            if constexpr (kPT) {
+        auto store_q8 = [&]() {
+            uint8_t *q8 = smem + C::kOffQ;
 #pragma unroll
-                for (int kb = 0; kb < C::kKB; ++kb) {
-                    const float sv = vsc[kb];
-                    const float lv = log2f(sv);
-                    tsk[kb] = ksc[kb];
-                    // below 2^-60 the exponent takes 2^-60 (and the sum its
-                    // reciprocal): P stays far from fp32 underflow, at an
-                    // error below p * 2^-60 * 448
-                    tlv[kb] = sv > 0.0f ? fmaxf(lv, kMinLog2VScale) : 0.0f;
-                    tiv[kb] = sv > 0.0f ? (lv > kMinLog2VScale ? __frcp_rn(sv) : 0x1p60f) : 0.0f;
+            for (int v = 0; v < kQV; ++v) {
+                const int e = (threadIdx.x + v * C::kConsumers) * 8;
+                const int g = e / D, d = e % D;
+                const uint4 w = qreg[v];
+                uint2 packed;
+                if (p.q_scale.pow2) {
+                    packed.x = quantize_q_bf16x2<true>(w.x, p.q_scale) | (quantize_q_bf16x2<true>(w.y, p.q_scale) << 16);
+                    packed.y = quantize_q_bf16x2<true>(w.z, p.q_scale) | (quantize_q_bf16x2<true>(w.w, p.q_scale) << 16);
+                } else {
+                    packed.x = quantize_q_bf16x2<false>(w.x, p.q_scale) | (quantize_q_bf16x2<false>(w.y, p.q_scale) << 16);
+                    packed.y = quantize_q_bf16x2<false>(w.z, p.q_scale) | (quantize_q_bf16x2<false>(w.w, p.q_scale) << 16);
                 }
-                load_scales(i + 1);   // the next tile's, in flight during this one
-            }
-            if (!warp_wait(&s_full[i & 1], (i >> 1) & 1, fail, p.err)) { ok = false; break; }
-            tc_fence_after_sync();
-            float sc[C::kKB][16];
-#pragma unroll
-            for (int kb = 0; kb < C::kKB; ++kb)
-                tmem_ld_x16(tmem + lane_base + ((i & 1) * C::kKB + kb) * kNPad + gbase, sc[kb]);
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s_free[i & 1]);
-
-            // this thread's keys: t, t + 128, ... of the tile
-            float z[C::kKB][GH];
-            bool any_past_end = false;
-#pragma unroll
-            for (int kb = 0; kb < C::kKB; ++kb) {
-                const int64_t key = (t0 + i) * C::kKeys + kb * 128 + t;
-                const bool valid = key < len && key >= lo;
-                any_past_end |= key >= len;
-                const int64_t dist = len - 1 - key;
-                const bool has_bias = bias && valid && dist < p.rel_extent;
-#pragma unroll
-                for (int g = 0; g < GH; ++g) {
-                    float zz = -INFINITY;
-                    if (valid && gbase + g < p.G) {
-                        zz = kPT ? fmaf(sc[kb][g], p.score_log2 * tsk[kb], tlv[kb])
-                                 : sc[kb][g] * p.score_log2;
-                        if (has_bias)
-                            zz = fmaf(bf16_bits_to_float(__ldg(bias + g * p.rel_extent + dist)),
-                                      kLog2e, zz);
-                    }
-                    z[kb][g] = zz;
-                }
-            }
-            // block-wide max per head: warp shuffles, then the 4 warps of the
-            // warpgroup via shared memory and a (bounded) mbarrier exchange
-            float *rb = red + (i & 1) * 64;
-#pragma unroll
-            for (int g = 0; g < GH; ++g) {
-                float mx = z[0][g];
-#pragma unroll
-                for (int kb = 1; kb < C::kKB; ++kb) mx = fmaxf(mx, z[kb][g]);
-                mx = warp_max(mx);
-                if (lane == 0) rb[wq * 16 + g] = mx;
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&red_bar[i & 1]);
-            if (!warp_wait(&red_bar[i & 1], (i >> 1) & 1, fail, p.err)) { ok = false; break; }
-            float alpha[GH], neg_m8[GH];
-            uint8_t *phi = smem + C::kOffP + (i % C::kOBuf) * 2 * C::kPBytes;
-            uint8_t *plo = phi + C::kPBytes;
-#pragma unroll
-            for (int g = 0; g < GH; ++g) {
-                const float tile_max =
-                    fmaxf(fmaxf(rb[g], rb[16 + g]), fmaxf(rb[32 + g], rb[48 + g]));
-                const float m_new = fmaxf(m_run[g], tile_max);
-                alpha[g] = (m_new == -INFINITY) ? 1.0f : exp2f(m_run[g] - m_new);
-                // P = 2^(z - m + 8); with no visible key yet (m = -inf) every
-                // z is -inf and P is 0
-                neg_m8[g] = (m_new == -INFINITY) ? 0.0f : 8.0f - m_new;
-                m_run[g] = m_new;
-            }
-            // Two heads at a time: P of heads g and g + 1 for this key as a
-            // packed f16 pair, split into two e4m3 terms, hi = e4m3(P) and
-            // lo = e4m3(P - hi) (the difference is exact in f16).
-#pragma unroll
-            for (int g = 0; g < GH; g += 2) {
-                float ls0 = 0.0f, ls1 = 0.0f;
-#pragma unroll
-                for (int kb = 0; kb < C::kKB; ++kb) {
-                    const float p0 = ex2_approx(z[kb][g] + neg_m8[g]);
-                    const float p1 = ex2_approx(z[kb][g + 1] + neg_m8[g + 1]);
-                    if constexpr (kPT) {   // the row sum takes P / v_scale
-                        ls0 = fmaf(p0, tiv[kb], ls0);
-                        ls1 = fmaf(p1, tiv[kb], ls1);
-                    } else {
-                        ls0 += p0;
-                        ls1 += p1;
-                    }
-                    const __half2 ph = __floats2half2_rn(p0, p1);
-                    const uint32_t h8 = __nv_cvt_halfraw2_to_fp8x2(ph, __NV_SATFINITE, __NV_E4M3);
-                    const __half2 hh = e4m3x2_to_half2(static_cast<uint16_t>(h8));
-                    const uint32_t l8 =
-                        __nv_cvt_halfraw2_to_fp8x2(__hsub2(ph, hh), __NV_SATFINITE, __NV_E4M3);
-                    const uint32_t off0 = kb * (kNPad * 128) + sw128_offset(gbase + g, t);
-                    const uint32_t off1 = kb * (kNPad * 128) + sw128_offset(gbase + g + 1, t);
-                    phi[off0] = static_cast<uint8_t>(h8 & 0xFF);
-                    phi[off1] = static_cast<uint8_t>((h8 >> 8) & 0xFF);
-                    plo[off0] = static_cast<uint8_t>(l8 & 0xFF);
-                    plo[off1] = static_cast<uint8_t>((l8 >> 8) & 0xFF);
-                }
-                l_part[g] = fmaf(l_part[g], alpha[g], ls0);
-                l_part[g + 1] = fmaf(l_part[g + 1], alpha[g + 1], ls1);
-            }
-            // Keys past the sequence end may hold stale bytes (NaN codes
-            // included); zero their V rows so that 0 * V stays 0 in the MMA.
-            // (Warpgroup 0 does it; the PV waits for every consumer warp.)
-            if (hs == 0 && any_past_end) {
-                uint8_t *vtile = smem + (i % C::kStages) * C::kStageBytes + C::kTileBytes;
-#pragma unroll
-                for (int kb = 0; kb < C::kKB; ++kb) {
-                    if ((t0 + i) * C::kKeys + kb * 128 + t < len) continue;
-#pragma unroll
-                    for (int cb = 0; cb < C::kCB; ++cb) {
-                        uint4 *r = reinterpret_cast<uint4 *>(vtile + cb * C::kCBBytes +
-                                                             (kb * 128 + t) * 128);
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) r[c] = make_uint4(0, 0, 0, 0);
-                    }
-                }
+                *reinterpret_cast<uint2 *>(q8 + (d / 128) * (kNPad * 128) + sw128_offset(g, d % 128)) = packed;
             }
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full[i % C::kOBuf]);
-            if (i >= 2 && !take_o(i - 2, alpha_2)) { ok = false; break; }
-#pragma unroll
-            for (int g = 0; g < GH; ++g) {
-                alpha_2[g] = alpha_1[g];
-                alpha_1[g] = alpha[g];
-            }
-        }
-        if (ok && ntiles >= 2) ok = take_o(ntiles - 2, alpha_2);
-        if (ok && ntiles >= 1) ok = take_o(ntiles - 1, alpha_1);
+            if (lane == 0) mbar_arrive(q_full);
+        };
 
-        // l per head: sum of the thread partials of the warpgroup
-#pragma unroll
-        for (int g = 0; g < GH; ++g) {
-            const float s = warp_sum(l_part[g]);
-            if (lane == 0) lred[wq * 16 + g] = s;
+        DecItem it{0, 0, 0, -1};
+        ok = pop_item(it);
+        if (ok && it.ntiles > 0) {
+            load_q(it);
+            store_q8();
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(l_bar);
-        if (!warp_wait(l_bar, 0, fail, p.err)) ok = false;
-        if (p.direct_out) {
-            // the only split: out = bf16(v_scale * o / l), as the merge computes it
+        while (ok && it.ntiles > 0) {
+            const int ntiles = it.ntiles;
+            const ItemGeom gm = item_geom<C::kKeys>(p, it.b, it.split);
+            const int64_t len = gm.len, lo = gm.lo, t0 = gm.t0;
+            const int b = it.b, split = it.split, h0 = it.kvh * p.G;
+            const uint16_t *bias = p.rel ? p.rel + static_cast<int64_t>(b) * p.bias_tok_stride +
+                                               static_cast<int64_t>(h0 + gbase) * p.rel_extent
+                                         : nullptr;
+
+            // rescale factors of the two previous tiles (a tile's O^T is taken two
+            // tiles later): alpha_1 of tile j - 1, alpha_2 of tile j - 2
+            float m_run[GH], l_part[GH], alpha_1[GH], alpha_2[GH], o_acc[C::kCB][GH];
 #pragma unroll
             for (int g = 0; g < GH; ++g) {
-                if (gbase + g < p.G) {
-                    const float L = lred[g] + lred[16 + g] + lred[32 + g] + lred[48 + g];
-                    const bool live = ok && m_run[g] != -INFINITY;
-                    const float f = (live && L > 0.0f) ? p.out_scale / L : 0.0f;
-                    uint16_t *o = p.out + (static_cast<int64_t>(b) * p.Hq + h0 + gbase + g) * D;
+                m_run[g] = -INFINITY;
+                l_part[g] = 0.0f;
+                alpha_1[g] = alpha_2[g] = 1.0f;
 #pragma unroll
-                    for (int mh = 0; mh < C::kCB; ++mh)
-                        o[mh * 128 + t] = __bfloat16_as_ushort(
-                            __float2bfloat16_rn((live ? o_acc[mh][g] : 0.0f) * f));
+                for (int mh = 0; mh < C::kCB; ++mh) o_acc[mh][g] = 0.0f;
+            }
+            // Accumulate this warpgroup's heads of O^T of the CTA's tile j
+            // (rescaled) into the registers.
+            auto take_o = [&](int j, const float *alpha) -> bool {
+                const int ob = j % C::kOBuf;
+                if (!warp_wait(&o_full[ob], (j / C::kOBuf) & 1, fail, p.err)) return false;
+                tc_fence_after_sync();
+#pragma unroll
+                for (int mh = 0; mh < C::kCB; ++mh) {
+                    // this warpgroup's columns: the P_hi product of head g in
+                    // o[g], the P_lo product in o[GH + g]
+                    float o[16];
+                    tmem_ld_x16(tmem + lane_base + C::kColO + (ob * C::kCB + mh) * NP + 2 * gbase, o);
+#pragma unroll
+                    for (int g = 0; g < GH; ++g)
+                        o_acc[mh][g] = fmaf(o_acc[mh][g], alpha[g], o[g] + o[GH + g]);
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&o_free[ob]);
+                return true;
+            };
+
+            // kPT: the raw scales of this thread's keys of tile i (ksc, vsc),
+            // loaded a tile ahead so that their latency stays off the chain
+            float ksc[C::kKB], vsc[C::kKB];
+            auto load_scales = [&](int i) {
+#pragma unroll
+                for (int kb = 0; kb < C::kKB; ++kb) {
+                    const int64_t key = (t0 + i) * C::kKeys + kb * 128 + t;
+                    const int64_t lb = key / p.block_size;
+                    ksc[kb] = 1.0f;
+                    vsc[kb] = 0.0f;   // marks a key that is not visible
+                    if (i < ntiles && key < len && key >= lo && lb < p.max_blocks) {
+                        const int32_t id =
+                            __ldg(p.block_table + static_cast<int64_t>(b) * p.max_blocks + lb);
+                        if (id >= 0 && id < p.num_blocks) {
+                            const int64_t si = (static_cast<int64_t>(id) * p.num_kv_heads + it.kvh) *
+                                                   p.block_size + key % p.block_size;
+                            ksc[kb] = __ldg(p.k_tok_scale + si);
+                            vsc[kb] = __ldg(p.v_tok_scale + si);
+                        }
+                    }
+                }
+            };
+            if constexpr (kPT) load_scales(0);
+            DecItem nx{0, 0, 0, -1};
+            for (int i = 0; i < ntiles; ++i) {
+                const int TT = T + i;
+                if (i == ntiles - 1) {
+                    // the next item: its record and its Q rows, in flight
+                    // during this tile
+                    if (!pop_item(nx)) { ok = false; break; }
+                    if (nx.ntiles > 0) load_q(nx);
+                }
+                // per-token factors of this thread's keys: K scale, log2 and
+                // reciprocal of the V scale (1, 0, 0 where not visible; the
+                // score of such a key is -inf anyway)
+                float tsk[C::kKB], tlv[C::kKB], tiv[C::kKB];
+                if constexpr (kPT) {
+#pragma unroll
+                    for (int kb = 0; kb < C::kKB; ++kb) {
+                        const float sv = vsc[kb];
+                        const float lv = log2f(sv);
+                        tsk[kb] = ksc[kb];
+                        // below 2^-60 the exponent takes 2^-60 (and the sum its
+                        // reciprocal): P stays far from fp32 underflow, at an
+                        // error below p * 2^-60 * 448
+                        tlv[kb] = sv > 0.0f ? fmaxf(lv, kMinLog2VScale) : 0.0f;
+                        tiv[kb] = sv > 0.0f ? (lv > kMinLog2VScale ? __frcp_rn(sv) : 0x1p60f) : 0.0f;
+                    }
+                    load_scales(i + 1);   // the next tile's, in flight during this one
+                }
+                if (!warp_wait(&s_full[TT & 1], (TT >> 1) & 1, fail, p.err)) { ok = false; break; }
+                tc_fence_after_sync();
+                float sc[C::kKB][16];
+#pragma unroll
+                for (int kb = 0; kb < C::kKB; ++kb)
+                    tmem_ld_x16(tmem + lane_base + ((TT & 1) * C::kKB + kb) * kNPad + gbase, sc[kb]);
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s_free[TT & 1]);
+
+                // this thread's keys: t, t + 128, ... of the tile
+                float z[C::kKB][GH];
+                bool any_past_end = false;
+#pragma unroll
+                for (int kb = 0; kb < C::kKB; ++kb) {
+                    const int64_t key = (t0 + i) * C::kKeys + kb * 128 + t;
+                    const bool valid = key < len && key >= lo;
+                    any_past_end |= key >= len;
+                    const int64_t dist = len - 1 - key;
+                    const bool has_bias = bias && valid && dist < p.rel_extent;
+#pragma unroll
+                    for (int g = 0; g < GH; ++g) {
+                        float zz = -INFINITY;
+                        if (valid && gbase + g < p.G) {
+                            zz = kPT ? fmaf(sc[kb][g], p.score_log2 * tsk[kb], tlv[kb])
+                                     : sc[kb][g] * p.score_log2;
+                            if (has_bias)
+                                zz = fmaf(bf16_bits_to_float(__ldg(bias + g * p.rel_extent + dist)),
+                                          kLog2e, zz);
+                        }
+                        z[kb][g] = zz;
+                    }
+                }
+                // block-wide max per head: warp shuffles, then the 4 warps of the
+                // warpgroup via shared memory and a (bounded) mbarrier exchange
+                float *rb = red + (TT & 1) * 64;
+#pragma unroll
+                for (int g = 0; g < GH; ++g) {
+                    float mx = z[0][g];
+#pragma unroll
+                    for (int kb = 1; kb < C::kKB; ++kb) mx = fmaxf(mx, z[kb][g]);
+                    mx = warp_max(mx);
+                    if (lane == 0) rb[wq * 16 + g] = mx;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&red_bar[TT & 1]);
+                if (!warp_wait(&red_bar[TT & 1], (TT >> 1) & 1, fail, p.err)) { ok = false; break; }
+                float alpha[GH], neg_m8[GH];
+                uint8_t *pt = smem + C::kOffP + (TT % C::kOBuf) * 2 * C::kPBytes;
+#pragma unroll
+                for (int g = 0; g < GH; ++g) {
+                    const float tile_max =
+                        fmaxf(fmaxf(rb[g], rb[16 + g]), fmaxf(rb[32 + g], rb[48 + g]));
+                    const float m_new = fmaxf(m_run[g], tile_max);
+                    alpha[g] = (m_new == -INFINITY) ? 1.0f : exp2f(m_run[g] - m_new);
+                    // P = 2^(z - m + 8); with no visible key yet (m = -inf) every
+                    // z is -inf and P is 0
+                    neg_m8[g] = (m_new == -INFINITY) ? 0.0f : 8.0f - m_new;
+                    m_run[g] = m_new;
+                }
+                // Two heads at a time: P of heads g and g + 1 for this key as a
+                // packed f16 pair, split into two e4m3 terms, hi = e4m3(P) and
+                // lo = e4m3(P - hi) (the difference is exact in f16).
+#pragma unroll
+                for (int g = 0; g < GH; g += 2) {
+                    float ls0 = 0.0f, ls1 = 0.0f;
+#pragma unroll
+                    for (int kb = 0; kb < C::kKB; ++kb) {
+                        const float p0 = ex2_approx(z[kb][g] + neg_m8[g]);
+                        const float p1 = ex2_approx(z[kb][g + 1] + neg_m8[g + 1]);
+                        if constexpr (kPT) {   // the row sum takes P / v_scale
+                            ls0 = fmaf(p0, tiv[kb], ls0);
+                            ls1 = fmaf(p1, tiv[kb], ls1);
+                        } else {
+                            ls0 += p0;
+                            ls1 += p1;
+                        }
+                        const __half2 ph = __floats2half2_rn(p0, p1);
+                        const uint32_t h8 = __nv_cvt_halfraw2_to_fp8x2(ph, __NV_SATFINITE, __NV_E4M3);
+                        const __half2 hh = e4m3x2_to_half2(static_cast<uint16_t>(h8));
+                        const uint32_t l8 =
+                            __nv_cvt_halfraw2_to_fp8x2(__hsub2(ph, hh), __NV_SATFINITE, __NV_E4M3);
+                        uint8_t *blk = pt + kb * C::kPBlock;
+                        const int r_hi = 2 * gbase + g, r_lo = 2 * gbase + GH + g;
+                        blk[sw128_offset(r_hi, t)] = static_cast<uint8_t>(h8 & 0xFF);
+                        blk[sw128_offset(r_hi + 1, t)] = static_cast<uint8_t>((h8 >> 8) & 0xFF);
+                        blk[sw128_offset(r_lo, t)] = static_cast<uint8_t>(l8 & 0xFF);
+                        blk[sw128_offset(r_lo + 1, t)] = static_cast<uint8_t>((l8 >> 8) & 0xFF);
+                    }
+                    l_part[g] = fmaf(l_part[g], alpha[g], ls0);
+                    l_part[g + 1] = fmaf(l_part[g + 1], alpha[g + 1], ls1);
+                }
+                // Keys past the sequence end may hold stale bytes (NaN codes
+                // included); zero their V rows so that 0 * V stays 0 in the MMA.
+                // (Warpgroup 0 does it; the PV waits for every consumer warp.)
+                if (hs == 0 && any_past_end) {
+                    uint8_t *vtile = smem + (TT % C::kStages) * C::kStageBytes + C::kTileBytes;
+#pragma unroll
+                    for (int kb = 0; kb < C::kKB; ++kb) {
+                        if ((t0 + i) * C::kKeys + kb * 128 + t < len) continue;
+#pragma unroll
+                        for (int cb = 0; cb < C::kCB; ++cb) {
+                            uint4 *r = reinterpret_cast<uint4 *>(vtile + cb * C::kCBBytes +
+                                                                 (kb * 128 + t) * 128);
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) r[c] = make_uint4(0, 0, 0, 0);
+                        }
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&p_full[TT % C::kOBuf]);
+                // the MMA thread takes the next item's Q8 after this item's last P
+                if (i == ntiles - 1 && nx.ntiles > 0) store_q8();
+                if (i >= 2 && !take_o(TT - 2, alpha_2)) { ok = false; break; }
+#pragma unroll
+                for (int g = 0; g < GH; ++g) {
+                    alpha_2[g] = alpha_1[g];
+                    alpha_1[g] = alpha[g];
                 }
             }
-        }
-        const int64_t row0 = (static_cast<int64_t>(b) * p.Hq + h0 + gbase) * p.num_slots + split;
-        if (!p.direct_out && t == 0) {
+            if (ok && ntiles >= 2) ok = take_o(T + ntiles - 2, alpha_2);
+            if (ok && ntiles >= 1) ok = take_o(T + ntiles - 1, alpha_1);
+
+            // l per head: sum of the thread partials of the warpgroup
 #pragma unroll
             for (int g = 0; g < GH; ++g) {
-                if (gbase + g < p.G) {
-                    float *ml = p.part_ml + (row0 + static_cast<int64_t>(g) * p.num_slots) * 2;
-                    ml[0] = ok ? m_run[g] : -INFINITY;
-                    ml[1] = lred[g] + lred[16 + g] + lred[32 + g] + lred[48 + g];
+                const float s = warp_sum(l_part[g]);
+                if (lane == 0) lred[wq * 16 + g] = s;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(l_bar);
+            if (ok && !warp_wait(l_bar, A & 1, fail, p.err)) ok = false;
+            if (p.direct_out) {
+                // the only split: out = bf16(v_scale * o / l), as the merge computes it
+#pragma unroll
+                for (int g = 0; g < GH; ++g) {
+                    if (gbase + g < p.G) {
+                        const float L = lred[g] + lred[16 + g] + lred[32 + g] + lred[48 + g];
+                        const bool live = ok && m_run[g] != -INFINITY;
+                        const float f = (live && L > 0.0f) ? p.out_scale / L : 0.0f;
+                        uint16_t *o = p.out + (static_cast<int64_t>(b) * p.Hq + h0 + gbase + g) * D;
+#pragma unroll
+                        for (int mh = 0; mh < C::kCB; ++mh)
+                            o[mh * 128 + t] = __bfloat16_as_ushort(
+                                __float2bfloat16_rn((live ? o_acc[mh][g] : 0.0f) * f));
+                    }
                 }
             }
-        }
+            const int64_t row0 = (static_cast<int64_t>(b) * p.Hq + h0 + gbase) * p.num_slots + split;
+            if (!p.direct_out && t == 0) {
 #pragma unroll
-        for (int g = 0; g < GH && !p.direct_out; ++g) {
-            if (gbase + g < p.G) {
-                float *po = p.part_o + (row0 + static_cast<int64_t>(g) * p.num_slots) * D;
-#pragma unroll
-                for (int mh = 0; mh < C::kCB; ++mh) po[mh * 128 + t] = o_acc[mh][g];
+                for (int g = 0; g < GH; ++g) {
+                    if (gbase + g < p.G) {
+                        float *ml = p.part_ml + (row0 + static_cast<int64_t>(g) * p.num_slots) * 2;
+                        ml[0] = ok ? m_run[g] : -INFINITY;
+                        ml[1] = lred[g] + lred[16 + g] + lred[32 + g] + lred[48 + g];
+                    }
+                }
             }
+#pragma unroll
+            for (int g = 0; g < GH && !p.direct_out; ++g) {
+                if (gbase + g < p.G) {
+                    float *po = p.part_o + (row0 + static_cast<int64_t>(g) * p.num_slots) * D;
+#pragma unroll
+                    for (int mh = 0; mh < C::kCB; ++mh) po[mh * 128 + t] = o_acc[mh][g];
+                }
+            }
+            T += ntiles;
+            ++A;
+            it = nx;
         }
     }
 
@@ -732,7 +914,7 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
     __syncthreads();
     if (warp == C::kMmaWarp) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem, C::kTmemCols);
+        tmem_dealloc(tmem, kTmemCols);
     }
 }
 
@@ -807,8 +989,9 @@ struct SplitPlan {
     int split_tiles;
 };
 
-// Split plan: enough CTAs for ~8 waves of the resident CTAs, at least 4096
-// keys per split, all splits of equal length in tiles.
+// Split plan: ~16 work items per resident CTA of the persistent launch (the
+// counter hands them out, so short last items even out the tail), at least
+// 2048 keys per split, all splits of equal length in tiles.
 bool plan_splits(int32_t num_seqs, int32_t num_kv_heads, int32_t head_dim,
                  int32_t max_blocks_per_seq, int32_t block_size, int32_t window,
                  int32_t split_tokens, int num_sms, SplitPlan *plan) {
@@ -826,14 +1009,14 @@ bool plan_splits(int32_t num_seqs, int32_t num_kv_heads, int32_t head_dim,
         st = split_tokens / keys;
     } else {
         const int64_t ctas_per_sm = head_dim == 128 ? DecCfg<128>::kCtasPerSm : 1;
-        const int64_t target = static_cast<int64_t>(num_sms) * ctas_per_sm * 8;
+        const int64_t target = static_cast<int64_t>(num_sms) * ctas_per_sm * 16;
         int64_t pairs = static_cast<int64_t>(num_seqs) * num_kv_heads;
         if (pairs < 1) pairs = 1;
         const int64_t want = (target + pairs - 1) / pairs;
         st = (tiles + want - 1) / want;
-        // at least 4096 keys per split: each CTA's start (TMEM, barriers, q
-        // quantization, the first loads) is paid once per split
-        const int64_t min_st = (4096 + keys - 1) / keys;
+        // at least 2048 keys per split: each split costs a partial result
+        // (written and merged) and a Q quantization
+        const int64_t min_st = (2048 + keys - 1) / keys;
         if (st < min_st) st = min_st;
     }
     const int64_t S = (tiles + st - 1) / st;
@@ -849,22 +1032,42 @@ int slots_for(int32_t head_dim, int num_splits) {
     return num_splits;
 }
 
+// Workspace: the partial o and (m, l) of every split, then the work-item
+// counter of the persistent launch (kSchedBytes).
+constexpr size_t kSchedBytes = 256;
+
 size_t workspace_bytes_for(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim, int slots) {
-    return static_cast<size_t>(num_seqs) * num_q_heads * slots * (head_dim + 2) * sizeof(float);
+    return static_cast<size_t>(num_seqs) * num_q_heads * slots * (head_dim + 2) * sizeof(float) +
+           kSchedBytes;
 }
 
 template <int D, int GMAX, bool kPT>
 fp8kv_status launch_decode(const CUtensorMap &km, const CUtensorMap &vm, const DecodeParams &p,
-                           int num_kv_heads, int num_seqs, cudaStream_t stream) {
+                           int num_sms, cudaStream_t stream) {
     using C = DecCfg<D>;
     auto kern = decode_kernel<D, GMAX, kPT>;
+    // The whole unified L1 as shared memory: without this preference an SM
+    // may take a carveout that holds only one of the kCtasPerSm CTAs.
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
-        cudaSuccess) {
+            cudaSuccess ||
+        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared) != cudaSuccess) {
         cudaGetLastError();
         return FP8KV_ERR_LAUNCH;
     }
-    dim3 grid(num_kv_heads, num_seqs, p.num_slots);
-    kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(km, vm, p);
+    // persistent: kCtasPerSm CTAs per SM at most; with no more items than
+    // that, one CTA per item and no counter
+    const int64_t slots = static_cast<int64_t>(num_sms) * C::kCtasPerSm;
+    int grid = static_cast<int>(slots);
+    DecodeParams q = p;
+    if (p.num_items <= slots) {
+        grid = p.num_items;
+        q.sched = nullptr;
+    } else if (cudaMemsetAsync(p.sched, 0, sizeof(uint32_t), stream) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8KV_ERR_LAUNCH;
+    }
+    kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(km, vm, q);
     if (cudaGetLastError() != cudaSuccess) return FP8KV_ERR_LAUNCH;
     return FP8KV_OK;
 }
@@ -993,20 +1196,25 @@ fp8kv_status decode_impl(const fp8kv_cache *cache, const fp8kv_bf16 *q, int32_t 
     p.out = out;
     p.out_scale = v_scale;
     p.direct_out = slots == 1 ? 1 : 0;
+    p.sched = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(workspace) + need - kSchedBytes);
+    p.num_seqs = num_seqs;
+    const int64_t items = static_cast<int64_t>(Hkv) * num_seqs * slots;
+    if (items >= (1ll << 31)) return FP8KV_ERR_UNSUPPORTED;
+    p.num_items = static_cast<int32_t>(items);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (pt) {
         if (D == 128)
-            st = G <= 8 ? launch_decode<128, 8, true>(km, vm, p, Hkv, num_seqs, s)
-                        : launch_decode<128, 16, true>(km, vm, p, Hkv, num_seqs, s);
+            st = G <= 8 ? launch_decode<128, 8, true>(km, vm, p, sms, s)
+                        : launch_decode<128, 16, true>(km, vm, p, sms, s);
         else
-            st = G <= 8 ? launch_decode<256, 8, true>(km, vm, p, Hkv, num_seqs, s)
-                        : launch_decode<256, 16, true>(km, vm, p, Hkv, num_seqs, s);
+            st = G <= 8 ? launch_decode<256, 8, true>(km, vm, p, sms, s)
+                        : launch_decode<256, 16, true>(km, vm, p, sms, s);
     } else if (D == 128) {
-        st = G <= 8 ? launch_decode<128, 8, false>(km, vm, p, Hkv, num_seqs, s)
-                    : launch_decode<128, 16, false>(km, vm, p, Hkv, num_seqs, s);
+        st = G <= 8 ? launch_decode<128, 8, false>(km, vm, p, sms, s)
+                    : launch_decode<128, 16, false>(km, vm, p, sms, s);
     } else {
-        st = G <= 8 ? launch_decode<256, 8, false>(km, vm, p, Hkv, num_seqs, s)
-                    : launch_decode<256, 16, false>(km, vm, p, Hkv, num_seqs, s);
+        st = G <= 8 ? launch_decode<256, 8, false>(km, vm, p, sms, s)
+                    : launch_decode<256, 16, false>(km, vm, p, sms, s);
     }
     if (st != FP8KV_OK) return st;
     if (p.direct_out) return FP8KV_OK;   // one split: the decode kernel wrote out

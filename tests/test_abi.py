@@ -139,13 +139,14 @@ def test_decode_rejects_bad_arguments_on_host(lib):
 def test_workspace_size_is_host_only_with_explicit_splits(lib):
     def per_slot(B, Hq, D):
         return B * Hq * (D + 2) * 4          # fp32 partial o plus (m, l) per query head
+    sched = 256                              # the persistent launch's work-item counter
     # 2 seqs x 8 q heads, max 4 blocks of 16 = 64 keys -> one split of 256 keys
-    n1 = lib.decode_workspace_size(2, 8, 2, 128, 4, 16, 0, 256)
+    n1 = lib.decode_workspace_size(2, 8, 2, 128, 4, 16, 0, 256) - sched
     assert n1 % per_slot(2, 8, 128) == 0
     slots_per_split = n1 // per_slot(2, 8, 128)
     assert 1 <= slots_per_split <= 4
     # 1024 keys in splits of 256 keys: 4 splits
-    n2 = lib.decode_workspace_size(1, 4, 1, 256, 64, 16, 0, 256)
+    n2 = lib.decode_workspace_size(1, 4, 1, 256, 64, 16, 0, 256) - sched
     assert n2 % per_slot(1, 4, 256) == 0 and (n2 // per_slot(1, 4, 256)) % 4 == 0
     assert lib.decode_workspace_size(1, 4, 1, 64, 4, 16, 0, 128) == 0
 
