@@ -122,6 +122,7 @@ struct DecodeParams {
     int32_t Hq;
     int32_t G;
     int32_t block_size;
+    int32_t bs_shift;       // log2(block_size) (a power of two)
     int32_t rel_extent;
     int32_t window;
     int32_t split_tiles;
@@ -693,7 +694,7 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
 #pragma unroll
                 for (int kb = 0; kb < C::kKB; ++kb) {
                     const int64_t key = (t0 + i) * C::kKeys + kb * 128 + t;
-                    const int64_t lb = key / p.block_size;
+                    const int64_t lb = key >> p.bs_shift;
                     ksc[kb] = 1.0f;
                     vsc[kb] = 0.0f;   // marks a key that is not visible
                     if (i < ntiles && key < len && key >= lo && lb < p.max_blocks) {
@@ -701,7 +702,7 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
                             __ldg(p.block_table + static_cast<int64_t>(b) * p.max_blocks + lb);
                         if (id >= 0 && id < p.num_blocks) {
                             const int64_t si = (static_cast<int64_t>(id) * p.num_kv_heads + it.kvh) *
-                                                   p.block_size + key % p.block_size;
+                                                   p.block_size + (key & (p.block_size - 1));
                             ksc[kb] = __ldg(p.k_tok_scale + si);
                             vsc[kb] = __ldg(p.v_tok_scale + si);
                         }
@@ -1174,6 +1175,7 @@ fp8kv_status decode_impl(const fp8kv_cache *cache, const fp8kv_bf16 *q, int32_t 
     p.Hq = num_q_heads;
     p.G = G;
     p.block_size = bs;
+    p.bs_shift = __builtin_ctz(static_cast<unsigned>(bs));
     p.rel_extent = rel_bias ? rel_extent : 0;
     p.window = window;
     p.split_tiles = plan.split_tiles;

@@ -87,6 +87,7 @@ struct PrefillParams {
     int32_t Hq;
     int32_t G;
     int32_t block_size;
+    int32_t bs_shift;       // log2(block_size) (a power of two)
     int32_t rel_extent;
     int32_t window;
     int32_t n_qtiles;
@@ -868,13 +869,13 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const int32_t key = t * kTile + 4 * lane + i;
-                        const int32_t lb = key / p.block_size;
+                        const int32_t lb = key >> p.bs_shift;
                         if (key < it.len_k && lb < p.max_blocks) {
                             const int32_t id =
                                 __ldg(p.block_table + static_cast<int64_t>(it.b) * p.max_blocks + lb);
                             if (id >= 0 && id < p.num_blocks) {
                                 const int64_t si = (static_cast<int64_t>(id) * p.num_kv_heads + kvh) *
-                                                       p.block_size + key % p.block_size;
+                                                       p.block_size + (key & (p.block_size - 1));
                                 const float sv = __ldg(p.v_tok_scale + si);
                                 const float lv = log2f(sv);
                                 fkp[i] = p.score_log2 * __ldg(p.k_tok_scale + si);
@@ -1508,6 +1509,7 @@ fp8kv_status prefill_impl(const fp8kv_cache *cache, const fp8kv_bf16 *q, int32_t
     p.Hq = num_q_heads;
     p.G = num_q_heads / Hkv;
     p.block_size = bs;
+    p.bs_shift = __builtin_ctz(static_cast<unsigned>(bs));
     p.rel_extent = rel_bias ? rel_extent : 0;
     p.bias_vec = rel_bias && (reinterpret_cast<uintptr_t>(rel_bias) & 15) == 0 &&
                  bias_tok_stride % 8 == 0 && rel_extent % 8 == 0;
