@@ -126,7 +126,12 @@ fp8kv_status kv_store_e4m3(const fp8kv_cache *cache, const fp8kv_bf16 *k,
  * window:       0 = full causal; W > 0 = only keys with (len-1) - j < W.
  * out:          device bf16 [num_seqs][num_q_heads][head_dim].
  * workspace:    device, >= fp8kv_decode_workspace_size(...) bytes, 16-byte
- *               aligned; holds the per-split partial results.
+ *               aligned; holds the per-split partial results and the work
+ *               counter of the persistent launch (the call zeroes it on the
+ *               stream before the launch).  Calls that overlap on the GPU
+ *               must not share a workspace.
+ * Launch: one persistent kernel of at most two CTAs per SM that take the
+ * splits from that counter, then (with more than one split) a merge kernel.
  */
 fp8kv_status paged_attn_fp8_decode(const fp8kv_cache *cache, const fp8kv_bf16 *q,
                                    int32_t num_q_heads, const int32_t *block_table,
