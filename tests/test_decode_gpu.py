@@ -201,6 +201,41 @@ def test_full_decode_1m(fk):
     _full(fk, workloads.DECODE_1M, (0, 8))
 
 
+def test_one_workspace_for_calls_of_different_shapes(fk):
+    """The persistent launch's work counter lives in the workspace: calls of
+    different sizes in a row on one workspace (the large one through the
+    counter, the small one with one CTA per item) give the results of calls on
+    fresh workspaces, bit for bit."""
+    big = workloads.make_decode(workloads.DecodeSpec("big", B=16, Hq=32, Hkv=4, D=128, block_size=16,
+                                                     ctx_lo=1000, ctx_hi=30000, rel_extent=1024),
+                                device=DEV, seed=40)
+    small = workloads.make_decode(workloads.DecodeSpec("small", B=3, Hq=8, Hkv=1, D=128,
+                                                       block_size=16, ctx_lo=10, ctx_hi=3000),
+                                  device=DEV, seed=41)
+    caches = []
+    for inp, spec_h in ((big, (4, 128)), (small, (1, 128))):
+        kv = inp["kv"]
+        c = fk.KVCache.empty(kv.num_blocks, 16, spec_h[0], spec_h[1], device=DEV)
+        fk.kv_store_e4m3(c, kv.k, kv.v, kv.slot_mapping, 1.0, 1.0)
+        caches.append(c)
+
+    def call(i, ws=None):
+        inp = (big, small)[i]
+        kv = inp["kv"]
+        return fk.paged_attn_fp8_decode(caches[i], inp["q"], kv.block_table, kv.seq_lens, 1.0, 1.0,
+                                        1.0, rel_bias=inp["rel"], workspace=ws).clone()
+    ref_big, ref_small = call(0), call(1)
+    kvb = big["kv"]
+    n = fk.decode_workspace_size(16, 32, 4, 128, kvb.max_blocks, 16, 0, 0)
+    ws = torch.empty(n, dtype=torch.uint8, device=DEV)
+    a1 = call(0, ws)
+    s1 = call(1, ws)
+    a2 = call(0, ws)
+    torch.cuda.synchronize()
+    assert fk.device_error() == 0
+    assert torch.equal(a1, ref_big) and torch.equal(a2, ref_big) and torch.equal(s1, ref_small)
+
+
 def test_bounded_wait_runs_out_and_the_next_call_is_clean(fk):
     """The failure path of a bounded wait, made to happen: the test hook makes
     the decode producer skip its first tile's copy (nothing else changes), so

@@ -248,3 +248,11 @@ def test_decode_dominant_keys_with_tiny_v(fk, oracle_lib):
     rows = [(b, h) for b in range(2) for h in range(8)]
     ref = oracle_rows_pt(oracle_lib, inp, rows, 1.0)
     assert_close(np.stack([got[b, h] for b, h in rows]), ref, "tiny V scales")
+
+
+def test_decode_long_sequences_through_the_work_counter(fk, oracle_lib):
+    """Enough splits (more work items than the persistent grid has CTAs) that
+    the CTAs take them from the counter; empty and one-key sequences among
+    them."""
+    run_decode(fk, oracle_lib, [40000, 33000, 0, 20000, 5000, 1, 12345, 38000], 32, 4, 128, 16,
+               E=1024, v_dist="v_t3", seed=5)
