@@ -232,6 +232,7 @@ class DecodeRun:
                                      spec.window, 0)
         self.ws = torch.empty(n, dtype=torch.uint8, device=dev)
         self.step_amax = torch.zeros(2, dtype=torch.float32, device=dev)
+        self.amax_views = (self.step_amax[0:1], self.step_amax[1:2])
         torch.cuda.synchronize()
         # algorithmic bytes
         E = 0 if self.rel is None else self.rel.shape[2]
@@ -252,7 +253,7 @@ class DecodeRun:
             self.cache, self.q if q is None else q, self.k_new if k_new is None else k_new,
             self.v_new if v_new is None else v_new, kv.block_table,
             kv.seq_lens if seq_lens is None else seq_lens, sq, sk, sv, rel_bias=self.rel,
-            window=self.spec.window, amax_k=self.step_amax[0:1], amax_v=self.step_amax[1:2],
+            window=self.spec.window, amax_k=self.amax_views[0], amax_v=self.amax_views[1],
             out=self.out if out is None else out, workspace=self.ws)
 
     def step_separate(self):

@@ -109,20 +109,30 @@ def _check(status: int, call: str):
 
 
 def _ptr(t: Optional[torch.Tensor]):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    return None if t is None else t.data_ptr()
 
 
-def _stream(stream) -> ctypes.c_void_p:
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream(stream) -> int:
+    """The CUDA stream handle: the given torch stream, else the current one."""
     if stream is None:
+        if _raw_stream is not None:
+            return _raw_stream(torch.cuda.current_device())
         stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream)
+    return stream.cuda_stream
 
 
 def _need(t: torch.Tensor, dtype, name: str, device=None):
-    if t.dtype != dtype:
+    if t.dtype is not dtype:
         raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
-    if device is not None and t.device != device:
-        raise ValueError("%s must be on %s" % (name, device))
+    if device is not None:
+        # a CUDA device compares by index (no device object per check)
+        ok = (t.is_cuda and t.get_device() == device.index) if device.type == "cuda" \
+            else t.device == device
+        if not ok:
+            raise ValueError("%s must be on %s" % (name, device))
 
 
 class KVCache:
@@ -137,6 +147,7 @@ class KVCache:
         if not (k.is_contiguous() and v.is_contiguous()):
             raise ValueError("cache arrays must be contiguous")
         self.k, self.v = k, v
+        self._device = k.device
         self.num_blocks, self.num_kv_heads, self.block_size, self.head_dim = k.shape
         self._c = CacheStruct(k.data_ptr(), v.data_ptr(), self.num_blocks, self.block_size,
                               self.num_kv_heads, self.head_dim)
@@ -151,7 +162,7 @@ class KVCache:
 
     @property
     def device(self):
-        return self.k.device
+        return self._device
 
     def c(self):
         return ctypes.byref(self._c)

@@ -4,6 +4,7 @@
 #include <math.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include <cudaTypedefs.h>
@@ -77,6 +78,26 @@ uint32_t *device_error_word() {
 }
 
 bool scale_ok(float s) { return isfinite(s) && s > 0.0f; }
+
+bool func_attrs_once(const void *func, std::atomic<uint64_t> *done, int smem_bytes,
+                     bool max_carveout) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return false;
+    }
+    const uint64_t bit = 1ull << dev;
+    if (done->load(std::memory_order_acquire) & bit) return true;
+    if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) !=
+            cudaSuccess ||
+        (max_carveout && cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                              cudaSharedmemCarveoutMaxShared) != cudaSuccess)) {
+        cudaGetLastError();
+        return false;
+    }
+    done->fetch_or(bit, std::memory_order_release);
+    return true;
+}
 
 bool make_cache_map(CUtensorMap *map, const uint8_t *base, int64_t num_blocks, int block_size,
                     int num_kv_heads, int head_dim) {

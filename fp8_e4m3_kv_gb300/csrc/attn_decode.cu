@@ -1049,13 +1049,9 @@ fp8kv_status launch_decode(const CUtensorMap &km, const CUtensorMap &vm, const D
     auto kern = decode_kernel<D, GMAX, kPT>;
     // The whole unified L1 as shared memory: without this preference an SM
     // may take a carveout that holds only one of the kCtasPerSm CTAs.
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared) != cudaSuccess) {
-        cudaGetLastError();
+    static std::atomic<uint64_t> attrs_set{0};
+    if (!func_attrs_once(reinterpret_cast<const void *>(kern), &attrs_set, C::kSmemBytes, true))
         return FP8KV_ERR_LAUNCH;
-    }
     // persistent: kCtasPerSm CTAs per SM at most; with no more items than
     // that, one CTA per item and no counter
     const int64_t slots = static_cast<int64_t>(num_sms) * C::kCtasPerSm;

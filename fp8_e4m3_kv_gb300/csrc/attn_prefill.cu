@@ -1422,11 +1422,10 @@ fp8kv_status launch_prefill2(const CUtensorMap &km, const CUtensorMap &vm, const
     const int cap = g_prefill_max_ctas.load(std::memory_order_relaxed);
     if (cap > 0 && cap < sms) sms = cap;
     if (!prefill2_registers_ok<kPT>()) return FP8KV_ERR_UNSUPPORTED;
-    if (cudaFuncSetAttribute(prefill2_kernel<kPT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Pre2Cfg::kSmemBytes) != cudaSuccess) {
-        cudaGetLastError();
+    static std::atomic<uint64_t> attrs_set{0};
+    if (!func_attrs_once(reinterpret_cast<const void *>(prefill2_kernel<kPT>), &attrs_set,
+                         Pre2Cfg::kSmemBytes, false))
         return FP8KV_ERR_LAUNCH;
-    }
     // persistent: two pipelines per CTA, at most one CTA per SM
     const int64_t n_pairs = (p.n_qtiles + 1) / 2;
     const int64_t n_items = n_pairs * p.Hq * num_seqs;
@@ -1442,11 +1441,9 @@ fp8kv_status launch_prefill(const CUtensorMap &km, const CUtensorMap &vm, const 
                             int num_seqs, cudaStream_t stream) {
     using C = PreCfg<D>;
     auto kern = prefill_kernel<D>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
-        cudaSuccess) {
-        cudaGetLastError();
+    static std::atomic<uint64_t> attrs_set{0};
+    if (!func_attrs_once(reinterpret_cast<const void *>(kern), &attrs_set, C::kSmemBytes, false))
         return FP8KV_ERR_LAUNCH;
-    }
     dim3 grid(p.n_qtiles, p.Hq, num_seqs);
     kern<<<grid, kPreThreads, C::kSmemBytes, stream>>>(km, vm, p);
     if (cudaGetLastError() != cudaSuccess) return FP8KV_ERR_LAUNCH;

@@ -12,6 +12,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/fp8kv.h"
 
 namespace fp8kv {
@@ -488,5 +490,11 @@ bool scale_ok(float s);
 // rejects it.
 bool make_cache_map(CUtensorMap *map, const uint8_t *base, int64_t num_blocks, int block_size,
                     int num_kv_heads, int head_dim);
+
+// Sets a kernel's dynamic shared-memory size (and, with max_carveout, the
+// preference for the whole unified L1 as shared memory) once per device;
+// `done` holds one bit per device already set.  False on a CUDA error.
+bool func_attrs_once(const void *func, std::atomic<uint64_t> *done, int smem_bytes,
+                     bool max_carveout);
 
 }  // namespace fp8kv
