@@ -985,6 +985,93 @@ decode_merge_kernel(const float *__restrict__ part_o, const float *__restrict__ 
     }
 }
 
+// The same merge for launches with few (sequence, query head) rows and many
+// splits (a single long sequence): a CTA takes one row and one of
+// `gridDim.z` slices of its D values, so that the GPU has enough loads in
+// flight.  Lane l of a warp holds float4 l % L of
+// the slice (L = slice / 4) for split (l / L) of the warp's group of
+// 32 / L splits; the warps take the groups round-robin, four splits per
+// thread in flight.  Empty splits (m = -inf) are skipped by a select, so
+// their never-written partials are loaded but not used.  The thread
+// partials are then summed in a fixed order.
+constexpr int kMergeUnroll = 4;
+
+template <int D>
+__global__ void __launch_bounds__(kMergeWarps * 32)
+decode_merge_sliced_kernel(const float *__restrict__ part_o, const float *__restrict__ part_ml,
+                    uint16_t *__restrict__ out, int32_t Hq, int32_t S, float v_scale) {
+    __shared__ float red_m[kMergeWarps];
+    __shared__ __align__(16) float4 red_acc[kMergeWarps * 32];
+    __shared__ float red_l[kMergeWarps * 32];
+    const int h = blockIdx.x, b = blockIdx.y;
+    const int slice = D / static_cast<int>(gridDim.z);   // D values of this CTA
+    const int L = slice / 4;                             // lanes per split row
+    const int G = 32 / L;                                // splits per warp step
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int sg = lane / L, qd = lane % L;
+    const int64_t row = static_cast<int64_t>(b) * Hq + h;
+    const float *ml = part_ml + row * S * 2;
+    float m = -INFINITY;
+    for (int s = threadIdx.x; s < S; s += kMergeWarps * 32) m = fmaxf(m, ml[2 * s]);
+    m = warp_max(m);
+    if (lane == 0) red_m[warp] = m;
+    __syncthreads();
+    m = red_m[0];
+#pragma unroll
+    for (int w = 1; w < kMergeWarps; ++w) m = fmaxf(m, red_m[w]);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float l = 0.0f;
+    if (m != -INFINITY) {
+        const int step = kMergeWarps * G;
+        const float4 *pbase = reinterpret_cast<const float4 *>(part_o + row * S * D) +
+                              (blockIdx.z * slice) / 4 + qd;
+        for (int s0 = warp * G + sg; s0 < S; s0 += kMergeUnroll * step) {
+            float ms[kMergeUnroll], ls[kMergeUnroll];
+            float4 ov[kMergeUnroll];
+#pragma unroll
+            for (int u = 0; u < kMergeUnroll; ++u) {
+                const int s = s0 + u * step;
+                const bool in = s < S;
+                ms[u] = in ? ml[2 * s] : -INFINITY;
+                ls[u] = in ? ml[2 * s + 1] : 0.0f;
+                ov[u] = in ? pbase[static_cast<int64_t>(s) * (D / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < kMergeUnroll; ++u) {
+                const bool live = ms[u] != -INFINITY;
+                const float w = live ? exp2f(ms[u] - m) : 0.0f;
+                l = live ? fmaf(ls[u], w, l) : l;
+                acc.x = live ? fmaf(ov[u].x, w, acc.x) : acc.x;
+                acc.y = live ? fmaf(ov[u].y, w, acc.y) : acc.y;
+                acc.z = live ? fmaf(ov[u].z, w, acc.z) : acc.z;
+                acc.w = live ? fmaf(ov[u].w, w, acc.w) : acc.w;
+            }
+        }
+    }
+    red_acc[threadIdx.x] = acc;
+    red_l[threadIdx.x] = qd == 0 ? l : 0.0f;   // one l per split row
+    __syncthreads();
+    // output float4 q of the slice: the threads with qd == q, in order
+    if (threadIdx.x < L) {
+        float L_sum = 0.0f;
+        for (int t = 0; t < kMergeWarps * 32; t += L) L_sum += red_l[t];
+        const float f = L_sum > 0.0f ? v_scale / L_sum : 0.0f;
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int t = threadIdx.x; t < kMergeWarps * 32; t += L) {
+            const float4 v = red_acc[t];
+            a.x += v.x;
+            a.y += v.y;
+            a.z += v.z;
+            a.w += v.w;
+        }
+        uint16_t *o = out + row * D + blockIdx.z * slice + 4 * threadIdx.x;
+        o[0] = __bfloat16_as_ushort(__float2bfloat16_rn(a.x * f));
+        o[1] = __bfloat16_as_ushort(__float2bfloat16_rn(a.y * f));
+        o[2] = __bfloat16_as_ushort(__float2bfloat16_rn(a.z * f));
+        o[3] = __bfloat16_as_ushort(__float2bfloat16_rn(a.w * f));
+    }
+}
+
 struct SplitPlan {
     int num_splits;
     int split_tiles;
@@ -1216,11 +1303,22 @@ fp8kv_status decode_impl(const fp8kv_cache *cache, const fp8kv_bf16 *q, int32_t 
     }
     if (st != FP8KV_OK) return st;
     if (p.direct_out) return FP8KV_OK;   // one split: the decode kernel wrote out
-    if (D == 128)
-        decode_merge_kernel<128><<<dim3(num_q_heads, num_seqs), kMergeWarps * 32, 0, s>>>(
+    // slices of D per (sequence, head) for the sliced merge: enough CTAs for
+    // two per SM, with at least 32 values (8 lanes of float4) per split row
+    int zs = 1;
+    while (zs < D / 32 && static_cast<int64_t>(num_q_heads) * num_seqs * zs < 2ll * sms) zs *= 2;
+    const dim3 mgrid(num_q_heads, num_seqs, zs);
+    if (zs == 1 && D == 128)
+        decode_merge_kernel<128><<<mgrid, kMergeWarps * 32, 0, s>>>(p.part_o, p.part_ml, out,
+                                                                   num_q_heads, slots, v_scale);
+    else if (zs == 1)
+        decode_merge_kernel<256><<<mgrid, kMergeWarps * 32, 0, s>>>(p.part_o, p.part_ml, out,
+                                                                   num_q_heads, slots, v_scale);
+    else if (D == 128)
+        decode_merge_sliced_kernel<128><<<mgrid, kMergeWarps * 32, 0, s>>>(
             p.part_o, p.part_ml, out, num_q_heads, slots, v_scale);
     else
-        decode_merge_kernel<256><<<dim3(num_q_heads, num_seqs), kMergeWarps * 32, 0, s>>>(
+        decode_merge_sliced_kernel<256><<<mgrid, kMergeWarps * 32, 0, s>>>(
             p.part_o, p.part_ml, out, num_q_heads, slots, v_scale);
     if (cudaGetLastError() != cudaSuccess) return FP8KV_ERR_LAUNCH;
     return FP8KV_OK;
