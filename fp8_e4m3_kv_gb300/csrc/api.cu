@@ -112,6 +112,25 @@ bool make_cache_map(CUtensorMap *map, const uint8_t *base, int64_t num_blocks, i
             cudaGetLastError();
     });
     if (!g_encode_tiled) return false;
+    // The map depends only on the arguments: the last few are kept per host
+    // thread, so a decode loop over the same cache encodes it once.
+    struct Entry {
+        const uint8_t *base;
+        int64_t num_blocks;
+        int block_size, num_kv_heads, head_dim;
+        CUtensorMap map;
+    };
+    constexpr int kEntries = 4;
+    thread_local Entry entries[kEntries];
+    thread_local int n_entries = 0, next = 0;
+    for (int i = 0; i < n_entries; ++i) {
+        const Entry &e = entries[i];
+        if (e.base == base && e.num_blocks == num_blocks && e.block_size == block_size &&
+            e.num_kv_heads == num_kv_heads && e.head_dim == head_dim) {
+            *map = e.map;
+            return true;
+        }
+    }
     // cache[block][head][row][d] as (d, row, head, block); one box is one
     // head's block_size rows x 128 bytes, a contiguous run of the cache
     const cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)block_size,
@@ -124,7 +143,17 @@ bool make_cache_map(CUtensorMap *map, const uint8_t *base, int64_t num_blocks, i
                                 dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    if (r != CUDA_SUCCESS) return false;
+    Entry &e = entries[next];
+    e.base = base;
+    e.num_blocks = num_blocks;
+    e.block_size = block_size;
+    e.num_kv_heads = num_kv_heads;
+    e.head_dim = head_dim;
+    e.map = *map;
+    next = (next + 1) % kEntries;
+    if (n_entries < kEntries) ++n_entries;
+    return true;
 }
 
 }  // namespace fp8kv
