@@ -312,6 +312,78 @@ def paged_attn_fp8_decode(cache: KVCache, q: torch.Tensor, block_table: torch.Te
     return out
 
 
+class DecodeStep:
+    """A decode call bound to fixed buffers, validated once.
+
+    ``run()`` launches paged_attn_fp8_decode (or, with k_new and v_new,
+    paged_attn_fp8_decode_store) over the buffers' current contents with no
+    per-call argument checks: only the stream is looked up.  It is meant for
+    decode loops that update q, k_new / v_new, seq_lens and the block table in
+    place, as a serving loop or a captured CUDA graph does.  The buffers must
+    keep their shapes and stay alive (the object holds references to them);
+    the results are those of the one-shot calls, bit for bit."""
+
+    def __init__(self, cache: KVCache, q: torch.Tensor, block_table: torch.Tensor,
+                 seq_lens: torch.Tensor, q_scale: float, k_scale: float, v_scale: float,
+                 softmax_scale: Optional[float] = None, rel_bias: Optional[torch.Tensor] = None,
+                 window: int = 0, out: Optional[torch.Tensor] = None,
+                 workspace: Optional[torch.Tensor] = None, k_new: Optional[torch.Tensor] = None,
+                 v_new: Optional[torch.Tensor] = None, amax_k: Optional[torch.Tensor] = None,
+                 amax_v: Optional[torch.Tensor] = None):
+        _need(q, torch.bfloat16, "q", cache.device)
+        if q.dim() != 3 or not q.is_contiguous() or q.shape[2] != cache.head_dim:
+            raise ValueError("q must be contiguous [B][Hq][D]")
+        B, Hq, D = q.shape
+        fused = k_new is not None or v_new is not None
+        if fused:
+            for name, t in (("k_new", k_new), ("v_new", v_new)):
+                if t is None:
+                    raise ValueError("k_new and v_new go together")
+                _need(t, torch.bfloat16, name, cache.device)
+                if tuple(t.shape) != (B, cache.num_kv_heads, D) or not t.is_contiguous():
+                    raise ValueError("%s must be contiguous [B][Hkv][D]" % name)
+            for a in (amax_k, amax_v):
+                if a is not None:
+                    _need(a, torch.float32, "amax", cache.device)
+        elif amax_k is not None or amax_v is not None:
+            raise ValueError("amax_k / amax_v need k_new and v_new")
+        _table_and_lens(block_table, seq_lens, B, cache.device)
+        if softmax_scale is None:
+            softmax_scale = 1.0 / math.sqrt(D)
+        rel, bstride, E = _bias_args(rel_bias, Hq)
+        if out is None:
+            out = torch.empty_like(q)
+        _need(out, torch.bfloat16, "out", cache.device)
+        if tuple(out.shape) != tuple(q.shape) or not out.is_contiguous():
+            raise ValueError("out must be contiguous [B][Hq][D]")
+        mb = block_table.shape[1]
+        n = decode_workspace_size(B, Hq, cache.num_kv_heads, D, mb, cache.block_size, window, 0)
+        if workspace is None:
+            workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=cache.device)
+        _need(workspace, torch.uint8, "workspace", cache.device)
+        if workspace.numel() < n or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous uint8 tensor of >= %d bytes" % n)
+        self.out = out
+        self._keep = (cache, q, block_table, seq_lens, rel, out, workspace, k_new, v_new, amax_k,
+                      amax_v)
+        ws_bytes = workspace.numel()
+        if fused:
+            self._fn, self._name = _decode_store, "paged_attn_fp8_decode_store"
+            self._args = (cache.c(), _ptr(q), Hq, _ptr(k_new), _ptr(v_new), _ptr(block_table), mb,
+                          _ptr(seq_lens), B, q_scale, k_scale, v_scale, softmax_scale, _ptr(rel),
+                          bstride, E, window, _ptr(amax_k), _ptr(amax_v), _ptr(out),
+                          _ptr(workspace), ws_bytes)
+        else:
+            self._fn, self._name = _decode_ex, "paged_attn_fp8_decode"
+            self._args = (cache.c(), _ptr(q), Hq, _ptr(block_table), mb, _ptr(seq_lens), B,
+                          q_scale, k_scale, v_scale, softmax_scale, _ptr(rel), bstride, E, window,
+                          _ptr(out), _ptr(workspace), ws_bytes, 0)
+
+    def run(self, stream=None) -> torch.Tensor:
+        _check(self._fn(*self._args, _stream(stream)), self._name)
+        return self.out
+
+
 def kv_store_e4m3_per_token(cache: KVCache, k: torch.Tensor, v: torch.Tensor,
                             slot_mapping: torch.Tensor, k_scales: torch.Tensor,
                             v_scales: torch.Tensor, stream=None) -> None:
@@ -521,7 +593,7 @@ def device_error(clear: bool = True) -> int:
     return int(w.value)
 
 
-__all__ = ["KVCache", "Fp8KVError", "kv_store_e4m3", "kv_amax_calibrate", "kv_band_counts",
+__all__ = ["KVCache", "Fp8KVError", "DecodeStep", "kv_store_e4m3", "kv_amax_calibrate", "kv_band_counts",
            "band_counts_dict", "BAND_COUNTS_BYTES", "scale_from_amax",
            "paged_attn_fp8_decode", "paged_attn_fp8_decode_noalloc", "paged_attn_fp8_decode_store",
            "kv_store_e4m3_per_token", "paged_attn_fp8_decode_per_token",

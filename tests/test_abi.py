@@ -280,6 +280,7 @@ def test_decode_bindings_check_table_and_lengths(lib):
             torch.zeros(2, 1, 128, dtype=torch.bfloat16), t, n, 1.0, 1.0, 1.0),
         "per_token": lambda t, n: lib.paged_attn_fp8_decode_per_token(
             cache, q, t, n, 1.0, torch.ones(4, 1, 16), torch.ones(4, 1, 16)),
+        "bound_step": lambda t, n: lib.DecodeStep(cache, q, t, n, 1.0, 1.0, 1.0),
     }
     bad = [
         (bt.to(torch.int64), lens, TypeError),                  # int64 table

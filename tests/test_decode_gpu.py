@@ -236,6 +236,39 @@ def test_one_workspace_for_calls_of_different_shapes(fk):
     assert torch.equal(a1, ref_big) and torch.equal(a2, ref_big) and torch.equal(s1, ref_small)
 
 
+def test_bound_decode_step_matches_the_calls(fk):
+    """DecodeStep.run() over buffers updated in place gives the one-shot calls'
+    results bit for bit, for decode and for the fused store + decode."""
+    spec = workloads.DecodeSpec("bound", B=12, Hq=32, Hkv=4, D=128, block_size=16,
+                                ctx_lo=500, ctx_hi=9000, rel_extent=1024)
+    inp = workloads.make_decode(spec, device=DEV, seed=50)
+    kv = inp["kv"]
+    cache = fk.KVCache.empty(kv.num_blocks, 16, 4, 128, device=DEV)
+    fk.kv_store_e4m3(cache, kv.k, kv.v, kv.slot_mapping, 1.0, 1.0)
+    q = inp["q"].clone()
+    step = fk.DecodeStep(cache, q, kv.block_table, kv.seq_lens, 1.0, 1.0, 1.0,
+                         rel_bias=inp["rel"])
+    for seed in (1, 2):   # new contents of q between runs
+        q.copy_(torch.randn(q.shape, generator=torch.Generator(DEV).manual_seed(seed),
+                            device=DEV).to(torch.bfloat16))
+        got = step.run().clone()
+        ref = fk.paged_attn_fp8_decode(cache, q, kv.block_table, kv.seq_lens, 1.0, 1.0, 1.0,
+                                       rel_bias=inp["rel"])
+        torch.cuda.synchronize()
+        assert torch.equal(got, ref)
+    # fused: the same new token stored by both (the cache bytes are identical)
+    k_new = torch.randn(12, 4, 128, device=DEV).to(torch.bfloat16)
+    v_new = torch.randn(12, 4, 128, device=DEV).to(torch.bfloat16)
+    fused = fk.DecodeStep(cache, q, kv.block_table, kv.seq_lens, 1.0, 1.0, 1.0,
+                          rel_bias=inp["rel"], k_new=k_new, v_new=v_new)
+    got = fused.run().clone()
+    ref = fk.paged_attn_fp8_decode_store(cache, q, k_new, v_new, kv.block_table, kv.seq_lens, 1.0,
+                                         1.0, 1.0, rel_bias=inp["rel"])
+    torch.cuda.synchronize()
+    assert fk.device_error() == 0
+    assert torch.equal(got, ref)
+
+
 def test_bounded_wait_runs_out_and_the_next_call_is_clean(fk):
     """The failure path of a bounded wait, made to happen: the test hook makes
     the decode producer skip its first tile's copy (nothing else changes), so
