@@ -1091,9 +1091,9 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
             const int g0 = g;
             const int n = it.kt_hi - it.kt_lo + 1;
             g += n;
-            const int64_t pos = it.P0 + r;
+            const int32_t pos = it.P0 + r;   // positions are int32
             const bool row_ok = r < it.n_rows;
-            const int64_t pos_first = it.P0, pos_last = it.P0 + it.n_rows - 1;
+            const int32_t pos_first = it.P0, pos_last = it.P0 + it.n_rows - 1;
             const int64_t tok0 = static_cast<int64_t>(it.q_first) + it.qt * kTile;
             const uint16_t *bias_row =
                 (p.rel && row_ok) ? p.rel + (tok0 + r) * p.bias_tok_stride +
@@ -1158,10 +1158,10 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
             float2 lsum = make_float2(0.0f, 0.0f);   // two partial row sums
             float err_bound = 0.0f;   // sum of p_max * l_half over single-term halves
             for (int j = 0; j < n && ok; ++j) {
-                const int64_t k0 = static_cast<int64_t>(it.kt_lo + j) * kTile;
+                const int32_t k0 = (it.kt_lo + j) * kTile;
                 for (int hh = 0; hh < 2; ++hh) {
                     const int u = 2 * c + hh;   // unit: key half hh of this key tile
-                    const int64_t kh = k0 + hh * C::kHalf;
+                    const int32_t kh = k0 + hh * C::kHalf;
                     const bool full_half = (kh + C::kHalf - 1 <= pos_first) &&
                                            (p.window == 0 || pos_last - kh < p.window);
                     const bool bias_half = bias_row != nullptr && pos - kh >= 0 &&
@@ -1473,7 +1473,8 @@ fp8kv_status prefill_impl(const fp8kv_cache *cache, const fp8kv_bf16 *q, int32_t
     const int D = cache->head_dim, bs = cache->block_size, Hkv = cache->num_kv_heads;
     if (Hkv <= 0 || cache->num_blocks < 0 || num_q_heads % Hkv != 0) return FP8KV_ERR_ARG;
     if ((D != 128 && D != 256) || (bs != 16 && bs != 32 && bs != 64 && bs != 128) ||
-        num_seqs > 65535 || num_q_heads > 65535 || cache->num_blocks >= (1ll << 31))
+        num_seqs > 65535 || num_q_heads > 65535 || cache->num_blocks >= (1ll << 31) ||
+        static_cast<int64_t>(max_blocks_per_seq) * bs > (1ll << 31) - 256)   // int32 positions
         return FP8KV_ERR_UNSUPPORTED;
     if (rel_bias && (rel_extent <= 0 || bias_tok_stride < 0)) return FP8KV_ERR_ARG;
     if (num_seqs == 0 || max_seqlen_q == 0) return FP8KV_OK;
