@@ -648,7 +648,9 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
         while (ok && it.ntiles > 0) {
             const int ntiles = it.ntiles;
             const ItemGeom gm = item_geom<C::kKeys>(p, it.b, it.split);
-            const int64_t len = gm.len, lo = gm.lo, t0 = gm.t0;
+            // positions fit in int32 (the host bounds the block table's keys)
+            const int32_t len = static_cast<int32_t>(gm.len), lo = static_cast<int32_t>(gm.lo),
+                          t0 = static_cast<int32_t>(gm.t0);
             const int b = it.b, split = it.split, h0 = it.kvh * p.G;
             const uint16_t *bias = p.rel ? p.rel + static_cast<int64_t>(b) * p.bias_tok_stride +
                                                static_cast<int64_t>(h0 + gbase) * p.rel_extent
@@ -693,8 +695,8 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
             auto load_scales = [&](int i) {
 #pragma unroll
                 for (int kb = 0; kb < C::kKB; ++kb) {
-                    const int64_t key = (t0 + i) * C::kKeys + kb * 128 + t;
-                    const int64_t lb = key >> p.bs_shift;
+                    const int32_t key = (t0 + i) * C::kKeys + kb * 128 + t;
+                    const int32_t lb = key >> p.bs_shift;
                     ksc[kb] = 1.0f;
                     vsc[kb] = 0.0f;   // marks a key that is not visible
                     if (i < ntiles && key < len && key >= lo && lb < p.max_blocks) {
@@ -752,10 +754,10 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
                 bool any_past_end = false;
 #pragma unroll
                 for (int kb = 0; kb < C::kKB; ++kb) {
-                    const int64_t key = (t0 + i) * C::kKeys + kb * 128 + t;
+                    const int32_t key = (t0 + i) * C::kKeys + kb * 128 + t;
                     const bool valid = key < len && key >= lo;
                     any_past_end |= key >= len;
-                    const int64_t dist = len - 1 - key;
+                    const int32_t dist = len - 1 - key;
                     const bool has_bias = bias && valid && dist < p.rel_extent;
 #pragma unroll
                     for (int g = 0; g < GH; ++g) {
@@ -1212,7 +1214,8 @@ fp8kv_status decode_impl(const fp8kv_cache *cache, const fp8kv_bf16 *q, int32_t 
     if (Hkv <= 0 || cache->num_blocks < 0 || num_q_heads % Hkv != 0) return FP8KV_ERR_ARG;
     const int G = num_q_heads / Hkv;
     if ((D != 128 && D != 256) || G > kNPad || (bs != 16 && bs != 32 && bs != 64 && bs != 128) ||
-        num_seqs > 65535 || Hkv > 65535 || num_q_heads > 65535 || cache->num_blocks >= (1ll << 31))
+        num_seqs > 65535 || Hkv > 65535 || num_q_heads > 65535 || cache->num_blocks >= (1ll << 31) ||
+        static_cast<int64_t>(max_blocks_per_seq) * bs > (1ll << 31) - 256)   // int32 positions
         return FP8KV_ERR_UNSUPPORTED;
     if (rel_bias && (rel_extent <= 0 || bias_tok_stride < 0)) return FP8KV_ERR_ARG;
     if (split_tokens % (D == 128 ? DecCfg<128>::kKeys : DecCfg<256>::kKeys)) return FP8KV_ERR_ARG;
