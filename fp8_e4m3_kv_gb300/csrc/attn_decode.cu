@@ -729,13 +729,16 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
 #pragma unroll
                     for (int kb = 0; kb < C::kKB; ++kb) {
                         const float sv = vsc[kb];
-                        const float lv = log2f(sv);
+                        // the hardware log2 and reciprocal: their ~2^-22 relative
+                        // errors move a key's weight by ~1e-5 of itself, far
+                        // below the e4m3 rounding of P
+                        const float lv = __log2f(sv);
                         tsk[kb] = ksc[kb];
                         // below 2^-60 the exponent takes 2^-60 (and the sum its
                         // reciprocal): P stays far from fp32 underflow, at an
                         // error below p * 2^-60 * 448
                         tlv[kb] = sv > 0.0f ? fmaxf(lv, kMinLog2VScale) : 0.0f;
-                        tiv[kb] = sv > 0.0f ? (lv > kMinLog2VScale ? __frcp_rn(sv) : 0x1p60f) : 0.0f;
+                        tiv[kb] = sv > 0.0f ? (lv > kMinLog2VScale ? __fdividef(1.0f, sv) : 0x1p60f) : 0.0f;
                     }
                     load_scales(i + 1);   // the next tile's, in flight during this one
                 }
