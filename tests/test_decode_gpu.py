@@ -107,6 +107,15 @@ def test_explicit_splits_agree(fk, split):
             assert (np.abs(f - a) <= tol).all(), (b, h, float(np.abs(f - a).max()))
 
 
+def test_sixteen_heads_per_kv_head_through_the_work_counter(fk):
+    """16 query heads per KV head with more splits than CTAs (the counter
+    path), sampled rows against the oracle."""
+    rng = np.random.default_rng(3)
+    lens = [int(x) for x in rng.integers(5000, 20000, 32)]
+    rows = [(b, h) for b in (0, 7, 19, 31) for h in (0, 5, 16, 31)]
+    run_case(fk, lens, 32, 2, 128, 16, E=128, seed=21, rows=rows)
+
+
 def test_empty_and_single_key(fk):
     """len 0 gives zeros; len 1 gives v_scale * v8 of the only key (exact)."""
     err, got = run_case(fk, [0, 1, 5], 4, 1, 128, 16, scales=(1.0, 1.0, 2.0), seed=12,

@@ -86,3 +86,11 @@ def test_fused_step_against_oracle(fk):
     ref = oracle_decode_rows(inp, rows, 1.0, 1.0, 1.0, window=0, rel=inp["rel"])
     got = out.float().cpu().numpy()
     assert_close(np.stack([got[b, h] for b, h in rows]), ref, "fused decode")
+
+
+@pytest.mark.parametrize("D", [128, 256])
+def test_fused_step_through_the_work_counter(fk, D):
+    """More splits than the persistent grid has CTAs (the CTAs take them from
+    the counter), with an empty and a one-key sequence among them."""
+    lens = [40000, 30000, 0, 20000, 9000, 1] if D == 128 else [30000, 20000, 5000, 0]
+    run_both(fk, lens, 32 if D == 128 else 24, 4, D, 16, scales=(1.0, 1.0, 3.0), E=1024, seed=7)
