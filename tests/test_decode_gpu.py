@@ -20,7 +20,8 @@ def fk():
 
 
 def run_case(fk, lens, Hq, Hkv, D, bs, scales=(1.0, 1.0, 1.0), window=0, E=0, bias_bcast=False,
-             v_dist="normal", seed=0, split_tokens=0, fill=0x7F, rows=None, plant=False):
+             v_dist="normal", seed=0, split_tokens=0, fill=0x7F, rows=None, plant=False,
+             out_nan=False):
     spec = workloads.DecodeSpec("case", B=len(lens), Hq=Hq, Hkv=Hkv, D=D, block_size=bs,
                                 ctx_lo=1, ctx_hi=1, v_dist=v_dist, rel_extent=E, plant_v=plant)
     inp = workloads.make_decode(spec, device="cpu", seed=seed, lens=lens)
@@ -33,8 +34,12 @@ def run_case(fk, lens, Hq, Hkv, D, bs, scales=(1.0, 1.0, 1.0), window=0, E=0, bi
     cache = fk.KVCache.empty(kv.num_blocks, bs, Hkv, D, device=DEV, fill=fill)
     fk.kv_store_e4m3(cache, kd.k, kd.v, kd.slot_mapping, sk, sv)
     rel_d = None if inp["rel"] is None else inp["rel"].to(DEV)
+    # out_nan: the output starts as NaN, so a row the kernels skip shows up
+    out0 = (torch.full((len(lens), Hq, D), float("nan"), dtype=torch.bfloat16, device=DEV)
+            if out_nan else None)
     out = fk.paged_attn_fp8_decode(cache, inp["q"].to(DEV), kd.block_table, kd.seq_lens, sq, sk,
-                                   sv, rel_bias=rel_d, window=window, split_tokens=split_tokens)
+                                   sv, rel_bias=rel_d, window=window, split_tokens=split_tokens,
+                                   out=out0)
     torch.cuda.synchronize()
     assert fk.device_error() == 0
     got = out.float().cpu().numpy()
@@ -114,6 +119,23 @@ def test_sixteen_heads_per_kv_head_through_the_work_counter(fk):
     lens = [int(x) for x in rng.integers(5000, 20000, 32)]
     rows = [(b, h) for b in (0, 7, 19, 31) for h in (0, 5, 16, 31)]
     run_case(fk, lens, 32, 2, 128, 16, E=128, seed=21, rows=rows)
+
+
+@pytest.mark.parametrize("window", [0, 3000])
+def test_empty_and_short_sequences_among_long_ones_through_the_work_counter(fk, window):
+    """Empty, one-key and short sequences beside long ones, with more items
+    than CTAs (the counter path): every row is written (the output starts as
+    NaN), empty sequences give zeros, sampled rows match the oracle."""
+    rng = np.random.default_rng(5)
+    lens = [int(x) for x in rng.integers(8000, 20000, 40)]
+    for b, n in ((0, 0), (3, 1), (9, 0), (17, 200), (25, 0), (39, 2049)):
+        lens[b] = n
+    rows = [(b, h) for b in (3, 5, 17, 30, 39) for h in (0, 13, 31)]
+    err, got = run_case(fk, lens, 32, 4, 128, 16, E=128, window=window, seed=23, rows=rows,
+                        split_tokens=2048, out_nan=True)
+    assert not np.isnan(got).any()
+    for b in (0, 9, 25):
+        assert (got[b] == 0).all()
 
 
 def test_empty_and_single_key(fk):
