@@ -166,35 +166,100 @@ __device__ __forceinline__ void band_pair(uint32_t wd, const QScale &s, uint32_t
     e += lb ? 1.0f : (zb ? __fdividef(fabsf(fabsf(d.y) - cb), cb) : 0.0f);
 }
 
-// Band counters of one stream at one scale (band_pair over every stored
-// element); the error terms are summed in fp32 over a thread's 16 elements,
-// then in fp64.  chunk_shift is log2 of the chunks per row when that is a
-// power of two, else -1.  One 64-bit atomic per counter and block.
+// Band counters of one stream at one scale, through a table.  An element's
+// error term and its clip and flush tests depend only on its magnitude bits
+// t = bits & 0x7FFF (the quotient and the e4m3 code are sign-symmetric), so
+// each CTA first evaluates band_pair once per t into a table of 32,768 fp32
+// terms in shared memory, and the stream reads each element's term from it
+// (the same value, added in the same order as band_pair over the element's
+// word).  Both tests are monotone in t, the quotient and the nearest-even
+// conversion being non-decreasing in |x|: an element is flushed iff
+// 0 < t <= t_flush and clipped iff t_clip <= t < 0x7F80, with the two bounds
+// taken from the table's own entries.  The counts are then four comparisons
+// per element: not finite (t >= 0x7F80), zero, t >= t_clip, t <= t_flush.
+// The error terms are summed in fp32 over a thread's 16 elements, then in
+// fp64.  chunk_shift is log2 of the chunks per row when that is a power of
+// two, else -1.  One 64-bit atomic per counter and block.
+constexpr int kBandThreads = 1024;
+constexpr int kBandTab = 1 << 15;
+constexpr int kBandSmem = kBandTab * static_cast<int>(sizeof(float));
+
 template <bool kPow2>
-__global__ void __launch_bounds__(kStoreThreads)
+__global__ void __launch_bounds__(kBandThreads, 1)
 kv_band_kernel(const uint16_t *__restrict__ x, int64_t stride, const int64_t *__restrict__ slots,
                int64_t num_tokens, int32_t row_elems, int32_t chunk_shift, const QScale s,
                fp8kv_band_counts *out) {
-    __shared__ unsigned long long red_n[4][kStoreThreads / 32];
-    __shared__ double red_e[kStoreThreads / 32];
+    extern __shared__ float tab[];   // [kBandTab] error term of magnitude bits t
+    __shared__ unsigned long long red_n[4][kBandThreads / 32];
+    __shared__ double red_e[kBandThreads / 32];
+    __shared__ uint32_t t_flush, t_clip;
+    if (threadIdx.x == 0) {
+        t_flush = 0u;        // no flushed magnitude: only t = 0 is <= t_flush
+        t_clip = 0x7F80u;    // no clipped magnitude: only non-finite t are >= t_clip
+    }
+    __syncthreads();
+    for (uint32_t t = threadIdx.x; t < static_cast<uint32_t>(kBandTab); t += blockDim.x) {
+        uint32_t fin = 0, nz = 0, clip = 0, flush = 0;
+        float e = 0.0f;
+        band_pair<kPow2>(t, s, fin, nz, clip, flush, e);   // (t, +0): the +0 adds nothing
+        tab[t] = e;
+        if (flush) atomicMax(&t_flush, t);
+        if (clip) atomicMin(&t_clip, t);
+    }
+    __syncthreads();
+    const uint32_t tf = t_flush, tc = t_clip;
+
     const int32_t chunks = row_elems / kChunk;
     const int64_t total = num_tokens * chunks;
-    uint32_t c_fin = 0, c_nz = 0, c_clip = 0, c_flush = 0;   // this thread's counts
+    const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    uint32_t c_all = 0, c_inf = 0, c_zero = 0, c_hi = 0, c_lo = 0;   // this thread's counts
     double err = 0.0;
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t t = chunk_shift >= 0 ? (i >> chunk_shift) : i / chunks;
-        const int32_t c = static_cast<int32_t>(i - t * chunks);
-        if (slots && __ldg(slots + t) < 0) continue;
-        const uint4 *p = reinterpret_cast<const uint4 *>(x + t * stride + c * kChunk);
-        const uint4 lo = __ldcs(p), hi = __ldcs(p + 1);
-        const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-        float e16 = 0.0f;
+    // two chunks per iteration, both loaded before either is counted
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += 2 * step) {
+        uint4 v[2][2];
+        bool use[2];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) band_pair<kPow2>(w[k], s, c_fin, c_nz, c_clip, c_flush, e16);
-        err += static_cast<double>(e16);
+        for (int u = 0; u < 2; ++u) {
+            const int64_t ci = i + u * step;
+            use[u] = ci < total;
+            if (!use[u]) continue;
+            const int64_t t = chunk_shift >= 0 ? (ci >> chunk_shift) : ci / chunks;
+            const int32_t c = static_cast<int32_t>(ci - t * chunks);
+            if (slots && __ldg(slots + t) < 0) {
+                use[u] = false;
+                continue;
+            }
+            const uint4 *p = reinterpret_cast<const uint4 *>(x + t * stride + c * kChunk);
+            v[u][0] = __ldcs(p);
+            v[u][1] = __ldcs(p + 1);
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            if (!use[u]) continue;
+            const uint32_t w[8] = {v[u][0].x, v[u][0].y, v[u][0].z, v[u][0].w,
+                                   v[u][1].x, v[u][1].y, v[u][1].z, v[u][1].w};
+            float e16 = 0.0f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t t = (w[k] >> (16 * h)) & 0x7FFFu;
+                    e16 += tab[t];
+                    c_inf += t >= 0x7F80u ? 1u : 0u;
+                    c_zero += t == 0u ? 1u : 0u;
+                    c_hi += t >= tc ? 1u : 0u;
+                    c_lo += t <= tf ? 1u : 0u;
+                }
+            }
+            c_all += 16u;
+            err += static_cast<double>(e16);
+        }
     }
-    unsigned long long n_fin = c_fin, n_nz = c_nz, n_clip = c_clip, n_flush = c_flush;
+    // finite, non-zero, clipped (finite and t >= t_clip), flushed (non-zero
+    // and t <= t_flush)
+    unsigned long long n_fin = c_all - c_inf, n_nz = c_all - c_inf - c_zero, n_clip = c_hi - c_inf,
+                       n_flush = c_lo - c_zero;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -215,7 +280,7 @@ kv_band_kernel(const uint16_t *__restrict__ x, int64_t stride, const int64_t *__
     if (threadIdx.x == 0) {
         unsigned long long a[4] = {0, 0, 0, 0};
         double e = 0.0;
-        for (int w2 = 0; w2 < kStoreThreads / 32; ++w2) {
+        for (int w2 = 0; w2 < kBandThreads / 32; ++w2) {
 #pragma unroll
             for (int f = 0; f < 4; ++f) a[f] += red_n[f][w2];
             e += red_e[w2];
@@ -384,10 +449,18 @@ extern "C" fp8kv_status kv_band_counts(const fp8kv_bf16 *x, int64_t tok_stride,
     if ((chunks & (chunks - 1)) == 0)
         for (chunk_shift = 0; (1 << chunk_shift) < chunks; ++chunk_shift) {
         }
-    const int grid = grid_for(num_tokens * chunks, sms);
+    // one CTA per SM (the table fills most of its shared memory), fewer for
+    // small inputs
+    int64_t blocks = (num_tokens * chunks + kBandThreads - 1) / kBandThreads;
+    if (blocks > sms) blocks = sms;
+    const int grid = static_cast<int>(blocks);
     const QScale qs = make_qscale(scale);
     auto kernel = qs.pow2 ? kv_band_kernel<true> : kv_band_kernel<false>;
-    kernel<<<grid, kStoreThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+    static std::atomic<uint64_t> attrs_set[2];
+    if (!func_attrs_once(reinterpret_cast<const void *>(kernel), &attrs_set[qs.pow2 ? 1 : 0],
+                         kBandSmem, true))
+        return FP8KV_ERR_LAUNCH;
+    kernel<<<grid, kBandThreads, kBandSmem, static_cast<cudaStream_t>(stream)>>>(
         x, tok_stride, slot_mapping, num_tokens, row_elems, chunk_shift, qs, counts);
     if (cudaGetLastError() != cudaSuccess) return FP8KV_ERR_LAUNCH;
     return FP8KV_OK;
