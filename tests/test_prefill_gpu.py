@@ -222,12 +222,13 @@ def test_many_sequences_one_cta_per_item(fk):
     run_case(fk, q_lens, k_lens=k_lens, Hq=4, Hkv=1, E=128, seed=12, rows=rows)
 
 
-def _full_group(fk, which):
+def _full_group(fk, which, scales=(1.0, 1.0, 1.0)):
     spec = workloads.PREFILL_16K
     inp = workloads.make_prefill(spec, device=DEV, seed=0)
     kv = inp["kv"]
+    sq, sk, sv = scales
     cache = fk.KVCache.empty(kv.num_blocks, kv.block_size, spec.Hkv, spec.D, device=DEV)
-    fk.kv_store_e4m3(cache, kv.k, kv.v, kv.slot_mapping, 1.0, 1.0)
+    fk.kv_store_e4m3(cache, kv.k, kv.v, kv.slot_mapping, sk, sv)
     half = spec.n_seqs // 2
     lo, hi = (0, half) if which == 0 else (half, spec.n_seqs)
     window = spec.windows[which]
@@ -237,7 +238,7 @@ def _full_group(fk, which):
     rel_g = inp["rel"][cu[lo]:cu[hi]]
     out = fk.attn_fp8_varlen_prefill(cache, q_g, cu_g, kv.seq_lens[lo:hi].contiguous(),
                                      kv.block_table[lo:hi].contiguous(), max(inp["q_lens"][lo:hi]),
-                                     1.0, 1.0, 1.0, rel_bias=rel_g, window=window)
+                                     sq, sk, sv, rel_bias=rel_g, window=window)
     torch.cuda.synchronize()
     assert fk.device_error() == 0
     # a third of the SMs: each CTA takes about three times the items
@@ -245,7 +246,7 @@ def _full_group(fk, which):
         fk.set_prefill_max_ctas(50)
         out2 = fk.attn_fp8_varlen_prefill(cache, q_g, cu_g, kv.seq_lens[lo:hi].contiguous(),
                                           kv.block_table[lo:hi].contiguous(),
-                                          max(inp["q_lens"][lo:hi]), 1.0, 1.0, 1.0,
+                                          max(inp["q_lens"][lo:hi]), sq, sk, sv,
                                           rel_bias=rel_g, window=window)
         torch.cuda.synchronize()
     finally:
@@ -273,28 +274,37 @@ def _full_group(fk, which):
                             slot_mapping=kv.slot_mapping, num_blocks=kv.num_blocks,
                             block_size=kv.block_size)
     g_inp["kv"] = sub
-    ref = oracle_prefill_rows(g_inp, rows, 1.0, 1.0, 1.0, window=window, rel=rel_g)
+    ref = oracle_prefill_rows(g_inp, rows, sq, sk, sv, window=window, rel=rel_g)
     return assert_close(np.stack([got[t, h] for t, h in rows]), ref, spec.name)
 
 
-def test_full_prefill_causal_group(fk):
-    _full_group(fk, 0)
+# unit scales, and q / k scales that are not powers of two (the divided
+# quantization) with a V scale of 3
+FULL_SCALES = [(1.0, 1.0, 1.0), (0.7, 0.45, 3.0)]
 
 
-def test_full_prefill_window_group(fk):
-    _full_group(fk, 1)
+@pytest.mark.parametrize("scales", FULL_SCALES)
+def test_full_prefill_causal_group(fk, scales):
+    _full_group(fk, 0, scales)
 
 
-def test_full_chunk_over_64k_prefix(fk):
+@pytest.mark.parametrize("scales", FULL_SCALES)
+def test_full_prefill_window_group(fk, scales):
+    _full_group(fk, 1, scales)
+
+
+@pytest.mark.parametrize("scales", FULL_SCALES)
+def test_full_chunk_over_64k_prefix(fk, scales):
     """One 4,096-query chunk over 65,536 keys (a 61,440-key cached prefix), the
     bench's chunked-prefill workload, on sampled rows."""
     spec = workloads.PREFILL_CHUNK_64K
     inp = workloads.make_prefill(spec, device=DEV, seed=0)
     kv = inp["kv"]
+    sq, sk, sv = scales
     cache = fk.KVCache.empty(kv.num_blocks, kv.block_size, spec.Hkv, spec.D, device=DEV)
-    fk.kv_store_e4m3(cache, kv.k, kv.v, kv.slot_mapping, 1.0, 1.0)
+    fk.kv_store_e4m3(cache, kv.k, kv.v, kv.slot_mapping, sk, sv)
     out = fk.attn_fp8_varlen_prefill(cache, inp["q"], inp["cu_seqlens_q"], kv.seq_lens,
-                                     kv.block_table, max(inp["q_lens"]), 1.0, 1.0, 1.0,
+                                     kv.block_table, max(inp["q_lens"]), sq, sk, sv,
                                      rel_bias=inp["rel"], window=0)
     torch.cuda.synchronize()
     assert fk.device_error() == 0
@@ -311,7 +321,7 @@ def test_full_chunk_over_64k_prefix(fk):
                                    block_size=kv.block_size)
     host["q"] = inp["q"].cpu()
     host["rel"] = inp["rel"].cpu()
-    ref = oracle_prefill_rows(host, rows, 1.0, 1.0, 1.0, window=0, rel=host["rel"])
+    ref = oracle_prefill_rows(host, rows, sq, sk, sv, window=0, rel=host["rel"])
     assert_close(np.stack([got[t, h] for t, h in rows]), ref, spec.name)
 
 
