@@ -303,7 +303,9 @@ def e2e_decode(run, steps, warmup, world):
     copy of the step's inputs (q, new K, new V, lengths, packed in one pinned
     staging buffer at 256-byte offsets) to the device, the call (a DecodeStep
     bound to the staging buffers' device copies, as a decode loop keeps them),
-    and a read back of out."""
+    a read back of out and a host sync.  Timed twice: issued one by one
+    ("eager"), and as one CUDA graph of the three (DecodeStep.cuda_graph);
+    returns ms per step of each, and the bytes copied each way."""
     parts = {"q": run.q, "k_new": run.k_new, "v_new": run.v_new, "seq_lens": run.kv.seq_lens}
     offs, total = {}, 0
     for k, t in parts.items():
@@ -325,21 +327,31 @@ def e2e_decode(run, steps, warmup, world):
                              workspace=run.ws, k_new=dev["k_new"], v_new=dev["v_new"],
                              amax_k=run.amax_views[0], amax_v=run.amax_views[1])
 
-    def one():
+    def copy_in():
         dev_buf.copy_(host, non_blocking=True)
-        o = step.run()
-        out_h.copy_(o, non_blocking=True)
-    for _ in range(warmup):
-        one()
-    torch.cuda.synchronize()
-    barrier(world)
-    t0 = time.perf_counter()
-    for _ in range(steps):
-        one()
-        torch.cuda.current_stream().synchronize()   # the result is on the host each step
-    ms = (time.perf_counter() - t0) * 1e3 / steps
-    ms = max_over_ranks(ms, world)
-    return ms, h2d, d2h
+
+    def copy_out():
+        out_h.copy_(run.out, non_blocking=True)
+
+    def eager():
+        copy_in()
+        step.run()
+        copy_out()
+    # the same step as one CUDA graph (copy in, store + decode, read back)
+    graph = step.cuda_graph(pre=copy_in, post=copy_out)
+    res = {}
+    for name, one in (("eager", eager), ("graph", graph.replay)):
+        for _ in range(warmup):
+            one()
+        torch.cuda.synchronize()
+        barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            one()
+            torch.cuda.current_stream().synchronize()   # the result is on the host each step
+        ms = (time.perf_counter() - t0) * 1e3 / steps
+        res[name] = max_over_ranks(ms, world)
+    return res, h2d, d2h
 
 
 # ---------------------------------------------------------------------------
@@ -871,7 +883,8 @@ def main():
     clocks = clk.summary()
     value = run.step_bytes * world / ms / 1e6          # GB/s over all ranks
     achieved = run.decode_bytes / dms / 1e6
-    e2e_ms, h2d, d2h = e2e_decode(run, max(3, args.steps // 2), args.warmup, world)
+    e2e, h2d, d2h = e2e_decode(run, max(3, args.steps // 2), args.warmup, world)
+    e2e_ms = e2e["graph"]
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
@@ -884,7 +897,13 @@ def main():
                          "peak_source": pk["source"]},
             "e2e": {"value": run.step_bytes * world / e2e_ms / 1e6, "unit": "GB/s",
                     "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
+                    "d2h_bytes_per_step": d2h,
+                    "launch": "DecodeStep.cuda_graph: one graph replay per step (copy in, "
+                              "store + decode, read back), then a host sync",
+                    "eager": {"value": run.step_bytes * world / e2e["eager"] / 1e6,
+                              "ms_per_step": e2e["eager"],
+                              "launch": "the copy, DecodeStep.run and the read back issued "
+                                        "one by one"}},
             "gpu_launches": run.launches_per_step * args.steps,
             "separate_calls": {"ms_per_step": sep_ms, "value": run.step_bytes * world / sep_ms / 1e6,
                                "launches_per_step": 4},

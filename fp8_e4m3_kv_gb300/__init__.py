@@ -383,6 +383,25 @@ class DecodeStep:
         _check(self._fn(*self._args, _stream(stream)), self._name)
         return self.out
 
+    def cuda_graph(self, pre=None, post=None) -> "torch.cuda.CUDAGraph":
+        """Capture one step into a CUDA graph: ``pre()`` (for example the copy
+        of the step's inputs from pinned host memory into the bound buffers),
+        ``run()``, then ``post()`` (for example the copy of out to the host).
+        ``graph.replay()`` then runs the whole step as one launch on the
+        current stream, reading the buffers' contents at replay time.  The
+        step runs once before the capture (on the current stream, which is
+        then synchronized), so the launch set-up is done outside it."""
+        self.run()
+        torch.cuda.current_stream().synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            if pre is not None:
+                pre()
+            self.run()
+            if post is not None:
+                post()
+        return graph
+
 
 def kv_store_e4m3_per_token(cache: KVCache, k: torch.Tensor, v: torch.Tensor,
                             slot_mapping: torch.Tensor, k_scales: torch.Tensor,

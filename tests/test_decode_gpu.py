@@ -300,6 +300,68 @@ def test_bound_decode_step_matches_the_calls(fk):
     assert torch.equal(got, ref)
 
 
+def test_decode_step_cuda_graph_replays_the_step(fk):
+    """DecodeStep.cuda_graph: a graph of (copy of q, k_new, v_new from pinned
+    host memory, the fused store + decode, copy of out to pinned host memory),
+    replayed after new inputs are written to the host buffers, gives the
+    one-shot fused call's output bit for bit; sampled rows match the oracle."""
+    spec = workloads.DecodeSpec("graph", B=40, Hq=32, Hkv=4, D=128, block_size=16,
+                                ctx_lo=300, ctx_hi=12000, rel_extent=1024)
+    inp = workloads.make_decode(spec, device="cpu", seed=51)
+    kv = inp["kv"]
+    kd = to_device(kv, DEV)
+    cache = fk.KVCache.empty(kv.num_blocks, 16, 4, 128, device=DEV)
+    fk.kv_store_e4m3(cache, kd.k, kd.v, kd.slot_mapping, 1.0, 1.0)
+    rel = inp["rel"].to(DEV)
+    B, Hq, Hkv, D = 40, 32, 4, 128
+    q_h = torch.empty((B, Hq, D), dtype=torch.bfloat16).pin_memory()
+    kn_h = torch.empty((B, Hkv, D), dtype=torch.bfloat16).pin_memory()
+    vn_h = torch.empty_like(kn_h).pin_memory()
+    out_h = torch.empty((B, Hq, D), dtype=torch.bfloat16).pin_memory()
+    q, k_new, v_new = q_h.to(DEV), kn_h.to(DEV), vn_h.to(DEV)
+    step = fk.DecodeStep(cache, q, kd.block_table, kd.seq_lens, 1.0, 1.0, 1.0, rel_bias=rel,
+                         k_new=k_new, v_new=v_new)
+
+    def copy_in():
+        q.copy_(q_h, non_blocking=True)
+        k_new.copy_(kn_h, non_blocking=True)
+        v_new.copy_(vn_h, non_blocking=True)
+
+    def copy_out():
+        out_h.copy_(step.out, non_blocking=True)
+    graph = step.cuda_graph(pre=copy_in, post=copy_out)
+    for seed in (1, 2):   # new host inputs before each replay
+        g = torch.Generator().manual_seed(seed)
+        q_h.copy_(torch.randn((B, Hq, D), generator=g).to(torch.bfloat16))
+        kn_h.copy_(torch.randn((B, Hkv, D), generator=g).to(torch.bfloat16))
+        vn_h.copy_(torch.randn((B, Hkv, D), generator=g).to(torch.bfloat16))
+        graph.replay()
+        torch.cuda.current_stream().synchronize()
+        assert fk.device_error() == 0
+        got = out_h.clone()
+        ref = fk.paged_attn_fp8_decode_store(cache, q_h.to(DEV), kn_h.to(DEV), vn_h.to(DEV),
+                                             kd.block_table, kd.seq_lens, 1.0, 1.0, 1.0,
+                                             rel_bias=rel)
+        torch.cuda.synchronize()
+        assert torch.equal(got, ref.cpu())
+    # the last replay's step against the oracle: the cache holds the new
+    # tokens at each sequence's last position
+    kv_last = workloads.PagedKV(k=kv.k.clone(), v=kv.v.clone(), seq_lens=kv.seq_lens,
+                                tok_start=kv.tok_start, block_table=kv.block_table,
+                                slot_mapping=kv.slot_mapping, num_blocks=kv.num_blocks,
+                                block_size=kv.block_size)
+    for b in range(B):
+        last = int(kv.tok_start[b]) + int(kv.seq_lens[b]) - 1
+        kv_last.k[last] = kn_h[b]
+        kv_last.v[last] = vn_h[b]
+    host = dict(inp)
+    host["kv"] = kv_last
+    host["q"] = q_h.clone()
+    rows = [(b, h) for b in (0, 17, 39) for h in (0, 9, 31)]
+    ref_rows = oracle_decode_rows(host, rows, 1.0, 1.0, 1.0, rel=inp["rel"])
+    assert_close(np.stack([got[b, h].float().numpy() for b, h in rows]), ref_rows, "graph")
+
+
 def test_bounded_wait_runs_out_and_the_next_call_is_clean(fk):
     """The failure path of a bounded wait, made to happen: the test hook makes
     the decode producer skip its first tile's copy (nothing else changes), so
