@@ -126,6 +126,10 @@ struct DecodeParams {
     int32_t rel_extent;
     int32_t window;
     int32_t split_tiles;
+    // the first fine_splits splits of a sequence (in key order) take
+    // fine_tiles tiles each, the rest split_tiles (fine_splits 0: all equal)
+    int32_t fine_splits;
+    int32_t fine_tiles;
     int32_t num_slots;      // partial slots per (sequence, head) = splits
     QScale q_scale;
     float score_log2;       // softmax_scale * q_scale * k_scale * log2(e)
@@ -263,9 +267,18 @@ __device__ __forceinline__ ItemGeom item_geom(const DecodeParams &p, int b, int 
     ItemGeom g;
     g.len = p.seq_lens[b];
     g.lo = (p.window > 0 && g.len > p.window) ? g.len - p.window : 0;
-    g.t0 = g.lo / kKeys + static_cast<int64_t>(split) * p.split_tiles;
+    int64_t off, n;
+    if (split < p.fine_splits) {
+        off = static_cast<int64_t>(split) * p.fine_tiles;
+        n = p.fine_tiles;
+    } else {
+        off = static_cast<int64_t>(p.fine_splits) * p.fine_tiles +
+              static_cast<int64_t>(split - p.fine_splits) * p.split_tiles;
+        n = p.split_tiles;
+    }
+    g.t0 = g.lo / kKeys + off;
     g.t_end = (g.len + kKeys - 1) / kKeys;
-    g.ntiles = static_cast<int>(g.t_end - g.t0 < p.split_tiles ? g.t_end - g.t0 : p.split_tiles);
+    g.ntiles = static_cast<int>(g.t_end - g.t0 < n ? g.t_end - g.t0 : n);
     return g;
 }
 
@@ -1080,6 +1093,8 @@ decode_merge_sliced_kernel(const float *__restrict__ part_o, const float *__rest
 struct SplitPlan {
     int num_splits;
     int split_tiles;
+    int fine_splits;   // leading splits of fine_tiles tiles each
+    int fine_tiles;
 };
 
 // Split plan: ~16 work items per resident CTA of the persistent launch (the
@@ -1112,10 +1127,22 @@ bool plan_splits(int32_t num_seqs, int32_t num_kv_heads, int32_t head_dim,
         const int64_t min_st = (2048 + keys - 1) / keys;
         if (st < min_st) st = min_st;
     }
-    const int64_t S = (tiles + st - 1) / st;
+    int64_t S = (tiles + st - 1) / st;
+    // Automatic plans with several splits: the first split of each sequence
+    // (in key order) is cut into four.  Items go out last splits first, so
+    // these are the launch's last items, and the tail ends in quarter-size
+    // pieces.
+    int64_t F = 0, ft = 0;
+    if (split_tokens <= 0 && S >= 2 && st % 4 == 0) {
+        F = 4;
+        ft = st / 4;
+        S += F - 1;
+    }
     if (S > 65535 || st > (1 << 24)) return false;
     plan->num_splits = static_cast<int>(S);
     plan->split_tiles = static_cast<int>(st);
+    plan->fine_splits = static_cast<int>(F);
+    plan->fine_tiles = static_cast<int>(ft);
     return true;
 }
 
@@ -1268,6 +1295,8 @@ fp8kv_status decode_impl(const fp8kv_cache *cache, const fp8kv_bf16 *q, int32_t 
     p.rel_extent = rel_bias ? rel_extent : 0;
     p.window = window;
     p.split_tiles = plan.split_tiles;
+    p.fine_splits = plan.fine_splits;
+    p.fine_tiles = plan.fine_tiles;
     p.num_slots = slots;
     p.q_scale = make_qscale(q_scale);
     p.score_log2 = static_cast<float>(static_cast<double>(softmax_scale) * q_scale * k_scale *
