@@ -1097,9 +1097,10 @@ struct SplitPlan {
     int fine_tiles;
 };
 
-// Split plan: ~16 work items per resident CTA of the persistent launch (the
+// Split plan: ~8 work items per resident CTA of the persistent launch (the
 // counter hands them out, so short last items even out the tail), at least
-// 2048 keys per split, all splits of equal length in tiles.
+// 2048 keys per split and a whole number of quarter splits; the first split
+// of each sequence is then cut into quarters (below).
 bool plan_splits(int32_t num_seqs, int32_t num_kv_heads, int32_t head_dim,
                  int32_t max_blocks_per_seq, int32_t block_size, int32_t window,
                  int32_t split_tokens, int num_sms, SplitPlan *plan) {
@@ -1117,7 +1118,7 @@ bool plan_splits(int32_t num_seqs, int32_t num_kv_heads, int32_t head_dim,
         st = split_tokens / keys;
     } else {
         const int64_t ctas_per_sm = head_dim == 128 ? DecCfg<128>::kCtasPerSm : 1;
-        const int64_t target = static_cast<int64_t>(num_sms) * ctas_per_sm * 16;
+        const int64_t target = static_cast<int64_t>(num_sms) * ctas_per_sm * 8;
         int64_t pairs = static_cast<int64_t>(num_seqs) * num_kv_heads;
         if (pairs < 1) pairs = 1;
         const int64_t want = (target + pairs - 1) / pairs;
@@ -1126,6 +1127,7 @@ bool plan_splits(int32_t num_seqs, int32_t num_kv_heads, int32_t head_dim,
         // (written and merged) and a Q quantization
         const int64_t min_st = (2048 + keys - 1) / keys;
         if (st < min_st) st = min_st;
+        st = (st + 3) / 4 * 4;   // whole quarters for the cut below
     }
     int64_t S = (tiles + st - 1) / st;
     // Automatic plans with several splits: the first split of each sequence
