@@ -138,6 +138,38 @@ def test_empty_and_short_sequences_among_long_ones_through_the_work_counter(fk, 
         assert (got[b] == 0).all()
 
 
+@pytest.mark.parametrize("D,Hq,Hkv,offset", [(256, 24, 4, 0), (256, 24, 4, 1), (128, 32, 4, 1)])
+def test_merge_of_many_rows_and_an_out_not_8_byte_aligned(fk, D, Hq, Hkv, offset):
+    """Enough (sequence, head) rows that the merge runs one warp per row (at
+    head_dim 256 too), several splits per row, and out at an element offset
+    of 0 or 1 (2-byte aligned only): sampled rows match the oracle and the
+    padding element before out stays untouched."""
+    rng = np.random.default_rng(7 + D + offset)
+    B = 16
+    lens = [int(x) for x in rng.integers(300, 6000, B)]
+    lens[3] = 0
+    spec = workloads.DecodeSpec("case", B=B, Hq=Hq, Hkv=Hkv, D=D, block_size=16, ctx_lo=1,
+                                ctx_hi=1, rel_extent=128)
+    inp = workloads.make_decode(spec, device="cpu", seed=31, lens=lens)
+    kd = to_device(inp["kv"], DEV)
+    cache = fk.KVCache.empty(kd.num_blocks, 16, Hkv, D, device=DEV)
+    fk.kv_store_e4m3(cache, kd.k, kd.v, kd.slot_mapping, 1.0, 1.0)
+    flat = torch.full((B * Hq * D + 8,), float("nan"), dtype=torch.bfloat16, device=DEV)
+    out = flat[offset:offset + B * Hq * D].view(B, Hq, D)
+    fk.paged_attn_fp8_decode(cache, inp["q"].to(DEV), kd.block_table, kd.seq_lens, 1.0, 1.0,
+                             1.0, rel_bias=inp["rel"].to(DEV), out=out, split_tokens=1024)
+    torch.cuda.synchronize()
+    assert fk.device_error() == 0
+    got = out.float().cpu().numpy()
+    assert not np.isnan(got).any()
+    assert (got[3] == 0).all()
+    if offset:
+        assert torch.isnan(flat[:offset].float()).all()
+    rows = [(b, h) for b in (0, 5, 15) for h in (0, Hq // 2, Hq - 1)]
+    ref = oracle_decode_rows(inp, rows, 1.0, 1.0, 1.0, rel=inp["rel"])
+    assert_close(np.stack([got[b, h] for b, h in rows]), ref, "merge")
+
+
 def test_empty_and_single_key(fk):
     """len 0 gives zeros; len 1 gives v_scale * v8 of the only key (exact)."""
     err, got = run_case(fk, [0, 1, 5], 4, 1, 128, 16, scales=(1.0, 1.0, 2.0), seed=12,
