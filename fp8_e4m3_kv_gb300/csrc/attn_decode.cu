@@ -380,6 +380,9 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
+    // the merge launch that follows may be scheduled now: it waits for this
+    // whole grid's completion (and its writes) before reading any partial
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == C::kProducerWarp) {
         // ------------------------------------------------------------ producer
@@ -948,6 +951,9 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
 decode_merge_kernel(const float *__restrict__ part_o, const float *__restrict__ part_ml,
                     uint16_t *__restrict__ out, int32_t Hq, int32_t S, float v_scale) {
     constexpr int kV = D / 128;   // float4 per lane
+    // launched as a programmatic dependent of the decode grid: its partials
+    // are complete and visible once this returns
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     __shared__ float red_m[kMergeWarps];
     __shared__ float red_l[kMergeWarps];
     __shared__ __align__(16) float red_acc[kMergeWarps][D];
@@ -1018,6 +1024,7 @@ template <int D>
 __global__ void __launch_bounds__(kMergeWarps * 32)
 decode_merge_sliced_kernel(const float *__restrict__ part_o, const float *__restrict__ part_ml,
                     uint16_t *__restrict__ out, int32_t Hq, int32_t S, float v_scale) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // as in decode_merge_kernel
     __shared__ float red_m[kMergeWarps];
     __shared__ __align__(16) float4 red_acc[kMergeWarps * 32];
     __shared__ float red_l[kMergeWarps * 32];
@@ -1345,19 +1352,26 @@ fp8kv_status decode_impl(const fp8kv_cache *cache, const fp8kv_bf16 *q, int32_t 
     int zs = 1;
     while (zs < D / 32 && static_cast<int64_t>(num_q_heads) * num_seqs * zs < 2ll * sms) zs *= 2;
     const dim3 mgrid(num_q_heads, num_seqs, zs);
-    if (zs == 1 && D == 128)
-        decode_merge_kernel<128><<<mgrid, kMergeWarps * 32, 0, s>>>(p.part_o, p.part_ml, out,
-                                                                   num_q_heads, slots, v_scale);
-    else if (zs == 1)
-        decode_merge_kernel<256><<<mgrid, kMergeWarps * 32, 0, s>>>(p.part_o, p.part_ml, out,
-                                                                   num_q_heads, slots, v_scale);
-    else if (D == 128)
-        decode_merge_sliced_kernel<128><<<mgrid, kMergeWarps * 32, 0, s>>>(
-            p.part_o, p.part_ml, out, num_q_heads, slots, v_scale);
-    else
-        decode_merge_sliced_kernel<256><<<mgrid, kMergeWarps * 32, 0, s>>>(
-            p.part_o, p.part_ml, out, num_q_heads, slots, v_scale);
-    if (cudaGetLastError() != cudaSuccess) return FP8KV_ERR_LAUNCH;
+    // a programmatic dependent launch: the merge's CTAs may be scheduled while
+    // the decode grid drains, and wait (griddepcontrol.wait) for its end
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = mgrid;
+    cfg.blockDim = dim3(kMergeWarps * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    auto merge = zs == 1 ? (D == 128 ? decode_merge_kernel<128> : decode_merge_kernel<256>)
+                         : (D == 128 ? decode_merge_sliced_kernel<128> : decode_merge_sliced_kernel<256>);
+    if (cudaLaunchKernelEx(&cfg, merge, static_cast<const float *>(p.part_o),
+                           static_cast<const float *>(p.part_ml), out, num_q_heads, slots,
+                           v_scale) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8KV_ERR_LAUNCH;
+    }
     return FP8KV_OK;
 }
 }  // namespace
