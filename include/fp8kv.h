@@ -131,7 +131,9 @@ fp8kv_status kv_store_e4m3(const fp8kv_cache *cache, const fp8kv_bf16 *k,
  *               stream before the launch).  Calls that overlap on the GPU
  *               must not share a workspace.
  * Launch: one persistent kernel of at most two CTAs per SM that take the
- * splits from that counter, then (with more than one split) a merge kernel.
+ * splits from that counter, then (with more than one split) a merge kernel,
+ * launched as a programmatic dependent of the first (it waits for the first
+ * grid's completion before reading the partials).
  */
 fp8kv_status paged_attn_fp8_decode(const fp8kv_cache *cache, const fp8kv_bf16 *q,
                                    int32_t num_q_heads, const int32_t *block_table,
