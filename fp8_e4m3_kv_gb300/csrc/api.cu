@@ -99,8 +99,8 @@ bool func_attrs_once(const void *func, std::atomic<uint64_t> *done, int smem_byt
     return true;
 }
 
-bool make_cache_map(CUtensorMap *map, const uint8_t *base, int64_t num_blocks, int block_size,
-                    int num_kv_heads, int head_dim) {
+// The driver's tensor-map encoder, looked up once.
+static PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
     std::call_once(g_encode_once, [] {
         void *fn = nullptr;
         cudaDriverEntryPointQueryResult q;
@@ -111,7 +111,27 @@ bool make_cache_map(CUtensorMap *map, const uint8_t *base, int64_t num_blocks, i
         else
             cudaGetLastError();
     });
-    if (!g_encode_tiled) return false;
+    return g_encode_tiled;
+}
+
+bool make_rows_map(CUtensorMap *map, const void *base, int64_t rows, int heads, int head_dim) {
+    if (!encode_tiled() || rows < 1 || rows > (1ll << 31) - 1 || heads < 1 || head_dim < 64)
+        return false;
+    // x[row][head][d] as (d, head, row); one box is 32 rows of one head's
+    // first or second 64 values (128 bytes each)
+    const cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)heads, (cuuint64_t)rows};
+    const cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)heads * head_dim * 2};
+    const cuuint32_t box[3] = {64u, 1u, 32u};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    return g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_cache_map(CUtensorMap *map, const uint8_t *base, int64_t num_blocks, int block_size,
+                    int num_kv_heads, int head_dim) {
+    if (!encode_tiled()) return false;
     // The map depends only on the arguments: the last few are kept per host
     // thread, so a decode loop over the same cache encodes it once.
     struct Entry {

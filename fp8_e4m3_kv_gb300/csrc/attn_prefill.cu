@@ -103,6 +103,9 @@ struct PrefillParams {
     const float *k_tok_scale;
     const float *v_tok_scale;
     int32_t num_kv_heads;
+    // head_dim-128 kernel: each softmax warp copies the next item's Q rows
+    // with the tensor map qmap (only when its 32 rows are all the item's)
+    int32_t q_tma;
 };
 
 __device__ __forceinline__ void mbar_drain_p(uint64_t *bar, uint32_t parity, uint32_t *err) {
@@ -725,7 +728,7 @@ __device__ __forceinline__ bool pre2_next(const PrefillParams &p, const Pre2Seqs
 template <bool kPT>
 __global__ void __launch_bounds__(kPre2Threads, 1)
 prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                const PrefillParams p) {
+                const __grid_constant__ CUtensorMap qmap, const PrefillParams p) {
     using C = Pre2Cfg;
     constexpr int D = 128;
     extern __shared__ uint8_t smem_raw[];
@@ -743,6 +746,8 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     auto o_done = [&](int k, int hh) { return bars + 16 * k + 10 + hh; };// PV of P half done
     auto q_full = [&](int k) { return bars + 16 * k + 12; };             // Q8 of next item
     auto mma_done = [&](int k) { return bars + 16 * k + 13; };
+    // softmax warp w of pipeline k: its copy of the next item's Q rows landed
+    auto qbar = [&](int k, int w) { return bars + 36 + 4 * k + w; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc + 256);
     CtaFail *fail = reinterpret_cast<CtaFail *>(smem + C::kOffMisc + 260);
     // byte wq of lo_flag(k, hh): softmax warp wq of pipeline k wrote a second
@@ -797,6 +802,7 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
             }
             mbar_init(q_full(k), 4);
             mbar_init(mma_done(k), 1);
+            for (int w = 0; w < 4; ++w) mbar_init(qbar(k, w), 1);
         }
         fail->abort = 0;
         fence_mbar_init();
@@ -805,6 +811,7 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     if ((warp == 8 || warp == 11) && lane == 0) {
         tma_prefetch_map(&kmap);
         tma_prefetch_map(&vmap);
+        if (p.q_tma) tma_prefetch_map(&qmap);
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -1085,6 +1092,10 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
             return true;
         };
 
+        // this warp's copy of the next item's Q rows into its staging rows
+        // (P_hi / P_lo rows 32 wq .. 32 wq + 31: the epilogue's layout)
+        bool q_pending = false;
+        int q_copies = 0;
         Pre2Sched sc;
         Pre2Item it;
         while (ok && pre2_next(p, tab, k, sc, it)) {
@@ -1109,14 +1120,30 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
                 uint8_t *q8 = smem + C::kOffQ + k * C::kQBytes;
                 const int row_in_pair = lane >> 4, col = lane & 15;   // 8 bf16 per lane
                 uint4 v[16];
+                if (!kPT && q_pending) {
+                    // copied during the previous item: all 32 rows are this
+                    // item's, in the staging rows (swizzled like the epilogue's)
+                    if (!warp_wait_p(qbar(k, wq), (q_copies - 1) & 1, fail, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    q_pending = false;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int row = 32 * wq + 2 * i + row_in_pair;
-                    v[i] = make_uint4(0, 0, 0, 0);
-                    if (row < it.n_rows)
-                        v[i] = __ldg(reinterpret_cast<const uint4 *>(
-                            p.q + (tok0 + row) * p.Hq * D + static_cast<int64_t>(it.h) * D +
-                            col * 8));
+                    for (int i = 0; i < 16; ++i) {
+                        const int row = 32 * wq + 2 * i + row_in_pair;
+                        v[i] = *reinterpret_cast<const uint4 *>(
+                            (col < 8 ? p_hi : p_lo) + row * 128 + (((col & 7) ^ (row & 7)) << 4));
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int row = 32 * wq + 2 * i + row_in_pair;
+                        v[i] = make_uint4(0, 0, 0, 0);
+                        if (row < it.n_rows)
+                            v[i] = __ldg(reinterpret_cast<const uint4 *>(
+                                p.q + (tok0 + row) * p.Hq * D + static_cast<int64_t>(it.h) * D +
+                                col * 8));
+                    }
                 }
                 // this row's bias is read on the diagonal key tiles: start it
                 // toward L2 now
@@ -1139,20 +1166,41 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
                 __syncwarp();
                 if (lane == 0) mbar_arrive(q_full(k));
             }
-            // the pipeline's next item, and its Q rows toward L2
+            // the pipeline's next item: its Q rows are copied into this
+            // warp's staging rows once the epilogue below is done with them
+            // (when all 32 are the item's), else started toward L2
+            int32_t nq_row = -1, nq_h = 0;
             {
                 Pre2Sched peek = sc;
                 Pre2Item nx;
-                if (pre2_next(p, tab, k, peek, nx) && r < nx.n_rows) {
-                    const uint16_t *nq =
-                        p.q + (static_cast<int64_t>(nx.q_first) + nx.qt * kTile + r) * p.Hq * D +
-                        static_cast<int64_t>(nx.h) * D;
-                    prefetch_l2(nq);
-                    prefetch_l2(nq + 64);
+                if (pre2_next(p, tab, k, peek, nx)) {
+                    if (!kPT && p.q_tma && 32 * wq + 32 <= nx.n_rows) {
+                        nq_row = nx.q_first + nx.qt * kTile + 32 * wq;
+                        nq_h = nx.h;
+                    } else if (r < nx.n_rows) {
+                        const uint16_t *nq =
+                            p.q + (static_cast<int64_t>(nx.q_first) + nx.qt * kTile + r) * p.Hq * D +
+                            static_cast<int64_t>(nx.h) * D;
+                        prefetch_l2(nq);
+                        prefetch_l2(nq + 64);
+                    }
                 }
             }
             // the previous item's output, while the QKs of this one run
             if (have_prev && !(ok = epilogue())) break;
+            if (!kPT && nq_row >= 0) {
+                // the staging rows' generic reads and writes come before the
+                // copy writes them
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(qbar(k, wq), 2 * 32 * 128);
+                    tma_load_3d(p_hi + 32 * wq * 128, &qmap, qbar(k, wq), 0, nq_h, nq_row);
+                    tma_load_3d(p_lo + 32 * wq * 128, &qmap, qbar(k, wq), 64, nq_h, nq_row);
+                }
+                ++q_copies;
+                q_pending = true;
+            }
 
             float m_used = -INFINITY;
             float2 lsum = make_float2(0.0f, 0.0f);   // two partial row sums
@@ -1386,6 +1434,11 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
             prev_l = lsum;
         }
         if (ok && have_prev) epilogue();
+        // a copy still in flight (the loop ended early) lands before the CTA ends
+        if (!kPT && q_pending) {
+            if (lane == 0) mbar_drain_p(qbar(k, wq), (q_copies - 1) & 1, p.err);
+            __syncwarp();
+        }
     }
 
     tc_fence_before_sync();
@@ -1417,8 +1470,8 @@ bool prefill2_registers_ok() {
 std::atomic<int> g_prefill_max_ctas{0};
 
 template <bool kPT>
-fp8kv_status launch_prefill2(const CUtensorMap &km, const CUtensorMap &vm, const PrefillParams &p,
-                             int num_seqs, int sms, cudaStream_t stream) {
+fp8kv_status launch_prefill2(const CUtensorMap &km, const CUtensorMap &vm, const CUtensorMap &qm,
+                             const PrefillParams &p, int num_seqs, int sms, cudaStream_t stream) {
     const int cap = g_prefill_max_ctas.load(std::memory_order_relaxed);
     if (cap > 0 && cap < sms) sms = cap;
     if (!prefill2_registers_ok<kPT>()) return FP8KV_ERR_UNSUPPORTED;
@@ -1431,7 +1484,7 @@ fp8kv_status launch_prefill2(const CUtensorMap &km, const CUtensorMap &vm, const
     const int64_t n_items = n_pairs * p.Hq * num_seqs;
     const dim3 grid = p.persist ? dim3(static_cast<unsigned>(n_items < sms ? n_items : sms))
                                 : dim3(static_cast<unsigned>(n_pairs), p.Hq, num_seqs);
-    prefill2_kernel<kPT><<<grid, kPre2Threads, Pre2Cfg::kSmemBytes, stream>>>(km, vm, p);
+    prefill2_kernel<kPT><<<grid, kPre2Threads, Pre2Cfg::kSmemBytes, stream>>>(km, vm, qm, p);
     if (cudaGetLastError() != cudaSuccess) return FP8KV_ERR_LAUNCH;
     return FP8KV_OK;
 }
@@ -1528,9 +1581,16 @@ fp8kv_status prefill_impl(const fp8kv_cache *cache, const fp8kv_bf16 *q, int32_t
     p.k_tok_scale = k_scales;
     p.v_tok_scale = v_scales;
     p.num_kv_heads = Hkv;
+    // Q rows by tensor map (head_dim-128 kernel without per-token tables):
+    // rows are bounded by num_seqs * max_seqlen_q, and a warp copies only
+    // rows of its item's own queries
+    CUtensorMap qm = km;
+    p.q_tma = !per_token && D == 128 &&
+              make_rows_map(&qm, q, static_cast<int64_t>(num_seqs) * max_seqlen_q, num_q_heads, D);
+    if (!p.q_tma) qm = km;   // unused
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (per_token) return launch_prefill2<true>(km, vm, p, num_seqs, sms, s);
-    return D == 128 ? launch_prefill2<false>(km, vm, p, num_seqs, sms, s)
+    if (per_token) return launch_prefill2<true>(km, vm, qm, p, num_seqs, sms, s);
+    return D == 128 ? launch_prefill2<false>(km, vm, qm, p, num_seqs, sms, s)
                     : launch_prefill<256>(km, vm, p, num_seqs, s);
 }
 }  // namespace

@@ -252,6 +252,16 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
+// 3-D tiled load into shared memory, completing on `bar` (tx bytes).
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int32_t c0, int32_t c1, int32_t c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // tcgen05: tensor memory and MMA
 // ---------------------------------------------------------------------------
@@ -490,6 +500,10 @@ bool scale_ok(float s);
 // rejects it.
 bool make_cache_map(CUtensorMap *map, const uint8_t *base, int64_t num_blocks, int block_size,
                     int num_kv_heads, int head_dim);
+// Tensor map over a bf16 array [rows][heads][head_dim] (rows a bound on the
+// rows that are read), box (64 values, 1 head, 32 rows) = 32 rows of 128
+// bytes, 128-byte swizzle.  Returns false when the driver rejects it.
+bool make_rows_map(CUtensorMap *map, const void *base, int64_t rows, int heads, int head_dim);
 
 // Sets a kernel's dynamic shared-memory size (and, with max_carveout, the
 // preference for the whole unified L1 as shared memory) once per device;

@@ -251,7 +251,8 @@ size_t fp8kv_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads,
  *                [0, num_blocks), are read as zeros and set
  *                FP8KV_DEVERR_BAD_BLOCK.
  * max_seqlen_q:  an upper bound of the per-sequence query counts (sizes the
- *                grid; rows beyond a sequence's count do nothing).
+ *                grid and bounds the rows of q that are read, num_seqs *
+ *                max_seqlen_q; rows beyond a sequence's count do nothing).
  * rel_bias:      NULL, or device bf16; bias of query row t (global index),
  *                head h, distance d = pos_q - pos_k is
  *                rel_bias[t*bias_tok_stride + h*rel_extent + d] for
