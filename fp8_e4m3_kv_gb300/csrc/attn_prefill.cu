@@ -725,7 +725,11 @@ __device__ __forceinline__ bool pre2_next(const PrefillParams &p, const Pre2Seqs
 // offset), so that the MMA weights are p_j * v_scale_j, and the row sum adds
 // P_j / v_scale_j.  The producer writes the three per-key factors of each
 // key tile into its stage's table.
-template <bool kPT>
+// kUnfold: the bias is added to the scaled score (the q / k scales are too
+// extreme for the folded factor bias_fold); else as bias * bias_fold with the
+// score scale kept in the FMA of P.  Each is its own instantiation, so that
+// the softmax loop holds only the code it runs.
+template <bool kPT, bool kUnfold>
 __global__ void __launch_bounds__(kPre2Threads, 1)
 prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                 const __grid_constant__ CUtensorMap qmap, const PrefillParams p) {
@@ -1267,7 +1271,7 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
                         uint32_t Y[32];
                         load_bias64(bias_half ? bias_row : nullptr, d0, p.rel_extent,
                                     p.bias_vec != 0, Y);
-                        if (kPT) {
+                        if constexpr (kPT) {
                             // the scores are already in log2 units
 #pragma unroll
                             for (int e = 0; e < C::kHalf; ++e) {
@@ -1276,7 +1280,7 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
                                                                                  : (wd << 16));
                                 x[e] = fmaf(bv, kLog2eP, x[e]);
                             }
-                        } else if (p.bias_fold > 0.0f) {
+                        } else if constexpr (!kUnfold) {
                             // x + bias * log2(e) / score_log2: the score scale
                             // stays folded into the FMA of P (packed pairs;
                             // key e takes the upper half of its word for even e)
@@ -1452,12 +1456,12 @@ prefill2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
 // The register split relies on the kernel being launched with kRegsLaunch
 // registers per thread: with fewer, setmaxnreg.inc would wait for registers
 // that do not exist.  Checked once per process against the built kernel.
-template <bool kPT>
+template <bool kPT, bool kUnfold>
 bool prefill2_registers_ok() {
     static int ok = -1;
     if (ok < 0) {
         cudaFuncAttributes attr;
-        ok = (cudaFuncGetAttributes(&attr, prefill2_kernel<kPT>) == cudaSuccess &&
+        ok = (cudaFuncGetAttributes(&attr, prefill2_kernel<kPT, kUnfold>) == cudaSuccess &&
               attr.numRegs >= kRegsLaunch && attr.maxThreadsPerBlock >= kPre2Threads)
                  ? 1
                  : 0;
@@ -1469,14 +1473,15 @@ bool prefill2_registers_ok() {
 // CTAs of a persistent launch at most (0: one per SM).
 std::atomic<int> g_prefill_max_ctas{0};
 
-template <bool kPT>
+template <bool kPT, bool kUnfold>
 fp8kv_status launch_prefill2(const CUtensorMap &km, const CUtensorMap &vm, const CUtensorMap &qm,
                              const PrefillParams &p, int num_seqs, int sms, cudaStream_t stream) {
     const int cap = g_prefill_max_ctas.load(std::memory_order_relaxed);
     if (cap > 0 && cap < sms) sms = cap;
-    if (!prefill2_registers_ok<kPT>()) return FP8KV_ERR_UNSUPPORTED;
+    auto kern = prefill2_kernel<kPT, kUnfold>;
+    if (!prefill2_registers_ok<kPT, kUnfold>()) return FP8KV_ERR_UNSUPPORTED;
     static std::atomic<uint64_t> attrs_set{0};
-    if (!func_attrs_once(reinterpret_cast<const void *>(prefill2_kernel<kPT>), &attrs_set,
+    if (!func_attrs_once(reinterpret_cast<const void *>(kern), &attrs_set,
                          Pre2Cfg::kSmemBytes, false))
         return FP8KV_ERR_LAUNCH;
     // persistent: two pipelines per CTA, at most one CTA per SM
@@ -1484,7 +1489,7 @@ fp8kv_status launch_prefill2(const CUtensorMap &km, const CUtensorMap &vm, const
     const int64_t n_items = n_pairs * p.Hq * num_seqs;
     const dim3 grid = p.persist ? dim3(static_cast<unsigned>(n_items < sms ? n_items : sms))
                                 : dim3(static_cast<unsigned>(n_pairs), p.Hq, num_seqs);
-    prefill2_kernel<kPT><<<grid, kPre2Threads, Pre2Cfg::kSmemBytes, stream>>>(km, vm, qm, p);
+    kern<<<grid, kPre2Threads, Pre2Cfg::kSmemBytes, stream>>>(km, vm, qm, p);
     if (cudaGetLastError() != cudaSuccess) return FP8KV_ERR_LAUNCH;
     return FP8KV_OK;
 }
@@ -1589,9 +1594,11 @@ fp8kv_status prefill_impl(const fp8kv_cache *cache, const fp8kv_bf16 *q, int32_t
               make_rows_map(&qm, q, static_cast<int64_t>(num_seqs) * max_seqlen_q, num_q_heads, D);
     if (!p.q_tma) qm = km;   // unused
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (per_token) return launch_prefill2<true>(km, vm, qm, p, num_seqs, sms, s);
-    return D == 128 ? launch_prefill2<false>(km, vm, qm, p, num_seqs, sms, s)
-                    : launch_prefill<256>(km, vm, p, num_seqs, s);
+    if (per_token) return launch_prefill2<true, false>(km, vm, qm, p, num_seqs, sms, s);
+    if (D != 128) return launch_prefill<256>(km, vm, p, num_seqs, s);
+    const bool unfold = p.rel_extent > 0 && !(p.bias_fold > 0.0f);
+    return unfold ? launch_prefill2<false, true>(km, vm, qm, p, num_seqs, sms, s)
+                  : launch_prefill2<false, false>(km, vm, qm, p, num_seqs, sms, s);
 }
 }  // namespace
 

@@ -88,11 +88,13 @@ def test_large_bias_row_max_jumps(fk):
     run_case(fk, [600, 260], k_lens=[600, 900], E=1024, seed=7, rel_override=ramp)
 
 
-def test_bias_with_extreme_scales(fk):
+@pytest.mark.parametrize("window", [0, 100])
+def test_bias_with_extreme_scales(fk, window):
     """q and k scales of 2^-30: the kernel adds the bias unfolded (its factor
-    log2(e) / score scale would be 2^63.5); every code saturates."""
+    log2(e) / score scale would be 2^63.5; a kernel instantiation of its
+    own); every code saturates.  With and without a window."""
     run_case(fk, [200, 70], k_lens=[260, 70], scales=(2.0 ** -30, 2.0 ** -30, 1.0), E=128,
-             seed=9)
+             seed=9, window=window)
 
 
 def test_bias_broadcast_over_tokens(fk):
