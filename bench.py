@@ -89,7 +89,7 @@ def fp8_mma_probe(dev, shapes=((256, 2, 1), (128, 2, 2), (128, 1, 1), (64, 2, 2)
 # kernel sources it was taken on: once the kernel changes, the number no
 # longer describes it and is reported as null.
 DECODE_TRAFFIC = {
-    "03263abf33502aa4c3e964734357b2b49aa05b22efeb838d8ecadc79fdc84a72": 1086101632,
+    "49cf5816ab4d99e2a9b0bb5621eb089a88035d5fe97b4382a50f7b196655fb07": 1086110708,
 }
 DECODE_SOURCES = ("fp8_e4m3_kv_gb300/csrc/attn_decode.cu", "fp8_e4m3_kv_gb300/csrc/common.cuh")
 
