@@ -1107,7 +1107,8 @@ struct SplitPlan {
 // Split plan: ~8 work items per resident CTA of the persistent launch (the
 // counter hands them out, so short last items even out the tail), at least
 // 2048 keys per split and a whole number of quarter splits; the first split
-// of each sequence is then cut into quarters (below).
+// of each sequence is then cut into quarters (below).  A single sequence
+// instead takes the split length that fills whole rounds of the CTA slots.
 bool plan_splits(int32_t num_seqs, int32_t num_kv_heads, int32_t head_dim,
                  int32_t max_blocks_per_seq, int32_t block_size, int32_t window,
                  int32_t split_tokens, int num_sms, SplitPlan *plan) {
@@ -1135,14 +1136,30 @@ bool plan_splits(int32_t num_seqs, int32_t num_kv_heads, int32_t head_dim,
         const int64_t min_st = (2048 + keys - 1) / keys;
         if (st < min_st) st = min_st;
         st = (st + 3) / 4 * 4;   // whole quarters for the cut below
+        if (num_seqs == 1 && (tiles + st - 1) / st >= 2) {
+            // One sequence: every item has the same length, so take the
+            // split (up to twice as long) whose items fill whole rounds of
+            // the CTA slots best, i.e. the least rounds x split length.
+            const int64_t slots = static_cast<int64_t>(num_sms) * ctas_per_sm;
+            int64_t best = st, best_cost = -1;
+            for (int64_t c = st; c <= 2 * st; ++c) {
+                const int64_t items = pairs * ((tiles + c - 1) / c);
+                const int64_t cost = (items + slots - 1) / slots * c;
+                if (best_cost < 0 || cost < best_cost) {
+                    best = c;
+                    best_cost = cost;
+                }
+            }
+            st = best;
+        }
     }
     int64_t S = (tiles + st - 1) / st;
-    // Automatic plans with several splits: the first split of each sequence
-    // (in key order) is cut into four.  Items go out last splits first, so
-    // these are the launch's last items, and the tail ends in quarter-size
-    // pieces.
+    // Automatic plans with several splits over more than one sequence: the
+    // first split of each sequence (in key order) is cut into four.  Items go
+    // out last splits first, so these are the launch's last items, and the
+    // tail ends in quarter-size pieces.
     int64_t F = 0, ft = 0;
-    if (split_tokens <= 0 && S >= 2 && st % 4 == 0) {
+    if (split_tokens <= 0 && S >= 2 && st % 4 == 0 && num_seqs > 1) {
         F = 4;
         ft = st / 4;
         S += F - 1;
